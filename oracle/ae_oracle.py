@@ -1,0 +1,285 @@
+"""Plain float64 CPU oracle of the flow-matching action-expert denoise loop.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  The CUDA library
+never calls it, and it shares no code with the CUDA library: it reads plain
+NumPy arrays and writes plain NumPy arrays.
+
+Everything is computed in float64 with NumPy; inputs that are stored in bf16 on
+the GPU arrive here as the exact float values of those bf16 numbers.  The steps
+follow the pages in order; where the pages are silent the plainest reading is
+taken and named in the docstring of the function that takes it.
+
+Sources (page title, section):
+
+* [MolmoBot] "Inference optimization for MolmoBot VLA: torch.compile + CUDA
+  graphs + action-expert KV cache", Part 2 (the VLM runs once, the action expert
+  is integrated for ``num_steps`` Euler steps from noise; the context K/V is
+  computed once and reused by every step) and Part 1 (padded positions are
+  masked out and leave the actions unchanged).
+* [LoongForge] "How to Speed Up VLA Training Step by Step: A 3x Acceleration
+  Case Study on Pi0.5", section 1 (empty camera slots are masked; pad tokens do
+  not advance position_ids), section 2 (adaRMS: fp32, square, mean, rsqrt,
+  scale/shift/gate chunks; RoPE with rotate_half; gelu*up; gated residuals),
+  section 3 (MQA, the prefix-LM mask: prefix bidirectional, actions see every
+  valid prefix token and each other, pad rows/cols masked), section 5.3 (action
+  input projection, time MLP, action output projection).
+* [sglang] sglang PR #34599 summary, implementation items 1-2 (merged Q/K/V and
+  gate/up projections; mask, positions and sinusoidal time scaling computed once
+  per request instead of once per step).
+
+Parity status of each function is listed in ``PINS``: every function has a
+test that pins it to something other than itself, except the end-to-end action
+values, for which no page prints a worked example ("parity unpinned" for the
+end-to-end values; each of their ingredients is pinned).
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+PINS = {
+    "time_embedding": "tests/test_oracle_pins.py: unit-circle pairs, t=0 value, per-index period",
+    "time_mlp": "tests/test_oracle_pins.py: torch.nn.functional silu/linear chain",
+    "ada_rms": "tests/test_oracle_pins.py: scale=shift=0 equals torch rms_norm",
+    "rope": "tests/test_oracle_pins.py: complex-rotation form, p=0 identity, relative invariance",
+    "gelu_tanh": "tests/test_oracle_pins.py: torch gelu(approximate='tanh')",
+    "attention": "tests/test_oracle_pins.py: brute-force joint prefix-LM attention via torch SDPA",
+    "expert_layer": "tests/test_oracle_pins.py: identity modulation equals a standard pre-norm block",
+    "sample": "tests/test_oracle_pins.py: zero velocity, constant velocity closed form, pad/mask "
+              "invariance (bitwise), hoisted == recomputed (bitwise), batch independence; "
+              "end-to-end values: parity unpinned (no page prints an expected action)",
+}
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Time conditioning
+# ---------------------------------------------------------------------------
+
+def time_embedding(t: float, width: int, min_period: float, max_period: float) -> np.ndarray:
+    """Sinusoidal embedding of the flow time t, length ``width``.
+
+    [sglang] item 2 and [LoongForge] section 5.3 name a sinusoidal time scaling
+    followed by a time MLP but print neither.  Reading: ``width/2`` periods
+    spaced geometrically from ``min_period`` to ``max_period`` (inclusive);
+    the embedding is [sin(2 pi t / p_j) for all j] followed by
+    [cos(2 pi t / p_j) for all j].
+    """
+    half = width // 2
+    if half == 1:
+        frac = np.zeros(1)
+    else:
+        frac = np.arange(half, dtype=np.float64) / (half - 1)
+    period = min_period * (max_period / min_period) ** frac
+    angle = 2.0 * math.pi * float(t) / period
+    return np.concatenate([np.sin(angle), np.cos(angle)])
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def time_mlp(e: np.ndarray, w_t1, b_t1, w_t2, b_t2) -> np.ndarray:
+    """Time MLP ([LoongForge] section 5.3): c = silu(W2 silu(W1 e + b1) + b2).
+
+    Reading: two D->D Linears, each followed by SiLU; c conditions every adaRMS.
+    """
+    a = silu(_f64(w_t1) @ e + _f64(b_t1))
+    return silu(_f64(w_t2) @ a + _f64(b_t2))
+
+
+def modulation(c: np.ndarray, w_mod, b_mod, n_chunks: int) -> List[np.ndarray]:
+    """Chunk ``W_mod c + b_mod`` into ``n_chunks`` vectors of width D.
+
+    [LoongForge] section 2 chunks adaRMS's conditioning into scale, shift and
+    gate, in that order.  The final norm before the action output projection
+    has scale and shift only (no residual follows it).
+    """
+    m = _f64(w_mod) @ c + _f64(b_mod)
+    return list(np.split(m, n_chunks))
+
+
+# ---------------------------------------------------------------------------
+# Layer pieces
+# ---------------------------------------------------------------------------
+
+def ada_rms(x: np.ndarray, scale: np.ndarray, shift: np.ndarray, eps: float) -> np.ndarray:
+    """Adaptive RMSNorm ([LoongForge] section 2): x * rsqrt(mean(x^2) + eps) * (1 + scale) + shift.
+
+    Reading: no separate learned norm weight; the mean runs over the last axis.
+    """
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return x * r * (1.0 + scale) + shift
+
+
+def rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotary embedding with the rotate_half pairing ([LoongForge] section 2).
+
+    x: [..., T, dh]; positions: [T].  Pair i rotates (x[i], x[i + dh/2]) by the
+    angle positions * theta^(-2i/dh):  x*cos + rotate_half(x)*sin with
+    rotate_half(x) = [-x2, x1].
+    """
+    dh = x.shape[-1]
+    half = dh // 2
+    inv_freq = theta ** (-(2.0 * np.arange(half, dtype=np.float64)) / dh)
+    ang = _f64(positions)[:, None] * inv_freq[None, :]          # [T, half]
+    cos, sin = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
+
+
+def gelu_tanh(x: np.ndarray) -> np.ndarray:
+    """GELU, tanh approximation (the "gelu" of gelu*up, [LoongForge] section 2)."""
+    return 0.5 * x * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
+
+
+def attention(q: np.ndarray, k_all: np.ndarray, v_all: np.ndarray) -> np.ndarray:
+    """Action-row attention of one request under the prefix-LM mask.
+
+    q: [Hq, H, dh] action queries.  k_all, v_all: [Hkv, n + H, dh] = the request's
+    VALID prefix rows (in order) followed by its H action rows.  Per
+    [LoongForge] section 3, action rows see every valid prefix token and every
+    action token (including themselves), so the key set is exactly the rows
+    passed in: masked and padded prefix rows are excluded from the set, not
+    added with -inf.  Query head h reads KV head h // (Hq / Hkv) (MQA/GQA).
+    Scale 1/sqrt(dh) (the pages are silent; the standard choice).
+    """
+    hq, _, dh = q.shape
+    group = hq // k_all.shape[0]
+    out = np.empty_like(q)
+    for h in range(hq):
+        kh, vh = k_all[h // group], v_all[h // group]
+        s = (q[h] @ kh.T) / math.sqrt(dh)                       # [H, n + H]
+        s = s - s.max(axis=-1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=-1, keepdims=True)
+        out[h] = p @ vh
+    return out
+
+
+def expert_layer(h: np.ndarray, mods1, mods2, w: Dict, l: int, kp: np.ndarray, vp: np.ndarray,
+                 positions: np.ndarray, dims, trace: Optional[Dict] = None) -> np.ndarray:
+    """One Gemma-style action-expert layer on the H action rows of one request.
+
+    h: [H, D] residual stream.  kp, vp: [n, Hkv*dh] valid prefix rows of layer l
+    (prefix K is already rotated at the VLM's own positions and is not re-roped).
+    Steps ([LoongForge] section 2; merged projections per [sglang] item 1 are
+    a layout choice and compute the same q, k, v and gate/up):
+      y = adaRMS1(h); q,k,v = y Wq^T, y Wk^T, y Wv^T; RoPE(q, k) at positions;
+      o = attention; h += gate1 * (o Wo^T);
+      y2 = adaRMS2(h); h += gate2 * ((gelu_tanh(y2 Wg^T) * (y2 Wu^T)) Wd^T).
+    """
+    H, D = h.shape
+    hq, hkv, dh = dims.n_q_heads, dims.n_kv_heads, dims.head_dim
+    s1, sh1, g1 = mods1
+    s2, sh2, g2 = mods2
+    y = ada_rms(h, s1, sh1, dims.rms_eps)
+    q = (y @ _f64(w["wq"][l]).T).reshape(H, hq, dh).transpose(1, 0, 2)
+    k = (y @ _f64(w["wk"][l]).T).reshape(H, hkv, dh).transpose(1, 0, 2)
+    v = (y @ _f64(w["wv"][l]).T).reshape(H, hkv, dh).transpose(1, 0, 2)
+    q = rope(q, positions, dims.rope_theta)
+    k = rope(k, positions, dims.rope_theta)
+    n = kp.shape[0]
+    k_all = np.concatenate([_f64(kp).reshape(n, hkv, dh).transpose(1, 0, 2), k], axis=1)
+    v_all = np.concatenate([_f64(vp).reshape(n, hkv, dh).transpose(1, 0, 2), v], axis=1)
+    o = attention(q, k_all, v_all).transpose(1, 0, 2).reshape(H, hq * dh)
+    if trace is not None:
+        trace.update(y=y, q=q, k=k, v=v, o=o)
+    h = h + g1 * (o @ _f64(w["wo"][l]).T)
+    y2 = ada_rms(h, s2, sh2, dims.rms_eps)
+    m = gelu_tanh(y2 @ _f64(w["wg"][l]).T) * (y2 @ _f64(w["wu"][l]).T)
+    if trace is not None:
+        trace.update(y2=y2, m=m)
+    return h + g2 * (m @ _f64(w["wd"][l]).T)
+
+
+# ---------------------------------------------------------------------------
+# Binding and the denoise loop
+# ---------------------------------------------------------------------------
+
+def bind_request(prefix_k, prefix_v, mask, row0: int, row1: int):
+    """Valid prefix rows of one request, in physical order, for every layer.
+
+    [LoongForge] section 1: masked camera slots and pads are invisible and do
+    not advance positions, so a request's prefix is its valid rows in order and
+    its action token i sits at position n_valid + i ([LoongForge] section 3:
+    actions follow the prefix).  Returns (K [L, n, kv], V [L, n, kv], n).
+    """
+    if mask is None:
+        idx = np.arange(row0, row1)
+    else:
+        idx = row0 + np.nonzero(np.asarray(mask[row0:row1]))[0]
+    return prefix_k[:, idx, :], prefix_v[:, idx, :], int(idx.size)
+
+
+def step_times(n_steps: int) -> List[float]:
+    """Euler schedule: n_steps steps of delta = -1/n_steps from t = 1.
+
+    [MolmoBot] Part 2 integrates ``num_steps`` Euler steps from noise at t=1.
+    Reading: the velocity of step k is evaluated at t_k = 1 - k/n_steps
+    (k = 0..n_steps-1), in float64.
+    """
+    return [1.0 - k / n_steps for k in range(n_steps)]
+
+
+def sample(dims, w: Dict, prefix_k, prefix_v, cu_lens, mask, noise, n_steps: int,
+           hoist: bool = True, dump: Optional[np.ndarray] = None) -> np.ndarray:
+    """Integrate the action chunk of every request from ``noise`` for ``n_steps`` Euler steps.
+
+    prefix_k, prefix_v: [L, total_rows, Hkv*dh]; cu_lens: [B+1] physical row
+    offsets; mask: [total_rows] (1 = valid) or None; noise: [B, H, A].
+    Each step: h = x W_in^T + b_in; L expert layers; v = adaRMS_f(h) W_out^T
+    + b_out; x <- x + delta * v with delta = -1/n_steps ([MolmoBot] Part 2).
+
+    ``hoist=True`` computes the request binding (valid rows, positions) and
+    each step's time conditioning once, as [MolmoBot] Part 2 and [sglang]
+    item 2 do; ``hoist=False`` recomputes them inside every step and layer.
+    The two must agree bitwise.  ``dump`` (optional, [S, L+1, B, H, D]) receives
+    the residual stream entering each layer and leaving the last one.
+    Requests are processed one at a time: request b's result does not depend
+    on the others.
+    """
+    B = len(cu_lens) - 1
+    x_all = _f64(noise).copy()
+    delta = -1.0 / n_steps
+    times = step_times(n_steps)
+    L = dims.layers
+    D, H = dims.width, dims.horizon
+
+    def cond(t):
+        e = time_embedding(t, D, dims.time_min_period, dims.time_max_period)
+        return time_mlp(e, w["w_t1"], w["b_t1"], w["w_t2"], w["b_t2"])
+
+    hoisted_c = [cond(t) for t in times] if hoist else None
+    for b in range(B):
+        r0, r1 = int(cu_lens[b]), int(cu_lens[b + 1])
+        if hoist:
+            kp, vp, n = bind_request(prefix_k, prefix_v, mask, r0, r1)
+            positions = n + np.arange(H, dtype=np.float64)
+        x = x_all[b]
+        for s, t in enumerate(times):
+            c = hoisted_c[s] if hoist else cond(t)
+            h = x @ _f64(w["w_in"]).T + _f64(w["b_in"])
+            for l in range(L):
+                if dump is not None:
+                    dump[s, l, b] = h
+                if not hoist:
+                    kp, vp, n = bind_request(prefix_k, prefix_v, mask, r0, r1)
+                    positions = n + np.arange(H, dtype=np.float64)
+                    c = cond(t)
+                m1 = modulation(c, w["w_mod1"][l], w["b_mod1"][l], 3)
+                m2 = modulation(c, w["w_mod2"][l], w["b_mod2"][l], 3)
+                h = expert_layer(h, m1, m2, w, l, kp[l], vp[l], positions, dims)
+            if dump is not None:
+                dump[s, L, b] = h
+            sf, shf = modulation(c, w["w_mod_f"], w["b_mod_f"], 2)
+            v = ada_rms(h, sf, shf, dims.rms_eps) @ _f64(w["w_out"]).T + _f64(w["b_out"])
+            x = x + delta * v
+        x_all[b] = x
+    return x_all
