@@ -1,0 +1,398 @@
+// C-ABI entry points and host runtime: argument checks, the weight packer,
+// the prefix binder, the per-n_steps time-conditioning table, and the step
+// loop.  No compute happens on the host; every step of the path is a kernel.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "ae_internal.h"
+
+using ae::Dims;
+using ae::TimeTable;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+ae_status set_msg(ae_ctx* c, ae_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c != nullptr) c->last_msg = buf;
+  else g_create_error = buf;
+  return st;
+}
+
+ae_status cuda_fail(ae_ctx* c, cudaError_t e, const char* what) {
+  const ae_status st = (e == cudaErrorMemoryAllocation) ? AE_ERR_OOM : AE_ERR_CUDA;
+  return set_msg(c, st, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define AE_CK(c, expr)                                 \
+  do {                                                 \
+    cudaError_t e_ = (expr);                           \
+    if (e_ != cudaSuccess) return cuda_fail(c, e_, #expr); \
+  } while (0)
+
+size_t elem_size(int dtype) { return dtype == AE_DTYPE_BF16 ? 2 : 4; }
+
+template <typename P>
+ae_status alloc(ae_ctx* c, P** p, size_t bytes) {
+  void* q = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMalloc");
+  c->allocations.push_back(q);
+  c->device_bytes += (int64_t)bytes;
+  *p = (P*)q;
+  return AE_OK;
+}
+
+#define AE_TRY(expr)                 \
+  do {                               \
+    ae_status s_ = (expr);           \
+    if (s_ != AE_OK) return s_;      \
+  } while (0)
+
+ae_status check_config(const ae_config* cfg) {
+  if (cfg->layers <= 0 || cfg->width <= 0 || cfg->mlp <= 0 || cfg->n_q_heads <= 0 ||
+      cfg->n_kv_heads <= 0 || cfg->head_dim <= 0 || cfg->action_dim <= 0 || cfg->horizon <= 0)
+    return set_msg(nullptr, AE_ERR_INVALID_ARG, "every dimension must be positive");
+  if (cfg->dtype != AE_DTYPE_BF16 && cfg->dtype != AE_DTYPE_F32)
+    return set_msg(nullptr, AE_ERR_INVALID_ARG, "dtype must be AE_DTYPE_BF16 or AE_DTYPE_F32");
+  if (cfg->n_q_heads % cfg->n_kv_heads != 0)
+    return set_msg(nullptr, AE_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
+  if (cfg->head_dim % 32 != 0 || cfg->head_dim > 256)
+    return set_msg(nullptr, AE_ERR_SHAPE, "head_dim must be a multiple of 32 and <= 256");
+  if (cfg->width % 32 != 0 || cfg->mlp % 32 != 0)
+    return set_msg(nullptr, AE_ERR_SHAPE, "width and mlp must be multiples of 32");
+  if (!(cfg->rms_eps > 0.0) || !(cfg->rope_theta > 0.0) || !(cfg->time_min_period > 0.0) ||
+      !(cfg->time_max_period > 0.0))
+    return set_msg(nullptr, AE_ERR_INVALID_ARG, "eps, rope_theta and time periods must be > 0");
+  return AE_OK;
+}
+
+ae_status check_weights(const ae_config* cfg, const ae_weights* w) {
+  const void* globals[] = {w->w_in, w->b_in, w->w_t1, w->b_t1, w->w_t2,
+                           w->b_t2, w->w_mod_f, w->b_mod_f, w->w_out, w->b_out};
+  for (const void* p : globals)
+    if (p == nullptr) return set_msg(nullptr, AE_ERR_INVALID_ARG, "a global weight pointer is NULL");
+  const void* const* per[] = {w->wq, w->wk, w->wv, w->wo, w->wg, w->wu,
+                              w->wd, w->w_mod1, w->b_mod1, w->w_mod2, w->b_mod2};
+  for (const void* const* arr : per) {
+    if (arr == nullptr) return set_msg(nullptr, AE_ERR_INVALID_ARG, "a per-layer weight array is NULL");
+    for (int l = 0; l < cfg->layers; ++l)
+      if (arr[l] == nullptr)
+        return set_msg(nullptr, AE_ERR_INVALID_ARG, "per-layer weight pointer of layer %d is NULL", l);
+  }
+  return AE_OK;
+}
+
+// Copy one caller tensor into library memory (device or host source).
+ae_status put(ae_ctx* c, void* dst, const void* src, size_t bytes) {
+  AE_CK(c, cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, c->stream));
+  return AE_OK;
+}
+
+// The weight packer: library-owned copies; Q/K/V rows and gate/up rows are
+// merged into one matrix each (sglang PR #34599 item 1), every layer's two
+// modulation Linears into one [2 * 3D, D] block.
+ae_status pack_weights(ae_ctx* c, const ae_weights* w) {
+  const Dims& d = c->d;
+  const size_t es = elem_size(d.dtype);
+  const size_t D = d.D, F = d.F, A = d.A, L = d.L;
+  const size_t qd = d.qdim(), kvd = d.kvdim(), nqkv = d.qkvdim();
+  AE_TRY(alloc(c, &c->w_in, D * A * es));
+  AE_TRY(alloc(c, &c->b_in, D * es));
+  AE_TRY(alloc(c, &c->w_t1, D * D * es));
+  AE_TRY(alloc(c, &c->b_t1, D * es));
+  AE_TRY(alloc(c, &c->w_t2, D * D * es));
+  AE_TRY(alloc(c, &c->b_t2, D * es));
+  AE_TRY(alloc(c, &c->w_modf, 2 * D * D * es));
+  AE_TRY(alloc(c, &c->b_modf, 2 * D * es));
+  AE_TRY(alloc(c, &c->w_out, A * D * es));
+  AE_TRY(alloc(c, &c->b_out, A * es));
+  AE_TRY(alloc(c, &c->w_qkv, L * nqkv * D * es));
+  AE_TRY(alloc(c, &c->w_o, L * D * qd * es));
+  AE_TRY(alloc(c, &c->w_gu, L * 2 * F * D * es));
+  AE_TRY(alloc(c, &c->w_d, L * D * F * es));
+  AE_TRY(alloc(c, &c->w_mod, L * 2 * 3 * D * D * es));
+  AE_TRY(alloc(c, &c->b_mod, L * 2 * 3 * D * es));
+  AE_TRY(put(c, c->w_in, w->w_in, D * A * es));
+  AE_TRY(put(c, c->b_in, w->b_in, D * es));
+  AE_TRY(put(c, c->w_t1, w->w_t1, D * D * es));
+  AE_TRY(put(c, c->b_t1, w->b_t1, D * es));
+  AE_TRY(put(c, c->w_t2, w->w_t2, D * D * es));
+  AE_TRY(put(c, c->b_t2, w->b_t2, D * es));
+  AE_TRY(put(c, c->w_modf, w->w_mod_f, 2 * D * D * es));
+  AE_TRY(put(c, c->b_modf, w->b_mod_f, 2 * D * es));
+  AE_TRY(put(c, c->w_out, w->w_out, A * D * es));
+  AE_TRY(put(c, c->b_out, w->b_out, A * es));
+  char* qkv = (char*)c->w_qkv;
+  char* gu = (char*)c->w_gu;
+  char* wmod = (char*)c->w_mod;
+  char* bmod = (char*)c->b_mod;
+  for (size_t l = 0; l < L; ++l) {
+    char* q = qkv + l * nqkv * D * es;
+    AE_TRY(put(c, q, w->wq[l], qd * D * es));
+    AE_TRY(put(c, q + qd * D * es, w->wk[l], kvd * D * es));
+    AE_TRY(put(c, q + (qd + kvd) * D * es, w->wv[l], kvd * D * es));
+    AE_TRY(put(c, (char*)c->w_o + l * D * qd * es, w->wo[l], D * qd * es));
+    char* g = gu + l * 2 * F * D * es;
+    AE_TRY(put(c, g, w->wg[l], F * D * es));
+    AE_TRY(put(c, g + F * D * es, w->wu[l], F * D * es));
+    AE_TRY(put(c, (char*)c->w_d + l * D * F * es, w->wd[l], D * F * es));
+    AE_TRY(put(c, wmod + (l * 2 + 0) * 3 * D * D * es, w->w_mod1[l], 3 * D * D * es));
+    AE_TRY(put(c, wmod + (l * 2 + 1) * 3 * D * D * es, w->w_mod2[l], 3 * D * D * es));
+    AE_TRY(put(c, bmod + (l * 2 + 0) * 3 * D * es, w->b_mod1[l], 3 * D * es));
+    AE_TRY(put(c, bmod + (l * 2 + 1) * 3 * D * es, w->b_mod2[l], 3 * D * es));
+  }
+  return AE_OK;
+}
+
+ae_status alloc_scratch(ae_ctx* c) {
+  const Dims& d = c->d;
+  const size_t es = elem_size(d.dtype);
+  const size_t M = (size_t)c->max_batch * d.H;
+  AE_TRY(alloc(c, &c->h, M * d.D * sizeof(float)));
+  AE_TRY(alloc(c, &c->y, M * d.D * es));
+  AE_TRY(alloc(c, &c->qkv_f, M * d.qkvdim() * sizeof(float)));
+  AE_TRY(alloc(c, &c->qkv, M * d.qkvdim() * es));
+  AE_TRY(alloc(c, &c->o, M * d.qdim() * es));
+  AE_TRY(alloc(c, &c->gu_f, M * 2 * d.F * sizeof(float)));
+  AE_TRY(alloc(c, &c->m, M * d.F * es));
+  AE_TRY(alloc(c, &c->valid_idx, (size_t)c->max_batch * (c->max_rows > 0 ? c->max_rows : 1) * sizeof(int)));
+  AE_TRY(alloc(c, &c->n_valid, (size_t)c->max_batch * sizeof(int)));
+  AE_TRY(alloc(c, &c->rope_cs, (size_t)c->max_batch * d.H * (d.dh / 2) * sizeof(float2)));
+  return AE_OK;
+}
+
+void free_all(ae_ctx* c) {
+  for (void* p : c->allocations) cudaFree(p);
+  c->allocations.clear();
+  if (c->status_host) cudaFreeHost(c->status_host);
+  c->status_host = nullptr;
+}
+
+ae_status get_table(ae_ctx* c, int n_steps, const TimeTable** out) {
+  for (const TimeTable& t : c->tables)
+    if (t.n_steps == n_steps) {
+      *out = &t;
+      return AE_OK;
+    }
+  const Dims& d = c->d;
+  TimeTable t;
+  t.n_steps = n_steps;
+  const size_t S = n_steps, D = d.D, L = d.L;
+  AE_TRY(alloc(c, &t.mod, S * L * 2 * 3 * D * sizeof(float)));
+  AE_TRY(alloc(c, &t.fin, S * 2 * D * sizeof(float)));
+  AE_TRY(alloc(c, &t.act, S * 2 * D * sizeof(float)));
+  AE_TRY(alloc(c, &t.c, S * D * sizeof(float)));
+  ae::launch_time_table(c, t, c->stream);
+  AE_CK(c, cudaGetLastError());
+  c->tables.push_back(t);
+  *out = &c->tables.back();
+  return AE_OK;
+}
+
+ae_status sticky(const ae_ctx* c) {
+  const int code = c->status_host ? *(volatile int*)c->status_host : 0;
+  return code != 0 ? AE_ERR_DEVICE : AE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ae_status_string(ae_status s) {
+  switch (s) {
+    case AE_OK: return "AE_OK";
+    case AE_ERR_INVALID_ARG: return "AE_ERR_INVALID_ARG";
+    case AE_ERR_SHAPE: return "AE_ERR_SHAPE";
+    case AE_ERR_NOT_BOUND: return "AE_ERR_NOT_BOUND";
+    case AE_ERR_CUDA: return "AE_ERR_CUDA";
+    case AE_ERR_DEVICE: return "AE_ERR_DEVICE";
+    case AE_ERR_OOM: return "AE_ERR_OOM";
+    case AE_ERR_UNSUPPORTED: return "AE_ERR_UNSUPPORTED";
+  }
+  return "AE_ERR_UNKNOWN";
+}
+
+ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
+                    int max_prefix_rows, void* stream, ae_ctx** out) {
+  if (out != nullptr) *out = nullptr;
+  if (cfg == nullptr || w == nullptr || out == nullptr)
+    return set_msg(nullptr, AE_ERR_INVALID_ARG, "cfg, w and out must be non-NULL");
+  AE_TRY(check_config(cfg));
+  AE_TRY(check_weights(cfg, w));
+  if (max_batch < 1 || max_batch > AE_MAX_BATCH)
+    return set_msg(nullptr, AE_ERR_SHAPE, "max_batch must be in 1..%d", AE_MAX_BATCH);
+  if (max_prefix_rows < 0)
+    return set_msg(nullptr, AE_ERR_SHAPE, "max_prefix_rows must be >= 0");
+
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess)
+    return set_msg(nullptr, AE_ERR_UNSUPPORTED, "no usable CUDA device: %s", cudaGetErrorString(e));
+  if (major != 10 || minor != 3)
+    return set_msg(nullptr, AE_ERR_UNSUPPORTED,
+                   "built for sm_103a; the current device is compute capability %d.%d", major, minor);
+
+  ae_ctx* c = new ae_ctx();
+  c->d = Dims{cfg->layers, cfg->width, cfg->mlp, cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim,
+              cfg->action_dim, cfg->horizon, cfg->rms_eps, cfg->rope_theta,
+              cfg->time_min_period, cfg->time_max_period, cfg->dtype};
+  c->max_batch = max_batch;
+  c->max_rows = max_prefix_rows;
+  c->stream = (cudaStream_t)stream;
+  c->device = dev;
+  c->sm_count = sms;
+  ae_status st = AE_OK;
+  e = cudaHostAlloc((void**)&c->status_host, sizeof(int), cudaHostAllocMapped);
+  if (e == cudaSuccess) {
+    *c->status_host = 0;
+    e = cudaHostGetDevicePointer((void**)&c->status_dev, c->status_host, 0);
+  }
+  if (e != cudaSuccess) st = cuda_fail(c, e, "status word");
+  if (st == AE_OK) st = pack_weights(c, w);
+  if (st == AE_OK) st = alloc_scratch(c);
+  if (st == AE_OK) {
+    e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) st = cuda_fail(c, e, "weight copies");
+  }
+  if (st != AE_OK) {
+    g_create_error = c->last_msg;
+    free_all(c);
+    delete c;
+    return st;
+  }
+  *out = c;
+  return AE_OK;
+}
+
+void ae_destroy(ae_ctx* c) {
+  if (c == nullptr) return;
+  cudaStreamSynchronize(c->stream);
+  free_all(c);
+  delete c;
+}
+
+ae_status ae_set_stream(ae_ctx* c, void* stream) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  c->stream = (cudaStream_t)stream;
+  return AE_OK;
+}
+
+ae_status ae_bind_prefix(ae_ctx* c, int batch, const void* prefix_k, const void* prefix_v,
+                         const int32_t* cu_lens, const uint8_t* prefix_mask) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  if (batch < 0 || batch > c->max_batch)
+    return set_msg(c, AE_ERR_SHAPE, "batch %d outside 0..%d", batch, c->max_batch);
+  if (batch > 0 && cu_lens == nullptr) return set_msg(c, AE_ERR_INVALID_ARG, "cu_lens is NULL");
+  ae::BindArgs a;
+  memset(&a, 0, sizeof(a));
+  a.batch = batch;
+  if (batch > 0) {
+    if (cu_lens[0] != 0) return set_msg(c, AE_ERR_SHAPE, "cu_lens[0] must be 0");
+    for (int b = 0; b < batch; ++b) {
+      const int64_t len = (int64_t)cu_lens[b + 1] - cu_lens[b];
+      if (len < 0) return set_msg(c, AE_ERR_SHAPE, "cu_lens decreases at request %d", b);
+      if (len > c->max_rows)
+        return set_msg(c, AE_ERR_SHAPE, "request %d has %lld prefix rows > max_prefix_rows %d", b,
+                       (long long)len, c->max_rows);
+    }
+  }
+  const int64_t total = batch > 0 ? cu_lens[batch] : 0;
+  if (total > 0 && (prefix_k == nullptr || prefix_v == nullptr))
+    return set_msg(c, AE_ERR_INVALID_ARG, "prefix_k / prefix_v is NULL");
+  for (int b = 0; b <= batch; ++b) a.cu[b] = batch > 0 ? cu_lens[b] : 0;
+  a.max_rows = c->max_rows;
+  a.mask = prefix_mask;
+  a.valid_idx = c->valid_idx;
+  a.n_valid = c->n_valid;
+  a.rope_cs = c->rope_cs;
+  a.H = c->d.H;
+  a.half_dh = c->d.dh / 2;
+  a.theta = c->d.theta;
+  a.status = c->status_dev;
+  c->launches_bind = ae::launch_bind(a, c->stream);
+  AE_CK(c, cudaGetLastError());
+  c->bind.batch = batch;
+  c->bind.pk = prefix_k;
+  c->bind.pv = prefix_v;
+  c->bind.total_rows = total;
+  c->bind.cu.assign(a.cu, a.cu + batch + 1);
+  return AE_OK;
+}
+
+ae_status ae_sample(ae_ctx* c, const float* noise, int n_steps, float* out) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  if (c->bind.batch < 0) return set_msg(c, AE_ERR_NOT_BOUND, "ae_sample before ae_bind_prefix");
+  if (n_steps < 1 || n_steps > AE_MAX_STEPS)
+    return set_msg(c, AE_ERR_SHAPE, "n_steps %d outside 1..%d", n_steps, AE_MAX_STEPS);
+  const int B = c->bind.batch;
+  if (B > 0 && (noise == nullptr || out == nullptr))
+    return set_msg(c, AE_ERR_INVALID_ARG, "noise / out_actions is NULL");
+  if (sticky(c) != AE_OK)
+    return set_msg(c, AE_ERR_DEVICE, "a device-side check failed earlier (code %d)", *c->status_host);
+  const Dims& d = c->d;
+  if (c->dump != nullptr) {
+    const size_t need = (size_t)n_steps * (d.L + 1) * B * d.H * d.D;
+    if (need > c->dump_cap)
+      return set_msg(c, AE_ERR_SHAPE, "debug dump holds %zu floats, needs %zu", c->dump_cap, need);
+  }
+  c->launches_sample = 0;
+  if (B == 0) return AE_OK;
+  const TimeTable* t = nullptr;
+  AE_TRY(get_table(c, n_steps, &t));
+  const size_t xbytes = (size_t)B * d.H * d.A * sizeof(float);
+  if (out != noise) AE_CK(c, cudaMemcpyAsync(out, noise, xbytes, cudaMemcpyDeviceToDevice, c->stream));
+  int64_t n = 0;
+  for (int s = 0; s < n_steps; ++s) n += ae::launch_step_simt(c, *t, s, out, c->stream);
+  c->launches_sample = n;
+  AE_CK(c, cudaGetLastError());
+  return AE_OK;
+}
+
+ae_status ae_set_debug_dump(ae_ctx* c, float* hidden, size_t capacity) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  c->dump = hidden;
+  c->dump_cap = hidden ? capacity : 0;
+  return AE_OK;
+}
+
+ae_status ae_synchronize(ae_ctx* c) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  AE_CK(c, cudaStreamSynchronize(c->stream));
+  if (sticky(c) != AE_OK)
+    return set_msg(c, AE_ERR_DEVICE, "device-side check failed (code %d)", *c->status_host);
+  return AE_OK;
+}
+
+ae_status ae_last_error(const ae_ctx* c, char* buf, size_t n) {
+  const std::string& m = c ? c->last_msg : g_create_error;
+  if (buf != nullptr && n > 0) {
+    const size_t k = m.size() < n - 1 ? m.size() : n - 1;
+    memcpy(buf, m.data(), k);
+    buf[k] = '\0';
+  }
+  return c ? sticky(c) : AE_OK;
+}
+
+ae_status ae_get_info(const ae_ctx* c, ae_info* info) {
+  if (c == nullptr || info == nullptr) return AE_ERR_INVALID_ARG;
+  info->launches_last_sample = c->launches_sample;
+  info->launches_last_bind = c->launches_bind;
+  info->device_bytes = c->device_bytes;
+  info->sm_count = c->sm_count;
+  info->path = c->d.dtype == AE_DTYPE_BF16 ? 1 : 0;
+  return AE_OK;
+}
+
+}  // extern "C"

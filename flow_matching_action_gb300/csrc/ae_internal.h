@@ -1,0 +1,127 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/ae.h"
+
+namespace ae {
+
+typedef __nv_bfloat16 bf16;
+
+// Device-side error codes written to the context's status word.
+enum DeviceError : int {
+  kDevOk = 0,
+  kDevBounds = 1,   // an index failed its bounds check; the access was skipped
+  kDevTimeout = 2,  // a bounded wait gave up
+};
+
+struct Dims {
+  int L, D, F, Hq, Hkv, dh, A, H;
+  double eps, theta, tmin, tmax;
+  int dtype;
+  int qdim() const { return Hq * dh; }
+  int kvdim() const { return Hkv * dh; }
+  int qkvdim() const { return (Hq + 2 * Hkv) * dh; }
+};
+
+// adaRMS modulation table for one n_steps: every (step, layer, norm) triple of
+// (scale, shift, gate) vectors plus the final norm's (scale, shift).
+struct TimeTable {
+  int n_steps = 0;
+  float* mod = nullptr;  // [S][L][2][3D]
+  float* fin = nullptr;  // [S][2D]
+  float* act = nullptr;  // [S][2][D] sinusoid / hidden of the time MLP (scratch)
+  float* c = nullptr;    // [S][D] time-MLP output
+};
+
+struct BindState {
+  int batch = -1;                       // -1: nothing bound
+  const void* pk = nullptr;             // borrowed prefix K
+  const void* pv = nullptr;             // borrowed prefix V
+  int64_t total_rows = 0;               // rows per layer of pk / pv
+  std::vector<int> cu;                  // host copy of cu_lens
+};
+
+}  // namespace ae
+
+struct ae_ctx {
+  ae::Dims d;
+  int max_batch = 0, max_rows = 0;
+  cudaStream_t stream = nullptr;
+  int device = 0, sm_count = 0;
+
+  // Library-owned weights (type T = bf16 or float per d.dtype).
+  void* w_in = nullptr;   // [D, A]
+  void* b_in = nullptr;   // [D]
+  void* w_t1 = nullptr;   // [D, D]
+  void* b_t1 = nullptr;
+  void* w_t2 = nullptr;
+  void* b_t2 = nullptr;
+  void* w_modf = nullptr; // [2D, D]
+  void* b_modf = nullptr; // [2D]
+  void* w_out = nullptr;  // [A, D]
+  void* b_out = nullptr;  // [A]
+  void* w_qkv = nullptr;  // [L][(Hq+2Hkv)dh, D]  rows: q heads | k heads | v heads
+  void* w_o = nullptr;    // [L][D, Hq dh]
+  void* w_gu = nullptr;   // [L][2F, D]           rows: gate | up
+  void* w_d = nullptr;    // [L][D, F]
+  void* w_mod = nullptr;  // [L][2][3D, D]
+  void* b_mod = nullptr;  // [L][2][3D]
+
+  // Scratch, sized for max_batch * H rows.
+  float* h = nullptr;        // [M, D]    residual stream
+  void* y = nullptr;         // [M, D]    T, normalized + modulated activations
+  float* qkv_f = nullptr;    // [M, qkv]  fp32 projection output
+  void* qkv = nullptr;       // [M, qkv]  T, after RoPE
+  void* o = nullptr;         // [M, Hq dh] T, attention output
+  float* gu_f = nullptr;     // [M, 2F]   fp32 gate/up output
+  void* m = nullptr;         // [M, F]    T, GeGLU output
+
+  // Bind tables.
+  int* valid_idx = nullptr;  // [max_batch][max_rows] physical row of each valid row
+  int* n_valid = nullptr;    // [max_batch]
+  float2* rope_cs = nullptr; // [max_batch][H][dh/2] (cos, sin) at the action positions
+  ae::BindState bind;
+
+  std::vector<ae::TimeTable> tables;
+
+  // Sticky device status: host-mapped so it can be read without a sync.
+  int* status_host = nullptr;
+  int* status_dev = nullptr;
+
+  float* dump = nullptr;
+  size_t dump_cap = 0;
+
+  int64_t launches_sample = 0, launches_bind = 0, device_bytes = 0;
+  std::vector<void*> allocations;
+  std::string last_msg;
+};
+
+namespace ae {
+
+// Parameters of the bind kernel; cu_lens travel by value with the launch.
+struct BindArgs {
+  int batch;
+  int max_rows;
+  int cu[AE_MAX_BATCH + 1];
+  const uint8_t* mask;
+  int* valid_idx;
+  int* n_valid;
+  float2* rope_cs;
+  int H, half_dh;
+  double theta;
+  int* status;
+};
+
+// Launch wrappers (ae_simt.cu).  Each returns the number of kernels it enqueued.
+int launch_bind(const BindArgs& a, cudaStream_t s);
+int launch_time_table(const ae_ctx* c, TimeTable& t, cudaStream_t s);
+int launch_step_simt(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s);
+
+}  // namespace ae

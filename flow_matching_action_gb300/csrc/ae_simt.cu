@@ -1,0 +1,438 @@
+// Plain SIMT kernels of the denoise loop: the fp32 path (AE_DTYPE_F32, the
+// debug build whose results sit within 1e-4 of the oracle) and the bind and
+// time-conditioning kernels both paths share.
+//
+// Each kernel computes one step of the expert layer as the LoongForge Pi0.5
+// blog (section 2) lists them: adaRMS, the merged Q/K/V projection, RoPE,
+// attention over [valid prefix || actions], gated residuals, gate/up GeGLU.
+// Accumulation is fp32 throughout; storage type T is float or bf16.
+#include <math.h>
+
+#include "ae_internal.h"
+
+namespace ae {
+namespace {
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ void report(int* status, int code) {
+  if (status != nullptr) *(volatile int*)status = code;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum over the block (blockDim.x a multiple of 32, <= 1024); result in every thread.
+__device__ float block_sum(float v) {
+  __shared__ float part[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) part[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < nw; ++w) t += part[w];
+  return t;
+}
+
+// ---------------------------------------------------------------- bind
+// Valid-row compaction and the RoPE table of the action positions.  Masked
+// rows are dropped and do not advance positions (LoongForge section 1), so
+// action token i of request b sits at position n_b + i.
+__global__ void k_bind(BindArgs a) {
+  const int b = blockIdx.x;
+  const int r0 = a.cu[b], r1 = a.cu[b + 1];
+  __shared__ int warp_cnt[32];
+  __shared__ int s_base;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) s_base = 0;
+  __syncthreads();
+  for (int start = r0; start < r1; start += blockDim.x) {
+    const int r = start + threadIdx.x;
+    const bool valid = r < r1 && (a.mask == nullptr || a.mask[r] != 0);
+    const unsigned bal = __ballot_sync(0xffffffffu, valid);
+    if (lane == 0) warp_cnt[warp] = __popc(bal);
+    __syncthreads();
+    int off = s_base;
+    for (int w = 0; w < warp; ++w) off += warp_cnt[w];
+    off += __popc(bal & ((1u << lane) - 1u));
+    if (valid) {
+      if (off < a.max_rows) a.valid_idx[(size_t)b * a.max_rows + off] = r;
+      else report(a.status, kDevBounds);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int w = 0; w < nw; ++w) tot += warp_cnt[w];
+      s_base += tot;
+    }
+    __syncthreads();
+  }
+  const int n = s_base;
+  if (threadIdx.x == 0) a.n_valid[b] = n;
+  const int dh = 2 * a.half_dh;
+  for (int e = threadIdx.x; e < a.H * a.half_dh; e += blockDim.x) {
+    const int i = e / a.half_dh, j = e - i * a.half_dh;
+    const double inv_freq = pow(a.theta, -2.0 * (double)j / (double)dh);
+    double sn, cs;
+    sincos((double)(n + i) * inv_freq, &sn, &cs);
+    a.rope_cs[((size_t)b * a.H + i) * a.half_dh + j] = make_float2((float)cs, (float)sn);
+  }
+}
+
+// ---------------------------------------------------------------- time table
+// Sinusoidal embedding of t_s = 1 - s/S: width/2 geometric periods from tmin
+// to tmax, sines then cosines.
+__global__ void k_time_embed(float* e, int S, int D, double tmin, double tmax) {
+  const int half = D / 2;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= S * half) return;
+  const int s = idx / half, j = idx - s * half;
+  const double t = 1.0 - (double)s / (double)S;
+  const double frac = half == 1 ? 0.0 : (double)j / (double)(half - 1);
+  const double period = tmin * pow(tmax / tmin, frac);
+  double sn, cs;
+  sincos(2.0 * 3.14159265358979323846 * t / period, &sn, &cs);
+  e[(size_t)s * D + j] = (float)sn;
+  e[(size_t)s * D + half + j] = (float)cs;
+}
+
+// ---------------------------------------------------------------- GEMM
+// C[m, n] = sum_k A[m, k] * W[n, k] with a per-element epilogue.
+// 64x64 output tile per 256-thread block, K in steps of 32, fp32 accumulate in
+// increasing k.
+template <typename TA, typename TW, typename Epi>
+__global__ void __launch_bounds__(256) k_gemm(int M, int N, int K, const TA* __restrict__ A,
+                                              long lda, const TW* __restrict__ W, long ldw,
+                                              Epi epi) {
+  __shared__ float As[32][65];
+  __shared__ float Ws[32][65];
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      const int r = i >> 5, kk = i & 31;
+      const int m = m0 + r, n = n0 + r, k = k0 + kk;
+      As[kk][r] = (m < M && k < K) ? to_f(A[(size_t)m * lda + k]) : 0.f;
+      Ws[kk][r] = (n < N && k < K) ? to_f(W[(size_t)n * ldw + k]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = Ws[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + ty + 16 * i, n = n0 + tx + 16 * j;
+      if (m < M && n < N) epi(m, n, acc[i][j]);
+    }
+}
+
+struct EpiStore {
+  float* out;
+  long ld;
+  __device__ void operator()(int m, int n, float v) const { out[(size_t)m * ld + n] = v; }
+};
+
+template <typename TW>
+struct EpiBiasAct {  // out = act(acc + bias); act = SiLU when silu != 0
+  float* out;
+  long ld;
+  const TW* bias;
+  int silu;
+  __device__ void operator()(int m, int n, float v) const {
+    v += to_f(bias[n]);
+    if (silu) v = v / (1.f + expf(-v));
+    out[(size_t)m * ld + n] = v;
+  }
+};
+
+struct EpiResidual {  // gated residual: h += gate * acc
+  float* h;
+  long ld;
+  const float* gate;
+  __device__ void operator()(int m, int n, float v) const { h[(size_t)m * ld + n] += gate[n] * v; }
+};
+
+template <typename TA, typename TW, typename Epi>
+void gemm(int M, int N, int K, const TA* A, long lda, const TW* W, long ldw, Epi epi,
+          cudaStream_t s) {
+  dim3 grid((N + 63) / 64, (M + 63) / 64);
+  k_gemm<TA, TW, Epi><<<grid, 256, 0, s>>>(M, N, K, A, lda, W, ldw, epi);
+}
+
+// ---------------------------------------------------------------- layer pieces
+// adaRMS (LoongForge section 2): y = h * rsqrt(mean(h^2) + eps) * (1 + scale) + shift.
+template <typename T>
+__global__ void k_rmsmod(const float* __restrict__ h, int D, float eps, const float* scale,
+                         const float* shift, T* __restrict__ y) {
+  const int m = blockIdx.x;
+  const float* hr = h + (size_t)m * D;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < D; k += blockDim.x) ss += hr[k] * hr[k];
+  ss = block_sum(ss);
+  const float r = 1.0f / sqrtf(ss / (float)D + eps);
+  for (int k = threadIdx.x; k < D; k += blockDim.x)
+    y[(size_t)m * D + k] = from_f<T>(hr[k] * r * (1.f + scale[k]) + shift[k]);
+}
+
+// RoPE with the rotate_half pairing (i, i + dh/2) on the q and k heads; v is
+// passed through.  Input fp32 [M, (Hq + 2 Hkv) dh], output T of the same shape.
+template <typename T>
+__global__ void k_rope(const float* __restrict__ qkv_f, T* __restrict__ qkv,
+                       const float2* __restrict__ cs, int M, int H, int Hq, int Hkv, int dh) {
+  const int half = dh / 2, nh = Hq + 2 * Hkv;
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)M * nh * half) return;
+  const int j = (int)(idx % half);
+  const long t = idx / half;
+  const int hh = (int)(t % nh), m = (int)(t / nh);
+  const size_t base = (size_t)m * nh * dh + (size_t)hh * dh;
+  const float x1 = qkv_f[base + j], x2 = qkv_f[base + j + half];
+  if (hh < Hq + Hkv) {
+    const float2 c = cs[(size_t)m * half + j];  // m = b * H + i
+    qkv[base + j] = from_f<T>(x1 * c.x - x2 * c.y);
+    qkv[base + j + half] = from_f<T>(x2 * c.x + x1 * c.y);
+  } else {
+    qkv[base + j] = from_f<T>(x1);
+    qkv[base + j + half] = from_f<T>(x2);
+  }
+}
+
+// Attention of one action row: one warp per (request, query head, action
+// token).  Keys are the request's valid prefix rows (through the bind table;
+// masked rows are never read) followed by its H action rows (LoongForge
+// section 3).  Online softmax in fp32, scale 1/sqrt(dh).
+template <typename T, int DPL>
+__global__ void k_attn(const T* __restrict__ qkv, const T* __restrict__ pk,
+                       const T* __restrict__ pv, long total_rows, const int* __restrict__ valid_idx,
+                       const int* __restrict__ n_valid, int max_rows, T* __restrict__ o, int B,
+                       int H, int Hq, int Hkv, float scale, int* status) {
+  constexpr int dh = DPL * 32;
+  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wg >= B * Hq * H) return;
+  const int i = wg % H, hh = (wg / H) % Hq, b = wg / (H * Hq);
+  const int kvh = hh / (Hq / Hkv);
+  const int kvdim = Hkv * dh, qkvdim = (Hq + 2 * Hkv) * dh;
+  const T* qrow = qkv + (size_t)(b * H + i) * qkvdim + hh * dh + lane * DPL;
+  float q[DPL], acc[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) {
+    q[d] = to_f(qrow[d]) * scale;
+    acc[d] = 0.f;
+  }
+  float mx = -INFINITY, l = 0.f;
+  const int n = n_valid[b];
+  for (int j = 0; j < n + H; ++j) {
+    const T *kr, *vr;
+    if (j < n) {
+      const int row = valid_idx[(size_t)b * max_rows + j];
+      if (row < 0 || row >= total_rows) {
+        report(status, kDevBounds);
+        continue;
+      }
+      kr = pk + (size_t)row * kvdim + kvh * dh + lane * DPL;
+      vr = pv + (size_t)row * kvdim + kvh * dh + lane * DPL;
+    } else {
+      const T* base = qkv + (size_t)(b * H + (j - n)) * qkvdim;
+      kr = base + (Hq + kvh) * dh + lane * DPL;
+      vr = base + (Hq + Hkv + kvh) * dh + lane * DPL;
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) s += q[d] * to_f(kr[d]);
+    s = warp_sum(s);
+    const float mn = fmaxf(mx, s);
+    const float corr = expf(mx - mn), p = expf(s - mn);
+    l = l * corr + p;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] = acc[d] * corr + p * to_f(vr[d]);
+    mx = mn;
+  }
+  T* orow = o + (size_t)(b * H + i) * (Hq * dh) + hh * dh + lane * DPL;
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) orow[d] = from_f<T>(acc[d] * inv);
+}
+
+// GeGLU: m = gelu_tanh(g) * u, with [g | u] the two halves of each row.
+template <typename T>
+__global__ void k_geglu(const float* __restrict__ gu, T* __restrict__ m, int M, int F) {
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)M * F) return;
+  const long r = idx / F;
+  const int j = (int)(idx - r * F);
+  const float g = gu[(size_t)r * 2 * F + j], u = gu[(size_t)r * 2 * F + F + j];
+  const float ge = 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
+  m[idx] = from_f<T>(ge * u);
+}
+
+// Action input projection: h = x W_in^T + b_in.
+template <typename T>
+__global__ void k_inproj(const float* __restrict__ x, const T* __restrict__ w_in,
+                         const T* __restrict__ b_in, float* __restrict__ h, int M, int D, int A) {
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)M * D) return;
+  const int m = (int)(idx / D), n = (int)(idx - (long)m * D);
+  float s = 0.f;
+  for (int a = 0; a < A; ++a) s += x[(size_t)m * A + a] * to_f(w_in[(size_t)n * A + a]);
+  h[idx] = s + to_f(b_in[n]);
+}
+
+// Final adaRMS (scale, shift), action output projection and the Euler update
+// x += delta * v.  One block per action row.
+template <typename T>
+__global__ void k_final(const float* __restrict__ h, int D, float eps, const float* sf,
+                        const float* shf, const T* __restrict__ w_out, const T* __restrict__ b_out,
+                        int A, float delta, float* __restrict__ x) {
+  extern __shared__ float yf[];
+  const int m = blockIdx.x;
+  const float* hr = h + (size_t)m * D;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < D; k += blockDim.x) ss += hr[k] * hr[k];
+  ss = block_sum(ss);
+  const float r = 1.0f / sqrtf(ss / (float)D + eps);
+  for (int k = threadIdx.x; k < D; k += blockDim.x) yf[k] = hr[k] * r * (1.f + sf[k]) + shf[k];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int a = warp; a < A; a += nw) {
+    float v = 0.f;
+    for (int k = lane; k < D; k += 32) v += yf[k] * to_f(w_out[(size_t)a * D + k]);
+    v = warp_sum(v);
+    if (lane == 0) x[(size_t)m * A + a] += delta * (v + to_f(b_out[a]));
+  }
+}
+
+inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / per); }
+
+template <typename T>
+int time_table_t(const ae_ctx* c, TimeTable& t, cudaStream_t s) {
+  const Dims& d = c->d;
+  const int S = t.n_steps, D = d.D;
+  float* e = t.act;              // [S][D]
+  float* a1 = t.act + (size_t)S * D;
+  k_time_embed<<<blocks_for((long)S * (D / 2), 256), 256, 0, s>>>(e, S, D, d.tmin, d.tmax);
+  gemm(S, D, D, e, D, (const T*)c->w_t1, D, EpiBiasAct<T>{a1, D, (const T*)c->b_t1, 1}, s);
+  gemm(S, D, D, a1, D, (const T*)c->w_t2, D, EpiBiasAct<T>{t.c, D, (const T*)c->b_t2, 1}, s);
+  // every layer's two modulation Linears at once: w_mod is [L * 2 * 3D, D]
+  const long nmod = (long)d.L * 2 * 3 * D;
+  gemm(S, (int)nmod, D, (const float*)t.c, D, (const T*)c->w_mod, D,
+       EpiBiasAct<T>{t.mod, nmod, (const T*)c->b_mod, 0}, s);
+  gemm(S, 2 * D, D, (const float*)t.c, D, (const T*)c->w_modf, D,
+       EpiBiasAct<T>{t.fin, 2L * D, (const T*)c->b_modf, 0}, s);
+  return 5;
+}
+
+template <typename T>
+void launch_attn(ae_ctx* c, int l, cudaStream_t s) {
+  const Dims& d = c->d;
+  const int B = c->bind.batch;
+  const long lay = (long)l * c->bind.total_rows * d.kvdim();
+  const T* pk = (const T*)c->bind.pk + lay;
+  const T* pv = (const T*)c->bind.pv + lay;
+  const long warps = (long)B * d.Hq * d.H;
+  const unsigned grid = blocks_for(warps * 32, 256);
+  const float scale = (float)(1.0 / sqrt((double)d.dh));
+#define AE_ATTN(DPL)                                                                        \
+  k_attn<T, DPL><<<grid, 256, 0, s>>>((const T*)c->qkv, pk, pv, c->bind.total_rows,        \
+                                      c->valid_idx, c->n_valid, c->max_rows, (T*)c->o, B, \
+                                      d.H, d.Hq, d.Hkv, scale, c->status_dev)
+  switch (d.dh / 32) {
+    case 1: AE_ATTN(1); break;
+    case 2: AE_ATTN(2); break;
+    case 3: AE_ATTN(3); break;
+    case 4: AE_ATTN(4); break;
+    case 5: AE_ATTN(5); break;
+    case 6: AE_ATTN(6); break;
+    case 7: AE_ATTN(7); break;
+    default: AE_ATTN(8); break;
+  }
+#undef AE_ATTN
+}
+
+template <typename T>
+int step_simt(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s) {
+  const Dims& d = c->d;
+  const int B = c->bind.batch, M = B * d.H, D = d.D, F = d.F, L = d.L;
+  const int nqkv = d.qkvdim();
+  const float eps = (float)d.eps;
+  int n = 0;
+  auto dump = [&](int l) {
+    if (c->dump == nullptr) return;
+    float* dst = c->dump + (((size_t)step * (L + 1) + l) * M) * D;
+    cudaMemcpyAsync(dst, c->h, (size_t)M * D * sizeof(float), cudaMemcpyDeviceToDevice, s);
+  };
+  k_inproj<T><<<blocks_for((long)M * D, 256), 256, 0, s>>>(x, (const T*)c->w_in,
+                                                           (const T*)c->b_in, c->h, M, D, d.A);
+  ++n;
+  for (int l = 0; l < L; ++l) {
+    dump(l);
+    const float* mod1 = t.mod + (((size_t)step * L + l) * 2 + 0) * 3 * D;
+    const float* mod2 = mod1 + 3 * D;
+    const T* wqkv = (const T*)c->w_qkv + (size_t)l * nqkv * D;
+    const T* wo = (const T*)c->w_o + (size_t)l * D * d.qdim();
+    const T* wgu = (const T*)c->w_gu + (size_t)l * 2 * F * D;
+    const T* wd = (const T*)c->w_d + (size_t)l * D * F;
+    k_rmsmod<T><<<M, 256, 0, s>>>(c->h, D, eps, mod1, mod1 + D, (T*)c->y);
+    gemm(M, nqkv, D, (const T*)c->y, D, wqkv, D, EpiStore{c->qkv_f, nqkv}, s);
+    k_rope<T><<<blocks_for((long)M * (nqkv / 2), 256), 256, 0, s>>>(
+        c->qkv_f, (T*)c->qkv, c->rope_cs, M, d.H, d.Hq, d.Hkv, d.dh);
+    launch_attn<T>(c, l, s);
+    gemm(M, D, d.qdim(), (const T*)c->o, d.qdim(), wo, d.qdim(), EpiResidual{c->h, D, mod1 + 2 * D},
+         s);
+    k_rmsmod<T><<<M, 256, 0, s>>>(c->h, D, eps, mod2, mod2 + D, (T*)c->y);
+    gemm(M, 2 * F, D, (const T*)c->y, D, wgu, D, EpiStore{c->gu_f, 2L * F}, s);
+    k_geglu<T><<<blocks_for((long)M * F, 256), 256, 0, s>>>(c->gu_f, (T*)c->m, M, F);
+    gemm(M, D, F, (const T*)c->m, F, wd, F, EpiResidual{c->h, D, mod2 + 2 * D}, s);
+    n += 9;
+  }
+  dump(L);
+  const float* fin = t.fin + (size_t)step * 2 * D;
+  const float delta = (float)(-1.0 / (double)t.n_steps);
+  k_final<T><<<M, 256, D * sizeof(float), s>>>(c->h, D, eps, fin, fin + D, (const T*)c->w_out,
+                                               (const T*)c->b_out, d.A, delta, x);
+  return n + 1;
+}
+
+}  // namespace
+
+int launch_bind(const BindArgs& a, cudaStream_t s) {
+  if (a.batch <= 0) return 0;
+  k_bind<<<a.batch, 256, 0, s>>>(a);
+  return 1;
+}
+
+int launch_time_table(const ae_ctx* c, TimeTable& t, cudaStream_t s) {
+  return c->d.dtype == AE_DTYPE_BF16 ? time_table_t<bf16>(c, t, s) : time_table_t<float>(c, t, s);
+}
+
+int launch_step_simt(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s) {
+  return c->d.dtype == AE_DTYPE_BF16 ? step_simt<bf16>(c, t, step, x, s)
+                                     : step_simt<float>(c, t, step, x, s);
+}
+
+}  // namespace ae

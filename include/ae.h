@@ -1,0 +1,219 @@
+/*
+ * ae.h - C ABI of the GB300 flow-matching action-expert sampler.
+ *
+ * The library runs the action expert of a vision-language-action model for
+ * n Euler steps of flow matching: starting from noise at t = 1, every step
+ * evaluates a Gemma-style expert on the H action tokens of each request
+ * (adaRMS conditioned on a sinusoidal time embedding, merged QKV, RoPE,
+ * MQA/GQA attention over [valid prefix KV || action KV], gated residuals,
+ * merged gate/up GeGLU MLP) and moves the actions by x <- x + delta * v with
+ * delta = -1/n.  Sources, by page and section:
+ *   - MolmoBot PR "Inference optimization for MolmoBot VLA: torch.compile +
+ *     CUDA graphs + action-expert KV cache", Part 2: the VLM context is
+ *     computed once per query and reused by every flow step.
+ *   - LoongForge blog "How to Speed Up VLA Training Step by Step: A 3x
+ *     Acceleration Case Study on Pi0.5", sections 1-3 and 5.3: the layer's
+ *     ops, the prefix-LM mask, masked camera slots, pad tokens that do not
+ *     advance positions, time MLP and action in/out projections.
+ *   - sglang PR #34599 summary, implementation items 1-2: merged Q/K/V and
+ *     gate/up weights; mask, positions and time scaling hoisted out of the
+ *     step loop.
+ *   - OxyGen, "Cross-task KV Sharing": one prefill's KV is read, not copied,
+ *     by the action expert.
+ *
+ * Conventions common to every call:
+ *   - Matrices are row-major [out, in] (a Linear's weight).  "T" below is the
+ *     storage type chosen by ae_config.dtype: bf16 (AE_DTYPE_BF16) or fp32
+ *     (AE_DTYPE_F32).  Flow state (noise, actions) is always fp32.
+ *   - "device" pointers are CUDA device (or managed) memory of the device
+ *     that was current when ae_create ran; "host" pointers are ordinary
+ *     host memory.
+ *   - Every call is stream-ordered on the context's stream and returns after
+ *     enqueueing (ae_create and ae_destroy synchronize that stream).  A call
+ *     that fails a host-side check returns at once and changes no state.
+ *   - Device-side checks (bounds, bounded waits) set a sticky status that the
+ *     next ae_sample returns as AE_ERR_DEVICE; ae_synchronize and
+ *     ae_last_error report it too.  No call throws or aborts.
+ *   - A context is not thread-safe; distinct contexts are independent.
+ */
+#ifndef AE_H_
+#define AE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define AE_API __attribute__((visibility("default")))
+#else
+#define AE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ae_ctx ae_ctx;
+
+typedef enum {
+  AE_OK = 0,
+  AE_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad enum     */
+  AE_ERR_SHAPE = -2,       /* a size outside what the context supports      */
+  AE_ERR_NOT_BOUND = -3,   /* ae_sample before a successful ae_bind_prefix  */
+  AE_ERR_CUDA = -4,        /* a CUDA runtime call failed (see ae_last_error) */
+  AE_ERR_DEVICE = -5,      /* a device-side check failed (sticky)           */
+  AE_ERR_OOM = -6,         /* device memory allocation failed               */
+  AE_ERR_UNSUPPORTED = -7  /* no GPU of compute capability 10.3 is current  */
+} ae_status;
+
+typedef enum { AE_DTYPE_BF16 = 0, AE_DTYPE_F32 = 1 } ae_dtype;
+
+/* Limits checked by the host side of every call. */
+#define AE_MAX_BATCH 64  /* requests per ae_bind_prefix                  */
+#define AE_MAX_STEPS 128 /* Euler steps per ae_sample                    */
+
+/*
+ * Expert dimensions.  Requirements: every size > 0; n_q_heads % n_kv_heads
+ * == 0; head_dim even, a multiple of 32 and <= 256; width and mlp multiples
+ * of 32; width even (the time embedding is width/2 sines then width/2
+ * cosines).  rms_eps is adaRMS's epsilon; rope_theta the RoPE base; the
+ * time-embedding periods run geometrically from time_min_period to
+ * time_max_period (LoongForge sections 2 and 5.3 name the sinusoidal time
+ * embedding and the time MLP without printing their constants).
+ */
+typedef struct {
+  int layers;      /* L  */
+  int width;       /* D  */
+  int mlp;         /* F  */
+  int n_q_heads;   /* Hq */
+  int n_kv_heads;  /* Hkv */
+  int head_dim;    /* dh */
+  int action_dim;  /* A  */
+  int horizon;     /* H, action tokens per request */
+  double rms_eps;
+  double rope_theta;
+  double time_min_period; /* double: the smallest period's angle reaches ~1.6e3 rad */
+  double time_max_period;
+  int dtype;       /* ae_dtype: storage type T of weights and prefix K/V */
+} ae_config;
+
+/*
+ * Weights, as device pointers of type T.  The per-layer members are HOST
+ * arrays of `layers` device pointers.  ae_create copies and repacks all of
+ * them into library-owned memory (merged QKV and gate/up as in sglang
+ * PR #34599 item 1), so the caller keeps ownership and may free them once
+ * ae_create has returned.
+ *   w_in [D, A], b_in [D]               action input projection
+ *   w_t1 [D, D], b_t1 [D], w_t2, b_t2   time MLP: c = silu(W2 silu(W1 e + b1) + b2)
+ *   wq [Hq*dh, D], wk [Hkv*dh, D], wv [Hkv*dh, D], wo [D, Hq*dh]
+ *   wg [F, D], wu [F, D], wd [D, F]     GeGLU MLP: (gelu_tanh(y Wg^T) * y Wu^T) Wd^T
+ *   w_mod1/w_mod2 [3D, D], b_mod1/b_mod2 [3D]   adaRMS (scale, shift, gate) of
+ *                                       the attention / MLP sublayer
+ *   w_mod_f [2D, D], b_mod_f [2D]       final adaRMS (scale, shift)
+ *   w_out [A, D], b_out [A]             action output projection
+ */
+typedef struct {
+  const void *w_in, *b_in;
+  const void *w_t1, *b_t1, *w_t2, *b_t2;
+  const void *w_mod_f, *b_mod_f;
+  const void *w_out, *b_out;
+  const void *const *wq, *const *wk, *const *wv, *const *wo;
+  const void *const *wg, *const *wu, *const *wd;
+  const void *const *w_mod1, *const *b_mod1, *const *w_mod2, *const *b_mod2;
+} ae_weights;
+
+/*
+ * Create a context on the current CUDA device.
+ *   max_batch       requests a bind may hold, 1..AE_MAX_BATCH
+ *   max_prefix_rows physical prefix rows one request may have (valid + masked)
+ *   stream          cudaStream_t the context enqueues on (NULL = legacy default)
+ *   out             receives the context; set to NULL on failure
+ * Allocates all device memory the context will use (weights, scratch, bind
+ * tables); later calls allocate only a per-n_steps time table on first use.
+ * Errors: AE_ERR_INVALID_ARG, AE_ERR_SHAPE, AE_ERR_UNSUPPORTED, AE_ERR_OOM,
+ * AE_ERR_CUDA.
+ */
+AE_API ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
+                    int max_prefix_rows, void* stream, ae_ctx** out);
+
+/* Destroy a context (synchronizes its stream first).  NULL is ignored. */
+AE_API void ae_destroy(ae_ctx* ctx);
+
+/* Change the stream later calls enqueue on. */
+AE_API ae_status ae_set_stream(ae_ctx* ctx, void* stream);
+
+/*
+ * Bind the VLM prefix KV of `batch` requests (MolmoBot Part 2: computed once,
+ * reused by every flow step; OxyGen: borrowed, never copied).
+ *   prefix_k, prefix_v  device T, packed varlen [layers][total_rows][Hkv*dh]
+ *                       with total_rows = cu_lens[batch].  K is already
+ *                       rotated at the VLM's positions and is not re-roped.
+ *   cu_lens             HOST int32 [batch + 1]: request b owns physical rows
+ *                       cu_lens[b] .. cu_lens[b+1]-1; cu_lens[0] == 0,
+ *                       non-decreasing, at most max_prefix_rows per request.
+ *   prefix_mask         device uint8 [total_rows], 1 = valid, 0 = masked or
+ *                       padding; NULL = every row valid.  Masked rows are never
+ *                       read (they may hold NaN) and do not advance positions
+ *                       (LoongForge section 1): action token i of request b
+ *                       sits at position n_b + i, n_b = its valid row count.
+ * prefix_k, prefix_v and prefix_mask must stay alive and unchanged until the
+ * last ae_sample that uses this binding has completed on the stream.
+ * batch == 0 is legal (ae_sample then does nothing).
+ * Errors: AE_ERR_INVALID_ARG, AE_ERR_SHAPE (batch > max_batch, a request
+ * longer than max_prefix_rows, bad cu_lens), AE_ERR_CUDA.
+ */
+AE_API ae_status ae_bind_prefix(ae_ctx* ctx, int batch, const void* prefix_k,
+                         const void* prefix_v, const int32_t* cu_lens,
+                         const uint8_t* prefix_mask);
+
+/*
+ * Run n_steps Euler steps of delta = -1/n_steps from t = 1 for every bound
+ * request (MolmoBot Part 2), the velocity of step k taken at t = 1 - k/n_steps.
+ *   noise        device fp32 [batch][horizon][action_dim], the state at t = 1
+ *   out_actions  device fp32 [batch][horizon][action_dim]; may equal noise
+ * The time-conditioning table for this n_steps is built on first use and
+ * cached in the context (it depends on the weights and n_steps only).
+ * Errors: AE_ERR_NOT_BOUND, AE_ERR_INVALID_ARG, AE_ERR_SHAPE (n_steps outside
+ * 1..AE_MAX_STEPS), AE_ERR_DEVICE (sticky status of an earlier call),
+ * AE_ERR_OOM, AE_ERR_CUDA.
+ */
+AE_API ae_status ae_sample(ae_ctx* ctx, const float* noise, int n_steps, float* out_actions);
+
+/*
+ * Optional per-layer hidden-state dump for parity checks.  When set, every
+ * ae_sample writes the fp32 residual stream entering layer l (l = 0..L-1) and
+ * leaving the last layer (l = L) of every step s to
+ *   hidden[((s * (L + 1) + l) * batch + b) * horizon + i][0 .. D-1].
+ * hidden: device fp32 with room for `capacity` floats; NULL switches it off.
+ * ae_sample returns AE_ERR_SHAPE if the dump does not fit.
+ */
+AE_API ae_status ae_set_debug_dump(ae_ctx* ctx, float* hidden, size_t capacity);
+
+/* Wait for the context's stream, then report the sticky device status. */
+AE_API ae_status ae_synchronize(ae_ctx* ctx);
+
+/*
+ * Copy a NUL-terminated description of the last error of this context (or of
+ * the last failed ae_create when ctx is NULL) into buf[0..n-1].  Returns the
+ * sticky device status (AE_OK if none).
+ */
+AE_API ae_status ae_last_error(const ae_ctx* ctx, char* buf, size_t n);
+
+/* Static name of a status code. */
+AE_API const char* ae_status_string(ae_status s);
+
+/* Counters a caller can read after ae_sample, e.g. to report kernel launches. */
+typedef struct {
+  int64_t launches_last_sample; /* kernels the last ae_sample enqueued      */
+  int64_t launches_last_bind;   /* kernels the last ae_bind_prefix enqueued */
+  int64_t device_bytes;         /* device memory the context holds          */
+  int sm_count;                 /* SMs of the context's device              */
+  int path;                     /* 0 = fp32 SIMT path, 1 = bf16 path         */
+} ae_info;
+
+AE_API ae_status ae_get_info(const ae_ctx* ctx, ae_info* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AE_H_ */
