@@ -1,0 +1,435 @@
+"""Throughput of the flow-matching action-expert denoise loop on GB300.
+
+One "step" = one whole pass of the hot path over one batch: ae_bind_prefix of
+the batch's prefix KV, then ae_sample with 10 Euler steps.  The headline is
+the Pi0.5-shaped batch-1 workload (two 256-token camera slots + 200 text
+tokens = 712 valid prefix rows, 18 expert layers, 50 x 32 action chunk); a
+batch-16 ragged-prefix line is reported beside it.  All inputs are synthetic
+(seeded N(0, sigma), see flow_matching_action_gb300/synth.py).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (requests
+are independent; there is no collective on the data path); the barrier and the
+max over ranks only bracket the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "action chunks/s and µs/flow step (B=1,B=16); % HBM / bf16 tensor roofline"
+N_FLOW_STEPS = 10
+
+
+def algorithmic(dims, n_valid, n_act=None):
+    """Algorithmic bytes and flops of ONE flow step (weights read once, prefix
+    KV of the valid rows read once per layer; activations neglected)."""
+    d = dims
+    H = d.horizon if n_act is None else n_act
+    per_layer_params = (d.q_dim + 2 * d.kv_dim) * d.width + d.width * d.q_dim + 3 * d.mlp * d.width
+    weight_bytes = d.layers * per_layer_params * 2
+    kv_bytes = sum(d.layers * 2 * n * d.kv_dim * 2 for n in n_valid)
+    B = len(n_valid)
+    gemm_flops = 2 * d.layers * per_layer_params * B * H
+    attn_flops = sum(4 * d.layers * d.n_q_heads * H * (n + H) * d.head_dim for n in n_valid)
+    return weight_bytes + kv_bytes, gemm_flops + attn_flops
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ae_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx = float(p[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+def make_workload(name: str, seed: int = 0):
+    from flow_matching_action_gb300 import synth
+    if name == "pi05_b1":
+        return synth.pi05_two_camera(seed, N_FLOW_STEPS)
+    if name == "pi05_b16":
+        return synth.pi05_batched(seed, N_FLOW_STEPS, 16)
+    if name == "pi05_b1_pad2048":
+        return synth.pi05_padded(seed, N_FLOW_STEPS, True)
+    if name == "tiny":
+        return synth.tiny(seed)
+    raise ValueError(name)
+
+
+def describe(wl) -> str:
+    return (f"{wl.name}: Pi0.5-shaped action expert L={wl.dims.layers} D={wl.dims.width} "
+            f"F={wl.dims.mlp} Hq={wl.dims.n_q_heads} Hkv={wl.dims.n_kv_heads} dh={wl.dims.head_dim}, "
+            f"batch {wl.batch}, valid prefix rows {min(wl.n_valid)}..{max(wl.n_valid)} "
+            f"(physical {sum(wl.n_rows)}), horizon {wl.dims.horizon} x {wl.dims.action_dim}, "
+            f"{wl.n_steps} Euler steps")
+
+
+def _dev(x, dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True):
+    import torch
+    from flow_matching_action_gb300 import ae
+
+    dtype = wl.dims.dtype
+    dev_w = {k: ([_dev(a, dtype) for a in v] if isinstance(v, list) else _dev(v, dtype))
+             for k, v in weights_np.items()}
+    stream = torch.cuda.Stream()
+    ex = ae.ActionExpert(wl.dims, dev_w, max(wl.batch, 1), max(max(wl.n_rows), 1),
+                         stream=stream.cuda_stream)
+    del dev_w
+    k = _dev(wl.prefix_k, dtype)
+    v = _dev(wl.prefix_v, dtype)
+    mask = torch.from_numpy(wl.mask).cuda()
+    cu = [int(c) for c in wl.cu_lens]
+    rng = np.random.default_rng(123)
+    n_noise = 4
+    noises = [torch.from_numpy(rng.standard_normal(wl.noise.shape).astype(np.float32)).cuda()
+              for _ in range(n_noise)]
+    out = torch.empty_like(noises[0])
+
+    def one_step(i):
+        ex.bind_prefix(k, v, cu, mask)
+        ex.sample(noises[i % n_noise], wl.n_steps, out)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            one_step(i)
+        ex.synchronize()
+        info = ex.info()
+        launches_per_step = info["launches_last_sample"] + info["launches_last_bind"]
+
+        # -- timed region: device-resident inputs
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        clocks = ClockSampler(torch.cuda.current_device())
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        time.sleep(0.3)  # let the sampler take its first reading
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            ex.bind_prefix(k, v, cu, mask)
+            mids[i].record(stream)
+            ex.sample(noises[i % n_noise], wl.n_steps, out)
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        dist_ctx.barrier()
+        total_ms = t0.elapsed_time(t1)
+        bind_ms = [starts[i].elapsed_time(mids[i]) for i in range(steps)]
+        sample_ms = [mids[i].elapsed_time(ends[i]) for i in range(steps)]
+
+        e2e = None
+        if measure_e2e:
+            e2e = run_e2e(ex, wl, steps, warmup, stream, dist_ctx)
+    ex.close()
+    return {"total_ms": total_ms, "bind_ms": bind_ms, "sample_ms": sample_ms, "clocks": clk,
+            "launches_per_step": launches_per_step, "e2e": e2e}
+
+
+def run_e2e(ex, wl, steps, warmup, stream, dist_ctx):
+    """The same metric through the public API with HOST buffers: every step copies
+    the step's inputs (prefix K/V, mask, noise) from pinned host memory, binds,
+    samples, and reads the actions back to pinned host memory."""
+    import torch
+    dtype = wl.dims.dtype
+    hk = torch.from_numpy(np.ascontiguousarray(wl.prefix_k))
+    hv = torch.from_numpy(np.ascontiguousarray(wl.prefix_v))
+    if dtype == "bf16":
+        hk, hv = hk.to(torch.bfloat16), hv.to(torch.bfloat16)
+    hk, hv = hk.pin_memory(), hv.pin_memory()
+    hmask = torch.from_numpy(wl.mask).pin_memory()
+    hnoise = torch.from_numpy(wl.noise).pin_memory()
+    hout = torch.empty_like(hnoise).pin_memory()
+    dk, dv = torch.empty_like(hk, device="cuda"), torch.empty_like(hv, device="cuda")
+    dmask = torch.empty_like(hmask, device="cuda")
+    dnoise = torch.empty_like(hnoise, device="cuda")
+    dout = torch.empty_like(dnoise)
+    cu = [int(c) for c in wl.cu_lens]
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hmask, hnoise))
+    d2h = hout.numel() * hout.element_size()
+
+    def one():
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dmask.copy_(hmask, non_blocking=True)
+        dnoise.copy_(hnoise, non_blocking=True)
+        ex.bind_prefix(dk, dv, cu, dmask)
+        ex.sample(dnoise, wl.n_steps, dout)
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(max(warmup, 1)):
+        one()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_ctx.max(t0.elapsed_time(t1))
+    return {"ms": ms, "h2d": h2d, "d2h": d2h}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_flow_step_seconds(wl, weights_np, budget_s=12.0, min_runs=1):
+    """Time the oracle (as it stands) on single flow steps of the workload until the budget is spent."""
+    from oracle import ae_oracle
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        ae_oracle.sample(wl.dims, weights_np, wl.prefix_k, wl.prefix_v, wl.cu_lens, wl.mask,
+                         wl.noise, 1)
+        times.append(time.perf_counter() - t0)
+        if len(times) >= min_runs and time.perf_counter() - t_start >= budget_s:
+            break
+    return statistics.median(times), len(times)
+
+
+def cpu_baseline(wl, weights_np, budget_s=12.0):
+    sec, runs = oracle_flow_step_seconds(wl, weights_np, budget_s)
+    chunk_s = sec * wl.n_steps
+    return {"value": wl.batch / chunk_s, "unit": "chunks/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{runs} single flow steps of {wl.name} (batch {wl.batch}) through the float64 "
+                      f"NumPy oracle, median {sec:.3f} s per flow step, scaled x{wl.n_steps} to a chunk"}
+
+
+# ----------------------------------------------------------------------------- dist
+class DistCtx:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl"
+            import torch
+            if not torch.cuda.is_available():
+                backend = "gloo"
+            else:
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained", p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="pi05_b1")
+    ap.add_argument("--batched", default="pi05_b16", help="second workload reported beside ('' = none)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+
+    dist_ctx = DistCtx(args.gpus)
+    from flow_matching_action_gb300 import synth
+    wl = make_workload(args.workload)
+    w = synth.make_weights(wl.dims, 0)
+    bytes_fs, flops_fs = algorithmic(wl.dims, wl.n_valid)
+
+    if args.impl == "reference":
+        if dist_ctx.rank != 0:
+            dist_ctx.close()
+            return
+        for _ in range(args.warmup):
+            pass  # the oracle has no warm-up state; its first run is timed like the rest
+        per = []
+        for _ in range(args.steps):
+            sec, _ = oracle_flow_step_seconds(wl, w, budget_s=0.0)
+            per.append(sec * wl.n_steps)
+        ms = statistics.median(per) * 1e3
+        value = wl.batch / (ms / 1e3)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "chunks/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": describe(wl)},
+                "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": blas_threads(),
+                                 "kind": "oracle",
+                                 "sample": f"each step: one flow step of {wl.name} through the float64 "
+                                           f"NumPy oracle, scaled x{wl.n_steps} to a chunk"},
+                "e2e": {"value": value, "unit": "chunks/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        dist_ctx.close()
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (sm_103a); the product has no CPU path")
+    torch.cuda.set_device(dist_ctx.local_rank)
+    from flow_matching_action_gb300 import build as ae_build
+    if dist_ctx.rank == 0:
+        ae_build.build()
+    dist_ctx.barrier()
+    ae_build.build()
+
+    res = run_gpu_arm(wl, w, args.steps, args.warmup, dist_ctx, measure_e2e=not args.no_e2e)
+    total_ms = dist_ctx.max(res["total_ms"])
+    ms_per_step = total_ms / args.steps
+    chunks = wl.batch * args.steps * dist_ctx.world
+    value = chunks / (total_ms / 1e3)
+    sample_ms = statistics.median(res["sample_ms"])
+    bind_ms = statistics.median(res["bind_ms"])
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    # roofline of the dominant launch: the whole ae_sample call (10 flow steps)
+    achieved_gbs = bytes_fs * wl.n_steps / (sample_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "chunks/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) prefix KV and noise)",
+        "config": {"workload": describe(wl), "batch": wl.batch, "valid_prefix_rows": wl.n_valid,
+                   "n_flow_steps": wl.n_steps, "step": "ae_bind_prefix + ae_sample(10 Euler steps)",
+                   "l2": "inputs larger than L2: 623 MB of bf16 weights streamed per flow step",
+                   "parallelism": f"replicas x{dist_ctx.world}"},
+        "us_per_flow_step": sample_ms * 1e3 / wl.n_steps,
+        "sample_ms_median": sample_ms, "sample_ms_p90": float(np.percentile(res["sample_ms"], 90)),
+        "bind_ms_median": bind_ms,
+        "roofline": {"kernel": "ae_sample (all its launches, one flow step = 1 unit)",
+                     "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm, "traffic": None,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_flow_step": bytes_fs},
+        "clocks": res["clocks"],
+        "gpu_launches": int(res["launches_per_step"] * args.steps),
+    }
+    if res["e2e"] is not None:
+        e = res["e2e"]
+        line["e2e"] = {"value": chunks / (e["ms"] / 1e3), "unit": "chunks/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if args.batched:
+        wl2 = make_workload(args.batched)
+        b2, f2 = algorithmic(wl2.dims, wl2.n_valid)
+        r2 = run_gpu_arm(wl2, w, max(3, args.steps // 4), args.warmup, dist_ctx, measure_e2e=False)
+        s2 = statistics.median(r2["sample_ms"])
+        t2 = dist_ctx.max(r2["total_ms"]) / max(3, args.steps // 4)
+        tflops = f2 * wl2.n_steps / (s2 / 1e3) / 1e12
+        line["batched"] = {"workload": describe(wl2), "chunks_per_s": wl2.batch / (t2 / 1e3) * dist_ctx.world,
+                           "ms_per_step": t2, "us_per_flow_step": s2 * 1e3 / wl2.n_steps,
+                           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
+                                        "unit": "TFLOP/s", "frac": tflops / tf_sust,
+                                        "peak_kind": f"{peak_kind} sustained cuBLAS bf16",
+                                        "algorithmic_flops_per_flow_step": f2}}
+    if dist_ctx.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, w)
+    if dist_ctx.rank == 0:
+        print(json.dumps(line))
+    dist_ctx.close()
+
+
+if __name__ == "__main__":
+    main()
