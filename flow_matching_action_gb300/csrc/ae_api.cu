@@ -105,6 +105,7 @@ ae_status pack_weights(ae_ctx* c, const ae_weights* w) {
   const size_t es = elem_size(d.dtype);
   const size_t D = d.D, F = d.F, A = d.A, L = d.L;
   const size_t qd = d.qdim(), kvd = d.kvdim(), nqkv = d.qkvdim();
+  (void)kvd;
   AE_TRY(alloc(c, &c->w_in, D * A * es));
   AE_TRY(alloc(c, &c->b_in, D * es));
   AE_TRY(alloc(c, &c->w_t1, D * D * es));
@@ -135,15 +136,37 @@ ae_status pack_weights(ae_ctx* c, const ae_weights* w) {
   char* gu = (char*)c->w_gu;
   char* wmod = (char*)c->w_mod;
   char* bmod = (char*)c->b_mod;
+  const size_t dh = d.dh, row = D * es;
   for (size_t l = 0; l < L; ++l) {
     char* q = qkv + l * nqkv * D * es;
-    AE_TRY(put(c, q, w->wq[l], qd * D * es));
-    AE_TRY(put(c, q + qd * D * es, w->wk[l], kvd * D * es));
-    AE_TRY(put(c, q + (qd + kvd) * D * es, w->wv[l], kvd * D * es));
+    if (c->fast) {
+      // every head's rows as rotation pairs: packed row 2j = dim j, 2j+1 = dim j + dh/2
+      const void* const* srcs[3] = {w->wq, w->wk, w->wv};
+      const size_t heads[3] = {(size_t)d.Hq, (size_t)d.Hkv, (size_t)d.Hkv};
+      size_t hb = 0;
+      for (int part = 0; part < 3; ++part)
+        for (size_t h = 0; h < heads[part]; ++h, ++hb) {
+          const char* src = (const char*)srcs[part][l] + h * dh * row;
+          char* dst = q + hb * dh * row;
+          AE_CK(c, cudaMemcpy2DAsync(dst, 2 * row, src, row, row, dh / 2, cudaMemcpyDefault, c->stream));
+          AE_CK(c, cudaMemcpy2DAsync(dst + row, 2 * row, src + dh / 2 * row, row, row, dh / 2,
+                                     cudaMemcpyDefault, c->stream));
+        }
+    } else {
+      AE_TRY(put(c, q, w->wq[l], qd * D * es));
+      AE_TRY(put(c, q + qd * D * es, w->wk[l], kvd * D * es));
+      AE_TRY(put(c, q + (qd + kvd) * D * es, w->wv[l], kvd * D * es));
+    }
     AE_TRY(put(c, (char*)c->w_o + l * D * qd * es, w->wo[l], D * qd * es));
     char* g = gu + l * 2 * F * D * es;
-    AE_TRY(put(c, g, w->wg[l], F * D * es));
-    AE_TRY(put(c, g + F * D * es, w->wu[l], F * D * es));
+    if (c->fast) {
+      // gate and up rows interleaved: packed row 2j = gate j, 2j+1 = up j
+      AE_CK(c, cudaMemcpy2DAsync(g, 2 * row, w->wg[l], row, row, F, cudaMemcpyDefault, c->stream));
+      AE_CK(c, cudaMemcpy2DAsync(g + row, 2 * row, w->wu[l], row, row, F, cudaMemcpyDefault, c->stream));
+    } else {
+      AE_TRY(put(c, g, w->wg[l], F * D * es));
+      AE_TRY(put(c, g + F * D * es, w->wu[l], F * D * es));
+    }
     AE_TRY(put(c, (char*)c->w_d + l * D * F * es, w->wd[l], D * F * es));
     AE_TRY(put(c, wmod + (l * 2 + 0) * 3 * D * D * es, w->w_mod1[l], 3 * D * D * es));
     AE_TRY(put(c, wmod + (l * 2 + 1) * 3 * D * D * es, w->w_mod2[l], 3 * D * D * es));
@@ -167,6 +190,11 @@ ae_status alloc_scratch(ae_ctx* c) {
   AE_TRY(alloc(c, &c->valid_idx, (size_t)c->max_batch * (c->max_rows > 0 ? c->max_rows : 1) * sizeof(int)));
   AE_TRY(alloc(c, &c->n_valid, (size_t)c->max_batch * sizeof(int)));
   AE_TRY(alloc(c, &c->rope_cs, (size_t)c->max_batch * d.H * (d.dh / 2) * sizeof(float2)));
+  if (c->fast) {
+    AE_TRY(alloc(c, &c->sumsq, (size_t)(d.D / 128) * M * sizeof(float)));
+    c->part_floats = ae::fast_part_floats(d, c->max_batch, c->sm_count);
+    AE_TRY(alloc(c, &c->part, 2 * c->part_floats * sizeof(float)));
+  }
   return AE_OK;
 }
 
@@ -260,8 +288,17 @@ ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
     e = cudaHostGetDevicePointer((void**)&c->status_dev, c->status_host, 0);
   }
   if (e != cudaSuccess) st = cuda_fail(c, e, "status word");
+  if (st == AE_OK && cfg->dtype == AE_DTYPE_BF16) {
+    std::string why;
+    if (!ae::fast_path_supported(c->d, &why)) st = set_msg(c, AE_ERR_SHAPE, "%s", why.c_str());
+    c->fast = true;
+  }
   if (st == AE_OK) st = pack_weights(c, w);
   if (st == AE_OK) st = alloc_scratch(c);
+  if (st == AE_OK && c->fast) {
+    e = ae::fast_setup(c);
+    if (e != cudaSuccess) st = cuda_fail(c, e, "TMA descriptors of the packed weights");
+  }
   if (st == AE_OK) {
     e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) st = cuda_fail(c, e, "weight copies");
@@ -354,7 +391,15 @@ ae_status ae_sample(ae_ctx* c, const float* noise, int n_steps, float* out) {
   const size_t xbytes = (size_t)B * d.H * d.A * sizeof(float);
   if (out != noise) AE_CK(c, cudaMemcpyAsync(out, noise, xbytes, cudaMemcpyDeviceToDevice, c->stream));
   int64_t n = 0;
-  for (int s = 0; s < n_steps; ++s) n += ae::launch_step_simt(c, *t, s, out, c->stream);
+  for (int s = 0; s < n_steps; ++s) {
+    if (c->fast) {
+      cudaError_t e = cudaSuccess;
+      n += ae::launch_step_fast(c, *t, s, out, c->stream, &e);
+      if (e != cudaSuccess) return cuda_fail(c, e, "bf16 step launch");
+    } else {
+      n += ae::launch_step_simt(c, *t, s, out, c->stream);
+    }
+  }
   c->launches_sample = n;
   AE_CK(c, cudaGetLastError());
   return AE_OK;

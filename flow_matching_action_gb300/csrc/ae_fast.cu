@@ -1,0 +1,230 @@
+// Driver of the bf16 tensor-core path: TMA descriptors, scratch sizing and
+// the launch sequence of one flow step.
+//
+// One flow step (MolmoBot PR, Part 2: only the action queries and t change
+// between steps; the prefix binding is reused):
+//   in-proj (+ sum of squares) ->
+//   per layer: [adaRMS1 -> merged QKV GEMM -> RoPE] -> attention ->
+//              [O GEMM -> gated residual] -> [adaRMS2 -> merged gate/up GEMM]
+//              -> [GeGLU -> down GEMM -> gated residual] ->
+//   final adaRMS + out-proj + Euler update.
+// A GEMM whose output tiles cannot fill the GPU splits K; its fp32 partials
+// are summed in split order (deterministic) by a reduce kernel or by the
+// next GEMM's operand producer.
+#include <string>
+
+#include "ae_internal.h"
+
+namespace ae {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// bf16 matrix [rows, K] row-major; boxes of 128 rows x 64 columns, 128-byte swizzle.
+cudaError_t make_weight_map(CUtensorMap* map, const void* ptr, long rows, long K) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool fast_path_supported(const Dims& d, std::string* why) {
+  auto no = [&](const char* m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (d.D % 128) return no("bf16 path needs width % 128 == 0");
+  if (d.F % 64) return no("bf16 path needs mlp % 64 == 0");
+  if (d.qkvdim() % 128) return no("bf16 path needs (n_q_heads + 2 n_kv_heads) * head_dim % 128 == 0");
+  if (d.qdim() % 64) return no("bf16 path needs n_q_heads * head_dim % 64 == 0");
+  return true;
+}
+
+size_t fast_part_floats(const Dims& d, int max_batch, int sm_count) {
+  // ksplit * M <= sm_count * 256 / n_tiles, so ksplit * M * N <= sm_count * 256 * 128
+  (void)d;
+  (void)max_batch;
+  return (size_t)sm_count * 256 * 128;
+}
+
+cudaError_t fast_setup(ae_ctx* c) {
+  const Dims& d = c->d;
+  cudaError_t e;
+  if ((e = make_weight_map(&c->map_qkv, c->w_qkv, (long)d.L * d.qkvdim(), d.D)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&c->map_o, c->w_o, (long)d.L * d.D, d.qdim())) != cudaSuccess) return e;
+  if ((e = make_weight_map(&c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&c->map_d, c->w_d, (long)d.L * d.D, d.F)) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
+                     cudaError_t* err) {
+  const Dims& d = c->d;
+  const int B = c->bind.batch, M = B * d.H, D = d.D, F = d.F, L = d.L;
+  const int nqkv = d.qkvdim(), qd = d.qdim();
+  const float eps = (float)d.eps;
+  const int sm = c->sm_count;
+  const GemmPlan pq = plan_gemm(nqkv, D, M, sm, true);
+  const GemmPlan po = plan_gemm(D, qd, M, sm, true);
+  const GemmPlan pg = plan_gemm(2 * F, D, M, sm, true);
+  const GemmPlan pd = plan_gemm(D, F, M, sm, true);
+  float* part0 = c->part;
+  float* part1 = c->part + c->part_floats;
+  bf16* qkv = (bf16*)c->qkv;
+  bf16* o = (bf16*)c->o;
+  bf16* m = (bf16*)c->m;
+  int n = 0;
+  *err = cudaSuccess;
+  auto ck = [&](cudaError_t e) {
+    if (e != cudaSuccess && *err == cudaSuccess) *err = e;
+  };
+  auto dump = [&](int l) {
+    if (c->dump == nullptr) return;
+    float* dst = c->dump + (((size_t)step * (L + 1) + l) * M) * D;
+    ck(cudaMemcpyAsync(dst, c->h, (size_t)M * D * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  };
+
+  launch_inproj_tc(x, (const bf16*)c->w_in, (const bf16*)c->b_in, c->h, c->sumsq, M, D, d.A, s);
+  ++n;
+  for (int l = 0; l < L; ++l) {
+    dump(l);
+    const float* mod1 = t.mod + (((size_t)step * L + l) * 2 + 0) * 3 * D;
+    const float* mod2 = mod1 + 3 * D;
+
+    // adaRMS1 -> merged QKV -> RoPE
+    TcGemmArgs a = {};
+    a.M = M;
+    a.status = c->status_dev;
+    a.w_row0 = l * nqkv;
+    a.b_mode = kBRms;
+    a.h = c->h;
+    a.sumsq = c->sumsq;
+    a.n_sumsq = D / 128;
+    a.scale = mod1;
+    a.shift = mod1 + D;
+    a.eps = eps;
+    a.rope_cs = c->rope_cs;
+    a.dh = d.dh;
+    a.n_rot_heads = d.Hq + d.Hkv;
+    if (pq.ksplit == 1) {
+      a.e_mode = kEQkvRope;
+      a.out_bf16 = qkv;
+    } else {
+      a.e_mode = kEPartial;
+      a.part = part0;
+    }
+    ck(launch_tc_gemm(c->map_qkv, pq, a, s));
+    ++n;
+    if (pq.ksplit > 1) {
+      launch_reduce_qkv(part0, pq.ksplit, M, nqkv, d.dh, d.Hq + d.Hkv, c->rope_cs, qkv, s);
+      ++n;
+    }
+
+    n += launch_attn_bf16(c, l, s);
+
+    // O projection -> gated residual
+    a = TcGemmArgs{};
+    a.M = M;
+    a.status = c->status_dev;
+    a.w_row0 = l * D;
+    a.b_mode = kBCopy;
+    a.act = o;
+    if (po.ksplit == 1) {
+      a.e_mode = kEResid;
+      a.h_out = c->h;
+      a.gate = mod1 + 2 * D;
+      a.sumsq_out = c->sumsq;
+    } else {
+      a.e_mode = kEPartial;
+      a.part = part0;
+    }
+    ck(launch_tc_gemm(c->map_o, po, a, s));
+    ++n;
+    if (po.ksplit > 1) {
+      launch_reduce_resid(part0, po.ksplit, M, D, c->h, mod1 + 2 * D, c->sumsq, s);
+      ++n;
+    }
+
+    // adaRMS2 -> merged gate/up (-> GeGLU when not split)
+    a = TcGemmArgs{};
+    a.M = M;
+    a.status = c->status_dev;
+    a.w_row0 = l * 2 * F;
+    a.b_mode = kBRms;
+    a.h = c->h;
+    a.sumsq = c->sumsq;
+    a.n_sumsq = D / 128;
+    a.scale = mod2;
+    a.shift = mod2 + D;
+    a.eps = eps;
+    if (pg.ksplit == 1) {
+      a.e_mode = kEGeglu;
+      a.out_bf16 = m;
+    } else {
+      a.e_mode = kEPartial;
+      a.part = part0;
+    }
+    ck(launch_tc_gemm(c->map_gu, pg, a, s));
+    ++n;
+
+    // (GeGLU of the partials ->) down projection -> gated residual
+    a = TcGemmArgs{};
+    a.M = M;
+    a.status = c->status_dev;
+    a.w_row0 = l * D;
+    if (pg.ksplit == 1) {
+      a.b_mode = kBCopy;
+      a.act = m;
+    } else {
+      a.b_mode = kBGeglu;
+      a.gu_part = part0;
+      a.gu_ks = pg.ksplit;
+      a.gu_ld = 2L * F;
+    }
+    if (pd.ksplit == 1) {
+      a.e_mode = kEResid;
+      a.h_out = c->h;
+      a.gate = mod2 + 2 * D;
+      a.sumsq_out = c->sumsq;
+    } else {
+      a.e_mode = kEPartial;
+      a.part = part1;
+    }
+    ck(launch_tc_gemm(c->map_d, pd, a, s));
+    ++n;
+    if (pd.ksplit > 1) {
+      launch_reduce_resid(part1, pd.ksplit, M, D, c->h, mod2 + 2 * D, c->sumsq, s);
+      ++n;
+    }
+  }
+  dump(L);
+  n += launch_final_bf16(c, t, step, x, s);
+  ck(cudaGetLastError());
+  return n;
+}
+
+}  // namespace ae

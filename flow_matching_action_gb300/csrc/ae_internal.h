@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -98,6 +99,14 @@ struct ae_ctx {
   float* dump = nullptr;
   size_t dump_cap = 0;
 
+  // bf16 tensor-core path: TMA descriptors of the stacked per-layer weights
+  // (rows of layer l start at l * rows-per-layer) and its extra scratch.
+  bool fast = false;
+  CUtensorMap map_qkv, map_o, map_gu, map_d;
+  float* sumsq = nullptr;    // [D/128][M] adaRMS sum of squares per 128-feature tile
+  float* part = nullptr;     // split-K partials
+  size_t part_floats = 0;
+
   int64_t launches_sample = 0, launches_bind = 0, device_bytes = 0;
   std::vector<void*> allocations;
   std::string last_msg;
@@ -123,5 +132,59 @@ struct BindArgs {
 int launch_bind(const BindArgs& a, cudaStream_t s);
 int launch_time_table(const ae_ctx* c, TimeTable& t, cudaStream_t s);
 int launch_step_simt(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s);
+int launch_attn_bf16(ae_ctx* c, int layer, cudaStream_t s);
+int launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s);
+
+// ---- tensor-core GEMM (ae_gemm_tc.cu)
+enum BMode : int { kBRms = 0, kBCopy = 1, kBGeglu = 2 };
+enum EMode : int { kEPartial = 0, kEQkvRope = 1, kEResid = 2, kEGeglu = 3 };
+
+struct TcGemmArgs {
+  int M, N, K;          // tokens, output features, reduction length
+  int w_row0;           // first row of this layer's matrix in the stacked weight
+  int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
+  int b_mode;
+  const float* h;       // kBRms: fp32 [M, K]
+  const float* sumsq;   // kBRms: [n_sumsq][M]
+  int n_sumsq;
+  const float* scale;   // kBRms: [K]
+  const float* shift;   // kBRms: [K]
+  float eps;
+  const bf16* act;      // kBCopy: bf16 [M, K]
+  const float* gu_part; // kBGeglu: [gu_ks][M][gu_ld] with (g_j, u_j) adjacent
+  int gu_ks;
+  long gu_ld;
+  int e_mode;
+  float* part;          // kEPartial: [ksplit][M][N]
+  bf16* out_bf16;       // kEQkvRope: [M][N]; kEGeglu: [M][N/2]
+  const float2* rope_cs;
+  int dh, n_rot_heads;
+  float* h_out;         // kEResid: fp32 [M][N], updated in place
+  const float* gate;    // kEResid: [N]
+  float* sumsq_out;     // kEResid: [N/128][M]
+  int* status;
+};
+
+struct GemmPlan {
+  int N, K, n_tiles, tok_tiles, tok_tile, kb_total, ksplit, tmem_cols, stages, grid;
+  size_t smem;
+};
+
+size_t tc_gemm_smem_bytes(int stages, int tok_tile);
+GemmPlan plan_gemm(int N, int K, int M, int sm_count, bool allow_split);
+cudaError_t launch_tc_gemm(const CUtensorMap& map, const GemmPlan& p, TcGemmArgs a, cudaStream_t s);
+void launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
+                       const float2* cs, bf16* out, cudaStream_t s);
+void launch_reduce_resid(const float* part, int ks, int M, int N, float* h, const float* gate,
+                         float* sumsq, cudaStream_t s);
+void launch_inproj_tc(const float* x, const bf16* w_in, const bf16* b_in, float* h, float* sumsq,
+                      int M, int D, int A, cudaStream_t s);
+
+// ---- bf16 path driver (ae_fast.cu)
+bool fast_path_supported(const Dims& d, std::string* why);
+cudaError_t fast_setup(ae_ctx* c);  // tensor maps and scratch, after the weights are packed
+size_t fast_part_floats(const Dims& d, int max_batch, int sm_count);
+int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
+                     cudaError_t* err);
 
 }  // namespace ae

@@ -435,4 +435,20 @@ int launch_step_simt(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
                                      : step_simt<float>(c, t, step, x, s);
 }
 
+int launch_attn_bf16(ae_ctx* c, int layer, cudaStream_t s) {
+  launch_attn<bf16>(c, layer, s);
+  return 1;
+}
+
+int launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s) {
+  const Dims& d = c->d;
+  const int M = c->bind.batch * d.H;
+  const float* fin = t.fin + (size_t)step * 2 * d.D;
+  const float delta = (float)(-1.0 / (double)t.n_steps);
+  k_final<bf16><<<M, 256, d.D * sizeof(float), s>>>(c->h, d.D, (float)d.eps, fin, fin + d.D,
+                                                    (const bf16*)c->w_out, (const bf16*)c->b_out,
+                                                    d.A, delta, x);
+  return 1;
+}
+
 }  // namespace ae
