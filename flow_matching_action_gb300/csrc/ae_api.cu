@@ -194,6 +194,9 @@ ae_status alloc_scratch(ae_ctx* c) {
     AE_TRY(alloc(c, &c->sumsq, (size_t)(d.D / 128) * M * sizeof(float)));
     c->part_floats = ae::fast_part_floats(d, c->max_batch, c->sm_count);
     AE_TRY(alloc(c, &c->part, 2 * c->part_floats * sizeof(float)));
+    const size_t units = ae::attn_part_units(c->max_batch, d.H, d.Hq, d.Hkv, c->max_rows, c->sm_count);
+    AE_TRY(alloc(c, &c->attn_o, units * 128 * d.dh * sizeof(float)));
+    AE_TRY(alloc(c, &c->attn_ml, units * 128 * sizeof(float2)));
   }
   return AE_OK;
 }
@@ -365,6 +368,9 @@ ae_status ae_bind_prefix(ae_ctx* c, int batch, const void* prefix_k, const void*
   c->bind.pv = prefix_v;
   c->bind.total_rows = total;
   c->bind.cu.assign(a.cu, a.cu + batch + 1);
+  int longest = 0;
+  for (int b = 0; b < batch; ++b) longest = a.cu[b + 1] - a.cu[b] > longest ? a.cu[b + 1] - a.cu[b] : longest;
+  c->bind.max_phys_rows = longest;
   return AE_OK;
 }
 

@@ -11,6 +11,8 @@
 // A GEMM whose output tiles cannot fill the GPU splits K; its fp32 partials
 // are summed in split order (deterministic) by a reduce kernel or by the
 // next GEMM's operand producer.
+#include <math.h>
+
 #include <string>
 
 #include "ae_internal.h"
@@ -61,6 +63,7 @@ bool fast_path_supported(const Dims& d, std::string* why) {
   if (d.F % 64) return no("bf16 path needs mlp % 64 == 0");
   if (d.qkvdim() % 128) return no("bf16 path needs (n_q_heads + 2 n_kv_heads) * head_dim % 128 == 0");
   if (d.qdim() % 64) return no("bf16 path needs n_q_heads * head_dim % 64 == 0");
+  if (d.dh % 64) return no("bf16 path needs head_dim % 64 == 0");
   return true;
 }
 
@@ -144,7 +147,29 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       ++n;
     }
 
-    n += launch_attn_bf16(c, l, s);
+    {
+      AttnArgs at = {};
+      const long lay = (long)l * c->bind.total_rows * d.kvdim();
+      at.qkv = qkv;
+      at.pk = (const bf16*)c->bind.pk + lay;
+      at.pv = (const bf16*)c->bind.pv + lay;
+      at.total_rows = c->bind.total_rows;
+      at.valid_idx = c->valid_idx;
+      at.n_valid = c->n_valid;
+      at.max_rows = c->max_rows;
+      at.plan_rows = c->bind.max_phys_rows;
+      at.batch = B;
+      at.H = d.H;
+      at.Hq = d.Hq;
+      at.Hkv = d.Hkv;
+      at.dh = d.dh;
+      at.scale = (float)(1.0 / sqrt((double)d.dh));
+      at.part_o = c->attn_o;
+      at.part_ml = c->attn_ml;
+      at.status = c->status_dev;
+      ck(launch_attn_tc(at, o, sm, s));
+      n += 2;
+    }
 
     // O projection -> gated residual
     a = TcGemmArgs{};

@@ -46,6 +46,7 @@ struct BindState {
   const void* pk = nullptr;             // borrowed prefix K
   const void* pv = nullptr;             // borrowed prefix V
   int64_t total_rows = 0;               // rows per layer of pk / pv
+  int max_phys_rows = 0;                // longest request of the binding
   std::vector<int> cu;                  // host copy of cu_lens
 };
 
@@ -106,6 +107,8 @@ struct ae_ctx {
   float* sumsq = nullptr;    // [D/128][M] adaRMS sum of squares per 128-feature tile
   float* part = nullptr;     // split-K partials
   size_t part_floats = 0;
+  float* attn_o = nullptr;   // attention partials
+  float2* attn_ml = nullptr;
 
   int64_t launches_sample = 0, launches_bind = 0, device_bytes = 0;
   std::vector<void*> allocations;
@@ -179,6 +182,26 @@ void launch_reduce_resid(const float* part, int ks, int M, int N, float* h, cons
                          float* sumsq, cudaStream_t s);
 void launch_inproj_tc(const float* x, const bf16* w_in, const bf16* b_in, float* h, float* sumsq,
                       int M, int D, int A, cudaStream_t s);
+
+// ---- tensor-core attention (ae_attn_tc.cu)
+struct AttnArgs {
+  const bf16* qkv;        // [M][(Hq + 2 Hkv) dh] after RoPE
+  const bf16* pk;         // this layer's prefix K [total_rows][Hkv dh]
+  const bf16* pv;
+  long total_rows;
+  const int* valid_idx;   // [batch][max_rows]
+  const int* n_valid;     // [batch]
+  int max_rows;           // row stride of valid_idx
+  int plan_rows;          // longest physical prefix of the bound requests (work split bound)
+  int batch, H, Hq, Hkv, dh;
+  float scale;
+  int q_tiles, chunks_per_cta, max_splits;  // set by the planner
+  float* part_o;          // [units][128][dh]
+  float2* part_ml;        // [units][128]
+  int* status;
+};
+size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int sm_count);
+cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s);
 
 // ---- bf16 path driver (ae_fast.cu)
 bool fast_path_supported(const Dims& d, std::string* why);
