@@ -33,15 +33,23 @@ constexpr int kChunk = 64;            // keys per chunk
 constexpr float kRescaleMargin = 8.f; // raise the exponent reference only past this
 
 struct AttnSmem {
-  uint32_t q, k, vt, p, bars, total;  // byte offsets from the 1024-aligned base
+  uint32_t q, k[2], v[2], p, bars, total;  // byte offsets from the 1024-aligned base
 };
 
+// Q: [dh/64][128 rows][128 B] K-major.  K: [dh/64][64 keys][128 B] K-major.
+// V: row-major rows of the chunk as an MN-major operand (MN = dh, K = keys):
+// 1024-byte atoms of 8 keys x 64 dims, dims-atoms 1024 B apart, key-atoms
+// dh/64 * 1024 B apart.  P: [128 rows][128 B] K-major.  K and V are double
+// buffered so the next chunk's gathers overlap this chunk's MMAs.
 __host__ __device__ inline AttnSmem attn_smem_layout(int dh) {
   AttnSmem L;
-  L.q = 0;                                  // [dh/64][128 rows][128 B]
-  L.k = L.q + (uint32_t)dh * 128 * 2;       // [dh/64][64 keys][128 B]
-  L.vt = L.k + (uint32_t)dh * kChunk * 2;   // [dh rows][128 B]: V^T, K = 64 keys
-  L.p = L.vt + (uint32_t)dh * kChunk * 2;   // [128 rows][128 B]
+  const uint32_t kv = (uint32_t)dh * kChunk * 2;
+  L.q = 0;
+  L.k[0] = L.q + (uint32_t)dh * 128 * 2;
+  L.k[1] = L.k[0] + kv;
+  L.v[0] = L.k[1] + kv;
+  L.v[1] = L.v[0] + kv;
+  L.p = L.v[1] + kv;
   L.bars = L.p + 128 * kChunk * 2;
   L.total = L.bars + 64;
   return L;
@@ -78,11 +86,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
   const int c_begin = sp * a.chunks_per_cta;
   const int c_end = min(c_begin + a.chunks_per_cta, n_chunks);
   if (c_begin >= c_end) return;  // uniform for the CTA
+  const int n_my = c_end - c_begin;
   const int rows = G * a.H;
   const int qkvdim = (a.Hq + 2 * a.Hkv) * dh;
   const int kvdim = a.Hkv * dh;
   const int kdb = dh / 64;
+  const int cpr = dh / 8;  // 16-byte chunks per head row
   const uint32_t tcols = attn_tmem_cols(dh);
+  const uint32_t v_sbo = (uint32_t)kdb * 1024;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_s, 1);
@@ -94,17 +105,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
     tmem_alloc(tmem_base_p, tcols);
     tmem_relinquish();
   }
-  // ---- Q tile (once): folded row r = 128 qt + row  ->  (head, token)
-  for (int i = threadIdx.x; i < 128 * (dh / 8); i += kAttnThreads) {
-    const int row = i / (dh / 8), ch = i % (dh / 8);
+
+  // gathers of one chunk's K and V rows of KV head g into buffer `buf`
+  auto load_chunk = [&](int c, int buf) {
+    const int key0 = c * kChunk;
+    const int nk = min(kChunk, n_keys - key0);
+    uint8_t* ks = smem + L.k[buf];
+    uint8_t* vs = smem + L.v[buf];
+    for (int i = threadIdx.x; i < kChunk * cpr; i += kAttnThreads) {
+      const int j = i / cpr, ch = i % cpr;
+      const bf16* ksrc = a.qkv;  // any valid address when zero-filling
+      const bf16* vsrc = a.qkv;
+      uint32_t bytes = 0;
+      if (j < nk) {
+        const int key = key0 + j;
+        if (key < n_pre) {
+          const int prow = a.valid_idx[(size_t)b * a.max_rows + key];
+          if (prow >= 0 && prow < a.total_rows) {
+            ksrc = a.pk + (size_t)prow * kvdim + g * dh + ch * 8;
+            vsrc = a.pv + (size_t)prow * kvdim + g * dh + ch * 8;
+            bytes = 16;
+          } else {
+            report(a.status, kDevBounds);
+          }
+        } else {
+          const bf16* base = a.qkv + (size_t)(b * a.H + (key - n_pre)) * qkvdim;
+          ksrc = base + (a.Hq + g) * dh + ch * 8;
+          vsrc = base + (a.Hq + a.Hkv + g) * dh + ch * 8;
+          bytes = 16;
+        }
+      }
+      const int grp = ch >> 3, cc = ch & 7;
+      cp_async16(ks + grp * kChunk * 128 + sw128_offset(j, cc), ksrc, bytes);
+      cp_async16(vs + (j >> 3) * v_sbo + grp * 1024 + sw128_offset(j & 7, cc), vsrc, bytes);
+    }
+  };
+
+  // ---- Q tile (once): folded row r = 128 qt + row  ->  (head, token); then chunk 0
+  for (int i = threadIdx.x; i < 128 * cpr; i += kAttnThreads) {
+    const int row = i / cpr, ch = i % cpr;
     const int r = qt * 128 + row;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    const bf16* src = a.qkv;
+    uint32_t bytes = 0;
     if (r < rows) {
       const int h = g * G + r / a.H, tok = r % a.H;
-      v = *reinterpret_cast<const uint4*>(a.qkv + (size_t)(b * a.H + tok) * qkvdim + h * dh + ch * 8);
+      src = a.qkv + (size_t)(b * a.H + tok) * qkvdim + h * dh + ch * 8;
+      bytes = 16;
     }
-    *reinterpret_cast<uint4*>(smem + L.q + (ch >> 3) * 128 * 128 + sw128_offset(row, ch & 7)) = v;
+    cp_async16(smem + L.q + (ch >> 3) * 128 * 128 + sw128_offset(row, ch & 7), src, bytes);
   }
+  load_chunk(c_begin, 0);
+  cp_async_commit();
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -115,37 +167,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
   float m_ref = -INFINITY, l = 0.f;
   bool failed = false;
 
-  for (int c = c_begin, ci = 0; c < c_end; ++c, ++ci) {
-    const int key0 = c * kChunk;
-    const int nk = min(kChunk, n_keys - key0);
-    // ---- K chunk (B operand of S: N = keys, K = dh) and V^T (B operand of O:
-    //      N = dh, K = keys) of KV head g; keys past the end are zero.
-    for (int i = threadIdx.x; i < kChunk * (dh / 8); i += kAttnThreads) {
-      const int j = i / (dh / 8), ch = i % (dh / 8);
-      uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
-      if (j < nk) {
-        const int key = key0 + j;
-        if (key < n_pre) {
-          const int prow = a.valid_idx[(size_t)b * a.max_rows + key];
-          if (prow >= 0 && prow < a.total_rows) {
-            kv = *reinterpret_cast<const uint4*>(a.pk + (size_t)prow * kvdim + g * dh + ch * 8);
-            vv = *reinterpret_cast<const uint4*>(a.pv + (size_t)prow * kvdim + g * dh + ch * 8);
-          } else {
-            report(a.status, kDevBounds);
-          }
-        } else {
-          const bf16* base = a.qkv + (size_t)(b * a.H + (key - n_pre)) * qkvdim;
-          kv = *reinterpret_cast<const uint4*>(base + (a.Hq + g) * dh + ch * 8);
-          vv = *reinterpret_cast<const uint4*>(base + (a.Hq + a.Hkv + g) * dh + ch * 8);
-        }
-      }
-      *reinterpret_cast<uint4*>(smem + L.k + (ch >> 3) * kChunk * 128 + sw128_offset(j, ch & 7)) = kv;
-      const bf16* ve = reinterpret_cast<const bf16*>(&vv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        bf16* dst = reinterpret_cast<bf16*>(smem + L.vt + sw128_offset(ch * 8 + e, j >> 3)) + (j & 7);
-        *dst = ve[e];
-      }
+  for (int ci = 0; ci < n_my; ++ci) {
+    const int c = c_begin + ci;
+    const int buf = ci & 1;
+    const int nk = min(kChunk, n_keys - c * kChunk);
+    // prefetch the next chunk into the other buffer (its last reader, the
+    // previous chunk's P V, completed before this iteration began)
+    if (ci + 1 < n_my) {
+      load_chunk(c + 1, buf ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -156,7 +189,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
       const uint32_t idesc = idesc_bf16(128, kChunk);
       for (int kb = 0; kb < kdb; ++kb) {
         const uint64_t ad = sdesc_sw128(smem_u32(smem + L.q + kb * 128 * 128));
-        const uint64_t bd = sdesc_sw128(smem_u32(smem + L.k + kb * kChunk * 128));
+        const uint64_t bd = sdesc_sw128(smem_u32(smem + L.k[buf] + kb * kChunk * 128));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_bf16(tm_s, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
@@ -219,13 +252,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // ---- O += P V
+    // ---- O += P V   (V as the MN-major operand: 16 keys = two 8-key atoms per step)
     if (threadIdx.x == 0) {
-      const uint32_t idesc = idesc_bf16(128, dh);
+      const uint32_t idesc = idesc_bf16(128, dh, true);
       const uint64_t ad = sdesc_sw128(smem_u32(smem + L.p));
-      const uint64_t bd = sdesc_sw128(smem_u32(smem + L.vt));
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mma_bf16(tm_o, ad + 2 * k, bd + 2 * k, idesc, (ci > 0 || k > 0) ? 1u : 0u);
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t bd = sdesc_sw128_mn(smem_u32(smem + L.v[buf] + k * 2 * v_sbo), 1024, v_sbo);
+        mma_bf16(tm_o, ad + 2 * k, bd, idesc, (ci > 0 || k > 0) ? 1u : 0u);
+      }
       mma_commit(bar_o);
     }
     ok = 1;
@@ -236,6 +271,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
     }
     tc_fence_after();
   }
+  cp_async_wait<0>();
   if (!failed) {
     const int r = qt * 128 + row;
     const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;

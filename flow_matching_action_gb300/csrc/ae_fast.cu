@@ -38,13 +38,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, K] row-major; boxes of 128 rows x 64 columns, 128-byte swizzle.
-cudaError_t make_weight_map(CUtensorMap* map, const void* ptr, long rows, long K) {
+// bf16 matrix [rows, K] row-major; boxes of box_rows rows x 64 columns, 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* map, const void* ptr, long rows, long K, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -68,19 +68,26 @@ bool fast_path_supported(const Dims& d, std::string* why) {
 }
 
 size_t fast_part_floats(const Dims& d, int max_batch, int sm_count) {
-  // ksplit * M <= sm_count * 256 / n_tiles, so ksplit * M * N <= sm_count * 256 * 128
-  (void)d;
-  (void)max_batch;
-  return (size_t)sm_count * 256 * 128;
+  // a split chosen to fill the GPU has ksplit * M <= sm_count * 256 / n_tiles, so
+  // ksplit * M * N <= sm_count * 256 * 128; the O and down projections always
+  // split at least 2 ways
+  const size_t maxM = (size_t)max_batch * d.H;
+  const size_t a = (size_t)sm_count * 256 * 128;
+  const size_t b = 2 * maxM * (size_t)d.D;
+  return a > b ? a : b;
 }
 
 cudaError_t fast_setup(ae_ctx* c) {
   const Dims& d = c->d;
   cudaError_t e;
-  if ((e = make_weight_map(&c->map_qkv, c->w_qkv, (long)d.L * d.qkvdim(), d.D)) != cudaSuccess) return e;
-  if ((e = make_weight_map(&c->map_o, c->w_o, (long)d.L * d.D, d.qdim())) != cudaSuccess) return e;
-  if ((e = make_weight_map(&c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D)) != cudaSuccess) return e;
-  if ((e = make_weight_map(&c->map_d, c->w_d, (long)d.L * d.D, d.F)) != cudaSuccess) return e;
+  const long maxM = (long)c->max_batch * d.H;
+  if ((e = make_map(&c->map_qkv, c->w_qkv, (long)d.L * d.qkvdim(), d.D, 128)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_o, c->w_o, (long)d.L * d.D, d.qdim(), 128)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D, 128)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_d, c->w_d, (long)d.L * d.D, d.F, 128)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_y, c->y, maxM, d.D, 16)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_oact, c->o, maxM, d.qdim(), 16)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_mact, c->m, maxM, d.F, 16)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
@@ -91,15 +98,16 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const int nqkv = d.qkvdim(), qd = d.qdim();
   const float eps = (float)d.eps;
   const int sm = c->sm_count;
-  const GemmPlan pq = plan_gemm(nqkv, D, M, sm, true);
-  const GemmPlan po = plan_gemm(D, qd, M, sm, true);
-  const GemmPlan pg = plan_gemm(2 * F, D, M, sm, true);
-  const GemmPlan pd = plan_gemm(D, F, M, sm, true);
+  const GemmPlan pq = plan_gemm(nqkv, D, M, sm, 1);
+  const GemmPlan po = plan_gemm(D, qd, M, sm, 2);
+  const GemmPlan pg = plan_gemm(2 * F, D, M, sm, 1);
+  const GemmPlan pd = plan_gemm(D, F, M, sm, 2);
   float* part0 = c->part;
   float* part1 = c->part + c->part_floats;
   bf16* qkv = (bf16*)c->qkv;
   bf16* o = (bf16*)c->o;
   bf16* m = (bf16*)c->m;
+  bf16* y = (bf16*)c->y;
   int n = 0;
   *err = cudaSuccess;
   auto ck = [&](cudaError_t e) {
@@ -110,26 +118,22 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     float* dst = c->dump + (((size_t)step * (L + 1) + l) * M) * D;
     ck(cudaMemcpyAsync(dst, c->h, (size_t)M * D * sizeof(float), cudaMemcpyDeviceToDevice, s));
   };
+  auto mod = [&](int l, int j) { return t.mod + (((size_t)step * L + l) * 2 + j) * 3 * D; };
 
-  launch_inproj_tc(x, (const bf16*)c->w_in, (const bf16*)c->b_in, c->h, c->sumsq, M, D, d.A, s);
+  // h = x W_in^T + b_in; y = adaRMS1 of layer 0
+  launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0),
+                     mod(0, 0) + D, eps, y, s);
   ++n;
   for (int l = 0; l < L; ++l) {
     dump(l);
-    const float* mod1 = t.mod + (((size_t)step * L + l) * 2 + 0) * 3 * D;
-    const float* mod2 = mod1 + 3 * D;
+    const float* mod1 = mod(l, 0);
+    const float* mod2 = mod(l, 1);
 
-    // adaRMS1 -> merged QKV -> RoPE
+    // merged QKV (+ RoPE)
     TcGemmArgs a = {};
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * nqkv;
-    a.b_mode = kBRms;
-    a.h = c->h;
-    a.sumsq = c->sumsq;
-    a.n_sumsq = D / 128;
-    a.scale = mod1;
-    a.shift = mod1 + D;
-    a.eps = eps;
     a.rope_cs = c->rope_cs;
     a.dh = d.dh;
     a.n_rot_heads = d.Hq + d.Hkv;
@@ -140,13 +144,14 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       a.e_mode = kEPartial;
       a.part = part0;
     }
-    ck(launch_tc_gemm(c->map_qkv, pq, a, s));
+    ck(launch_tc_gemm(c->map_qkv, c->map_y, pq, a, s));
     ++n;
     if (pq.ksplit > 1) {
       launch_reduce_qkv(part0, pq.ksplit, M, nqkv, d.dh, d.Hq + d.Hkv, c->rope_cs, qkv, s);
       ++n;
     }
 
+    // attention over [valid prefix || actions]
     {
       AttnArgs at = {};
       const long lay = (long)l * c->bind.total_rows * d.kvdim();
@@ -171,41 +176,22 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       n += 2;
     }
 
-    // O projection -> gated residual
+    // O projection -> gated residual -> adaRMS2
     a = TcGemmArgs{};
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * D;
-    a.b_mode = kBCopy;
-    a.act = o;
-    if (po.ksplit == 1) {
-      a.e_mode = kEResid;
-      a.h_out = c->h;
-      a.gate = mod1 + 2 * D;
-      a.sumsq_out = c->sumsq;
-    } else {
-      a.e_mode = kEPartial;
-      a.part = part0;
-    }
-    ck(launch_tc_gemm(c->map_o, po, a, s));
-    ++n;
-    if (po.ksplit > 1) {
-      launch_reduce_resid(part0, po.ksplit, M, D, c->h, mod1 + 2 * D, c->sumsq, s);
-      ++n;
-    }
+    a.e_mode = kEPartial;
+    a.part = part0;
+    ck(launch_tc_gemm(c->map_o, c->map_oact, po, a, s));
+    launch_resid_norm(part0, po.ksplit, M, D, c->h, mod1 + 2 * D, mod2, mod2 + D, eps, y, s);
+    n += 2;
 
-    // adaRMS2 -> merged gate/up (-> GeGLU when not split)
+    // merged gate/up -> GeGLU
     a = TcGemmArgs{};
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * 2 * F;
-    a.b_mode = kBRms;
-    a.h = c->h;
-    a.sumsq = c->sumsq;
-    a.n_sumsq = D / 128;
-    a.scale = mod2;
-    a.shift = mod2 + D;
-    a.eps = eps;
     if (pg.ksplit == 1) {
       a.e_mode = kEGeglu;
       a.out_bf16 = m;
@@ -213,38 +199,25 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       a.e_mode = kEPartial;
       a.part = part0;
     }
-    ck(launch_tc_gemm(c->map_gu, pg, a, s));
+    ck(launch_tc_gemm(c->map_gu, c->map_y, pg, a, s));
     ++n;
+    if (pg.ksplit > 1) {
+      launch_geglu_reduce(part0, pg.ksplit, M, F, m, s);
+      ++n;
+    }
 
-    // (GeGLU of the partials ->) down projection -> gated residual
+    // down projection -> gated residual -> adaRMS1 of the next layer
     a = TcGemmArgs{};
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * D;
-    if (pg.ksplit == 1) {
-      a.b_mode = kBCopy;
-      a.act = m;
-    } else {
-      a.b_mode = kBGeglu;
-      a.gu_part = part0;
-      a.gu_ks = pg.ksplit;
-      a.gu_ld = 2L * F;
-    }
-    if (pd.ksplit == 1) {
-      a.e_mode = kEResid;
-      a.h_out = c->h;
-      a.gate = mod2 + 2 * D;
-      a.sumsq_out = c->sumsq;
-    } else {
-      a.e_mode = kEPartial;
-      a.part = part1;
-    }
-    ck(launch_tc_gemm(c->map_d, pd, a, s));
-    ++n;
-    if (pd.ksplit > 1) {
-      launch_reduce_resid(part1, pd.ksplit, M, D, c->h, mod2 + 2 * D, c->sumsq, s);
-      ++n;
-    }
+    a.e_mode = kEPartial;
+    a.part = part1;
+    ck(launch_tc_gemm(c->map_d, c->map_mact, pd, a, s));
+    const float* nxt = l + 1 < L ? mod(l + 1, 0) : nullptr;
+    launch_resid_norm(part1, pd.ksplit, M, D, c->h, mod2 + 2 * D, nxt, nxt ? nxt + D : nullptr, eps,
+                      y, s);
+    n += 2;
   }
   dump(L);
   n += launch_final_bf16(c, t, step, x, s);

@@ -1,23 +1,20 @@
-// tcgen05 GEMMs of the bf16 path with the layer's elementwise work fused in.
+// tcgen05 GEMMs of the bf16 path and the elementwise kernels between them.
 //
 // Swap-AB: a CTA computes a 128-row slab of a weight matrix against a tile of
 // up to 256 action tokens, D[n, t] = sum_k W[n, k] X[t, k].  The weight rows
-// are the MMA's M = 128 operand (streamed by TMA into 128-byte-swizzled shared
-// memory, evict-first in L2: each weight is read once per flow step), the
-// token tile is the MMA's N operand, so a 50-token chunk costs a 64-wide
-// tile instead of a 128-row one.  The accumulator lives in TMEM.
-//
-// The token operand is produced by threads, so the layer's prologue is fused:
-//   kBRms    adaRMS of the fp32 residual stream (LoongForge Pi0.5 blog,
-//            section 2: rms over the row, (1 + scale), + shift), cast to bf16;
-//   kBCopy   a bf16 activation (attention output, GeGLU output);
-//   kBGeglu  GeGLU of split-K partials of the merged gate/up projection.
-// The epilogue fuses what follows the projection:
-//   kEQkvRope   RoPE (rotate_half pairs) on q and k, bf16 store of q|k|v;
-//   kEResid     gated residual h += gate * acc and the adaRMS sum of squares;
-//   kEGeglu     gelu_tanh(g) * u from the merged gate/up rows;
-//   kEPartial   fp32 split-K partials, summed in a fixed order later.
+// are the MMA's M = 128 operand and the token tile is its N operand, so a
+// 50-token chunk costs a 64-wide tile instead of a 128-row one.  Both operands
+// arrive by TMA into 128-byte-swizzled shared memory (weights evict-first in
+// L2: each is read once per flow step); the fp32 accumulator lives in TMEM.
 // Merged Q/K/V and gate/up weights follow sglang PR #34599, item 1.
+//
+// Epilogues:
+//   kEQkvRope   RoPE (rotate_half pairs) on q and k, bf16 q|k|v store
+//   kEGeglu     gelu_tanh(g) * u of the interleaved gate/up rows, bf16 store
+//   kEPartial   fp32 split-K partials, summed in split order later
+// The kernels after the GEMMs fuse the rest of the layer (LoongForge Pi0.5
+// blog, section 2): split-K sum + gated residual + the NEXT adaRMS (rms over
+// the row, (1 + scale), + shift) into the bf16 operand of the next GEMM.
 #include <math.h>
 
 #include "ae_internal.h"
@@ -28,17 +25,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
-constexpr int kProducerThreads = 192;  // warps 2..7
-constexpr int kATileBytes = 128 * 128; // 128 weight rows x 64 bf16
+constexpr int kThreads = 192;           // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kATileBytes = 128 * 128;  // 128 weight rows x 64 bf16
+constexpr int kBBoxRows = 16;           // token rows per activation TMA box
 
 __device__ __forceinline__ float gelu_tanh(float g) {
   return 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -51,54 +43,9 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Produce the 8 bf16 values of token tg, features k..k+7 of the token operand.
-__device__ __forceinline__ uint4 produce_chunk(const TcGemmArgs& a, int tg, int k, float r) {
-  uint4 out;
-  if (a.b_mode == kBCopy) {
-    out = *reinterpret_cast<const uint4*>(a.act + (size_t)tg * a.K + k);
-  } else if (a.b_mode == kBRms) {
-    const float4* hp = reinterpret_cast<const float4*>(a.h + (size_t)tg * a.K + k);
-    const float4* sp = reinterpret_cast<const float4*>(a.scale + k);
-    const float4* tp = reinterpret_cast<const float4*>(a.shift + k);
-    float x[8], s[8], t[8];
-    *reinterpret_cast<float4*>(x) = hp[0];
-    *reinterpret_cast<float4*>(x + 4) = hp[1];
-    *reinterpret_cast<float4*>(s) = sp[0];
-    *reinterpret_cast<float4*>(s + 4) = sp[1];
-    *reinterpret_cast<float4*>(t) = tp[0];
-    *reinterpret_cast<float4*>(t + 4) = tp[1];
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = x[e] * r * (1.f + s[e]) + t[e];
-    out = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                     pack_bf16(y[6], y[7]));
-  } else {  // kBGeglu: partial rows hold (g_j, u_j) pairs
-    float g[8], u[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) g[e] = u[e] = 0.f;
-    for (int j = 0; j < a.gu_ks; ++j) {
-      const float4* p =
-          reinterpret_cast<const float4*>(a.gu_part + ((size_t)j * a.M + tg) * a.gu_ld + 2 * k);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = p[q];
-        g[2 * q] += v.x;
-        u[2 * q] += v.y;
-        g[2 * q + 1] += v.z;
-        u[2 * q + 1] += v.w;
-      }
-    }
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = gelu_tanh(g[e]) * u[e];
-    out = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                     pack_bf16(y[6], y[7]));
-  }
-  return out;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
-    k_tc_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ TcGemmArgs a) {
+    k_tc_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
+              const __grid_constant__ TcGemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int S = a.stages;
@@ -110,8 +57,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = empty + S;
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(tmem_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
-  float* rms = reinterpret_cast<float*>(tmem_base_p + 4);       // [tok_tile]
-  float* red = rms + a.tok_tile;                                  // [4][16] + 4 votes
+  volatile int* votes = reinterpret_cast<volatile int*>(tmem_base_p + 2);  // [4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int idx = blockIdx.x;
@@ -126,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + kProducerThreads / 32);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
@@ -144,18 +90,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_d = *tmem_base_p;
 
   if (warp == 0) {
-    // ---------------- weight producer (TMA)
+    // ---------------- TMA producer: weight slab + token tile per 64-wide K block
     if (lane == 0) {
       prefetch_tensormap(&wmap);
-      const uint64_t pol = policy_evict_first();
+      prefetch_tensormap(&amap);
+      const uint64_t pol_w = policy_evict_first();
       const int row = a.w_row0 + n_tile * 128;
+      const uint32_t bytes = kATileBytes + (uint32_t)btile;
       int it = 0;
       for (; it < n_it; ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status)) break;
-        mbar_arrive_expect_tx(&full[s], kATileBytes);
-        tma_load_2d(smA + (size_t)s * kATileBytes, &wmap, &full[s], (kb_begin + it) * 64, row, pol);
+        const int kc = (kb_begin + it) * 64;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        tma_load_2d(smA + (size_t)s * kATileBytes, &wmap, &full[s], kc, row, pol_w);
+        uint8_t* bs = smB + (size_t)s * btile;
+        for (int r = 0; r < a.tok_tile; r += kBBoxRows)
+          tma_load_2d_nohint(bs + r * 128, &amap, &full[s], kc, t0 + r);
       }
       // drain: no copy may still be in flight when the CTA exits
       for (int j = it - S > 0 ? it - S : 0; j < it; ++j)
@@ -180,114 +132,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(tmem_full);
     }
   } else {
-    // ---------------- token-operand producers (warps 2..7)
-    const int ptid = threadIdx.x - 64;
-    if (a.b_mode == kBRms) {
-      for (int t = ptid; t < a.tok_tile; t += kProducerThreads) {
-        const int tg = t0 + t;
-        float r = 0.f;
-        if (tg < a.M) {
-          float ss = 0.f;
-          for (int j = 0; j < a.n_sumsq; ++j) ss += a.sumsq[(size_t)j * a.M + tg];
-          r = 1.0f / sqrtf(ss / (float)a.K + a.eps);
-        }
-        rms[t] = r;
-      }
-      named_bar(1, kProducerThreads);
-    }
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % S;
-      const uint32_t ph = (uint32_t)(it / S) & 1u;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      uint8_t* bs = smB + (size_t)s * btile;
-      const int kb = kb_begin + it;
-      for (int c = ptid; c < a.tok_tile * 8; c += kProducerThreads) {
-        const int t = c >> 3, ch = c & 7;
-        const int tg = t0 + t;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tg < a.M) v = produce_chunk(a, tg, kb * 64 + ch * 8, rms[t]);
-        *reinterpret_cast<uint4*>(bs + sw128_offset(t, ch)) = v;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
-    }
-
-    // ---------------- epilogue (warps 4..7: TMEM lanes 32*(warp%4) ..)
-    if (warp >= 4) {
-      const int q = warp & 3;
-      const int rowl = 32 * q + lane;
-      const int n = n_tile * 128 + rowl;
-      // every epilogue warp takes the same decision: a mismatch would leave a
-      // named barrier below waiting forever
-      volatile int* votes = reinterpret_cast<volatile int*>(red + 64);
-      if (lane == 0) votes[q] = (mbar_wait(tmem_full, 0, abort_flag, a.status) && !*abort_flag) ? 1 : 0;
-      named_bar(3, 128);
-      const bool go = votes[0] && votes[1] && votes[2] && votes[3];
-      if (go) {
-        tc_fence_after();
-        for (int c0 = 0; c0 < a.tok_tile; c0 += 16) {
-          float v[16];
-          tmem_ld16(tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-          if (a.e_mode == kEPartial) {
+    // ---------------- epilogue (warps 2..5: TMEM lanes 32 * (warp % 4) ..)
+    const int q = warp & 3;
+    const int n = n_tile * 128 + 32 * q + lane;
+    // every epilogue warp takes the same decision
+    if (lane == 0) votes[q] = (mbar_wait(tmem_full, 0, abort_flag, a.status) && !*abort_flag) ? 1 : 0;
+    named_bar(1, 128);
+    const bool go = votes[0] && votes[1] && votes[2] && votes[3];
+    if (go) {
+      tc_fence_after();
+      for (int c0 = 0; c0 < a.tok_tile; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+        if (a.e_mode == kEPartial) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int t = t0 + c0 + j;
-              if (t < a.M) a.part[((size_t)ks * a.M + t) * a.N + n] = v[j];
-            }
-          } else if (a.e_mode == kEQkvRope) {
-            const int half = a.dh >> 1;
-            const int hb = n / a.dh, p = n - hb * a.dh;
-            const int pair = p >> 1, odd = p & 1;
-            const bool rot = hb < a.n_rot_heads;
+          for (int j = 0; j < 16; ++j) {
+            const int t = t0 + c0 + j;
+            if (t < a.M) a.part[((size_t)ks * a.M + t) * a.N + n] = v[j];
+          }
+        } else if (a.e_mode == kEQkvRope) {
+          const int half = a.dh >> 1;
+          const int hb = n / a.dh, p = n - hb * a.dh;
+          const int pair = p >> 1, odd = p & 1;
+          const bool rot = hb < a.n_rot_heads;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-              const int t = t0 + c0 + j;
-              if (t < a.M) {
-                float outv = v[j];
-                if (rot) {
-                  const float2 cs = a.rope_cs[(size_t)t * half + pair];
-                  const float x1 = odd ? other : v[j], x2 = odd ? v[j] : other;
-                  outv = odd ? (x2 * cs.x + x1 * cs.y) : (x1 * cs.x - x2 * cs.y);
-                }
-                a.out_bf16[(size_t)t * a.N + hb * a.dh + pair + odd * half] = __float2bfloat16_rn(outv);
+          for (int j = 0; j < 16; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            const int t = t0 + c0 + j;
+            if (t < a.M) {
+              float outv = v[j];
+              if (rot) {
+                const float2 cs = a.rope_cs[(size_t)t * half + pair];
+                const float x1 = odd ? other : v[j], x2 = odd ? v[j] : other;
+                outv = odd ? (x2 * cs.x + x1 * cs.y) : (x1 * cs.x - x2 * cs.y);
               }
+              a.out_bf16[(size_t)t * a.N + hb * a.dh + pair + odd * half] = __float2bfloat16_rn(outv);
             }
-          } else if (a.e_mode == kEGeglu) {
+          }
+        } else {  // kEGeglu
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-              const int t = t0 + c0 + j;
-              if (t < a.M && !(n & 1))
-                a.out_bf16[(size_t)t * (a.N >> 1) + (n >> 1)] = __float2bfloat16_rn(gelu_tanh(v[j]) * other);
-            }
-          } else {  // kEResid
-            const float g = a.gate[n];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int t = t0 + c0 + j;
-              float sq = 0.f;
-              if (t < a.M) {
-                float* hp = a.h_out + (size_t)t * a.N + n;
-                const float hn = *hp + g * v[j];
-                *hp = hn;
-                sq = hn * hn;
-              }
-              sq = warp_sum(sq);
-              if (lane == 0) red[q * 16 + j] = sq;
-            }
-            named_bar(2, 128);
-            if (q == 0 && lane < 16) {
-              const int t = t0 + c0 + lane;
-              if (t < a.M)
-                a.sumsq_out[(size_t)n_tile * a.M + t] =
-                    red[lane] + red[16 + lane] + red[32 + lane] + red[48 + lane];
-            }
-            named_bar(2, 128);
+          for (int j = 0; j < 16; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            const int t = t0 + c0 + j;
+            if (t < a.M && !(n & 1))
+              a.out_bf16[(size_t)t * (a.N >> 1) + (n >> 1)] = __float2bfloat16_rn(gelu_tanh(v[j]) * other);
           }
         }
       }
@@ -297,18 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     // the last commit tracks every MMA this CTA issued: wait for it before freeing TMEM
-    if (*abort_flag) {
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(tmem_full, 0, abort_flag, a.status);
-      __syncwarp();
-      (void)ok;
-    }
+    if (*abort_flag && lane == 0) mbar_wait(tmem_full, 0, abort_flag, a.status);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_d, tmem_cols);
   }
 }
 
-// ---------------------------------------------------------------- split-K reductions
+// ---------------------------------------------------------------- between the GEMMs
 // Sum the split-K partials of the merged QKV projection in split order, apply
 // RoPE to q and k, store q|k|v in natural head layout.  One thread per rotation pair.
 __global__ void k_reduce_qkv(const float* __restrict__ part, int ks_n, int M, int N, int dh,
@@ -336,53 +220,97 @@ __global__ void k_reduce_qkv(const float* __restrict__ part, int ks_n, int M, in
   out[(size_t)t * N + hb * dh + pair + half] = __float2bfloat16_rn(o2);
 }
 
-// Sum split-K partials in split order, gated residual, adaRMS sum of squares
-// per 128-feature tile.  Block = one (feature tile, token).
-__global__ void __launch_bounds__(128) k_reduce_resid(const float* __restrict__ part, int ks_n,
-                                                      int M, int N, float* __restrict__ h,
-                                                      const float* __restrict__ gate,
-                                                      float* __restrict__ sumsq) {
-  const int tile = blockIdx.x, t = blockIdx.y;
-  const int n = tile * 128 + threadIdx.x;
-  float s = 0.f;
-  for (int j = 0; j < ks_n; ++j) s += part[((size_t)j * M + t) * N + n];
-  float* hp = h + (size_t)t * N + n;
-  const float hn = *hp + gate[n] * s;
-  *hp = hn;
-  __shared__ float wsum[4];
-  float sq = warp_sum(hn * hn);
-  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = sq;
+constexpr int kRowThreads = 256;
+
+__device__ float block_sum_256(float v, float* red) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  if (threadIdx.x == 0) sumsq[(size_t)tile * M + t] = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kRowThreads / 32; ++w) t += red[w];
+  return t;
 }
 
-// Action input projection h = x W_in^T + b_in, plus the sum of squares per
-// 128-feature tile for the first adaRMS.  Block = one (feature tile, token).
-__global__ void __launch_bounds__(128) k_inproj_tc(const float* __restrict__ x,
-                                                   const bf16* __restrict__ w_in,
-                                                   const bf16* __restrict__ b_in, float* __restrict__ h,
-                                                   float* __restrict__ sumsq, int M, int D, int A) {
-  const int tile = blockIdx.x, t = blockIdx.y;
-  const int n = tile * 128 + threadIdx.x;
-  float s = 0.f;
-  for (int k = 0; k < A; ++k) s += x[(size_t)t * A + k] * __bfloat162float(w_in[(size_t)n * A + k]);
-  const float hn = s + __bfloat162float(b_in[n]);
-  h[(size_t)t * D + n] = hn;
-  __shared__ float wsum[4];
-  float sq = warp_sum(hn * hn);
-  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = sq;
+// One token row: h += gate * (sum of the split-K partials, in split order);
+// then, if `scale` is given, y = adaRMS(h) with the next sublayer's
+// (scale, shift) as the bf16 operand of the next GEMM.
+__global__ void __launch_bounds__(kRowThreads) k_resid_norm(const float* __restrict__ part, int ks_n,
+                                                           int M, int D, float* __restrict__ h,
+                                                           const float* __restrict__ gate,
+                                                           const float* __restrict__ scale,
+                                                           const float* __restrict__ shift, float eps,
+                                                           bf16* __restrict__ y) {
+  __shared__ float red[kRowThreads / 32];
+  const int t = blockIdx.x;
+  float* hr = h + (size_t)t * D;
+  float ss = 0.f;
+  for (int n = threadIdx.x; n < D; n += kRowThreads) {
+    float s = 0.f;
+    for (int j = 0; j < ks_n; ++j) s += part[((size_t)j * M + t) * D + n];
+    const float hn = hr[n] + gate[n] * s;
+    hr[n] = hn;
+    ss += hn * hn;
+  }
+  if (scale == nullptr) return;
+  ss = block_sum_256(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)D + eps);
+  for (int n = threadIdx.x; n < D; n += kRowThreads)
+    y[(size_t)t * D + n] = __float2bfloat16_rn(hr[n] * r * (1.f + scale[n]) + shift[n]);
+}
+
+// Action input projection h = x W_in^T + b_in of one token row, then the first
+// layer's adaRMS into the bf16 operand of its QKV GEMM.
+__global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __restrict__ x,
+                                                            const bf16* __restrict__ w_in,
+                                                            const bf16* __restrict__ b_in, int D, int A,
+                                                            float* __restrict__ h,
+                                                            const float* __restrict__ scale,
+                                                            const float* __restrict__ shift, float eps,
+                                                            bf16* __restrict__ y) {
+  __shared__ float red[kRowThreads / 32];
+  extern __shared__ float xs[];
+  const int t = blockIdx.x;
+  for (int k = threadIdx.x; k < A; k += kRowThreads) xs[k] = x[(size_t)t * A + k];
   __syncthreads();
-  if (threadIdx.x == 0) sumsq[(size_t)tile * M + t] = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+  float* hr = h + (size_t)t * D;
+  float ss = 0.f;
+  for (int n = threadIdx.x; n < D; n += kRowThreads) {
+    float s = 0.f;
+    for (int k = 0; k < A; ++k) s += xs[k] * __bfloat162float(w_in[(size_t)n * A + k]);
+    const float hn = s + __bfloat162float(b_in[n]);
+    hr[n] = hn;
+    ss += hn * hn;
+  }
+  ss = block_sum_256(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)D + eps);
+  for (int n = threadIdx.x; n < D; n += kRowThreads)
+    y[(size_t)t * D + n] = __float2bfloat16_rn(hr[n] * r * (1.f + scale[n]) + shift[n]);
+}
+
+// GeGLU of the split-K partials of the interleaved gate/up projection:
+// m[t][j] = gelu_tanh(sum g) * (sum u), sums in split order.
+__global__ void k_geglu_reduce(const float* __restrict__ part, int ks_n, int M, int F,
+                               bf16* __restrict__ m) {
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)M * F) return;
+  const int t = (int)(idx / F), j = (int)(idx - (long)t * F);
+  float g = 0.f, u = 0.f;
+  for (int s = 0; s < ks_n; ++s) {
+    const float2 v = *reinterpret_cast<const float2*>(part + ((size_t)s * M + t) * 2 * F + 2 * j);
+    g += v.x;
+    u += v.y;
+  }
+  m[idx] = __float2bfloat16_rn(gelu_tanh(g) * u);
 }
 
 }  // namespace
 
 size_t tc_gemm_smem_bytes(int stages, int tok_tile) {
-  return 1024 + (size_t)stages * (kATileBytes + (size_t)tok_tile * 128) + (2 * stages + 1) * 8 +
-         16 + (size_t)tok_tile * 4 + 68 * 4;
+  return 1024 + (size_t)stages * (kATileBytes + (size_t)tok_tile * 128) + (2 * stages + 1) * 8 + 32;
 }
 
-GemmPlan plan_gemm(int N, int K, int M, int sm_count, bool allow_split) {
+GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split) {
   GemmPlan p;
   p.N = N;
   p.K = K;
@@ -395,22 +323,27 @@ GemmPlan plan_gemm(int N, int K, int M, int sm_count, bool allow_split) {
   p.tok_tile = tt;
   p.kb_total = K / 64;
   const int base = p.n_tiles * p.tok_tiles;
-  int ks = allow_split ? sm_count / base : 1;
+  int ks = sm_count / base;
+  if (ks < min_split) ks = min_split;
   if (ks < 1) ks = 1;
   if (ks > p.kb_total) ks = p.kb_total;
   p.ksplit = ks;
   int cols = 32;
   while (cols < tt) cols <<= 1;
   p.tmem_cols = cols;
-  int stages = 8;
-  while (stages > 2 && tc_gemm_smem_bytes(stages, tt) > 220 * 1024) --stages;
+  // as many stages as a CTA has K blocks, within the shared-memory budget
+  const int per_cta = (p.kb_total + ks - 1) / ks;
+  int stages = per_cta < 8 ? per_cta : 8;
+  if (stages < 2) stages = 2;
+  while (stages > 2 && tc_gemm_smem_bytes(stages, tt) > 200 * 1024) --stages;
   p.stages = stages;
   p.smem = tc_gemm_smem_bytes(stages, tt);
   p.grid = base * ks;
   return p;
 }
 
-cudaError_t launch_tc_gemm(const CUtensorMap& map, const GemmPlan& p, TcGemmArgs a, cudaStream_t s) {
+cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
+                           TcGemmArgs a, cudaStream_t s) {
   a.N = p.N;
   a.K = p.K;
   a.tok_tile = p.tok_tile;
@@ -427,7 +360,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& map, const GemmPlan& p, TcGemmArgs
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_tc_gemm<<<p.grid, kThreads, p.smem, s>>>(map, a);
+  k_tc_gemm<<<p.grid, kThreads, p.smem, s>>>(wmap, amap, a);
   return cudaGetLastError();
 }
 
@@ -437,14 +370,20 @@ void launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_ro
   k_reduce_qkv<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, ks, M, N, dh, n_rot_heads, cs, out);
 }
 
-void launch_reduce_resid(const float* part, int ks, int M, int N, float* h, const float* gate,
-                         float* sumsq, cudaStream_t s) {
-  k_reduce_resid<<<dim3(N / 128, M), 128, 0, s>>>(part, ks, M, N, h, gate, sumsq);
+void launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
+                       const float* scale, const float* shift, float eps, bf16* y, cudaStream_t s) {
+  k_resid_norm<<<M, kRowThreads, 0, s>>>(part, ks, M, D, h, gate, scale, shift, eps, y);
 }
 
-void launch_inproj_tc(const float* x, const bf16* w_in, const bf16* b_in, float* h, float* sumsq,
-                      int M, int D, int A, cudaStream_t s) {
-  k_inproj_tc<<<dim3(D / 128, M), 128, 0, s>>>(x, w_in, b_in, h, sumsq, M, D, A);
+void launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
+                        float* h, const float* scale, const float* shift, float eps, bf16* y,
+                        cudaStream_t s) {
+  k_inproj_norm<<<M, kRowThreads, A * sizeof(float), s>>>(x, w_in, b_in, D, A, h, scale, shift, eps, y);
+}
+
+void launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s) {
+  const long n = (long)M * F;
+  k_geglu_reduce<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, ks, M, F, m);
 }
 
 }  // namespace ae

@@ -103,7 +103,8 @@ struct ae_ctx {
   // bf16 tensor-core path: TMA descriptors of the stacked per-layer weights
   // (rows of layer l start at l * rows-per-layer) and its extra scratch.
   bool fast = false;
-  CUtensorMap map_qkv, map_o, map_gu, map_d;
+  CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
+  CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes 16 rows x 64
   float* sumsq = nullptr;    // [D/128][M] adaRMS sum of squares per 128-feature tile
   float* part = nullptr;     // split-K partials
   size_t part_floats = 0;
@@ -139,32 +140,17 @@ int launch_attn_bf16(ae_ctx* c, int layer, cudaStream_t s);
 int launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s);
 
 // ---- tensor-core GEMM (ae_gemm_tc.cu)
-enum BMode : int { kBRms = 0, kBCopy = 1, kBGeglu = 2 };
-enum EMode : int { kEPartial = 0, kEQkvRope = 1, kEResid = 2, kEGeglu = 3 };
+enum EMode : int { kEPartial = 0, kEQkvRope = 1, kEGeglu = 2 };
 
 struct TcGemmArgs {
   int M, N, K;          // tokens, output features, reduction length
   int w_row0;           // first row of this layer's matrix in the stacked weight
   int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
-  int b_mode;
-  const float* h;       // kBRms: fp32 [M, K]
-  const float* sumsq;   // kBRms: [n_sumsq][M]
-  int n_sumsq;
-  const float* scale;   // kBRms: [K]
-  const float* shift;   // kBRms: [K]
-  float eps;
-  const bf16* act;      // kBCopy: bf16 [M, K]
-  const float* gu_part; // kBGeglu: [gu_ks][M][gu_ld] with (g_j, u_j) adjacent
-  int gu_ks;
-  long gu_ld;
   int e_mode;
   float* part;          // kEPartial: [ksplit][M][N]
   bf16* out_bf16;       // kEQkvRope: [M][N]; kEGeglu: [M][N/2]
   const float2* rope_cs;
   int dh, n_rot_heads;
-  float* h_out;         // kEResid: fp32 [M][N], updated in place
-  const float* gate;    // kEResid: [N]
-  float* sumsq_out;     // kEResid: [N/128][M]
   int* status;
 };
 
@@ -174,14 +160,17 @@ struct GemmPlan {
 };
 
 size_t tc_gemm_smem_bytes(int stages, int tok_tile);
-GemmPlan plan_gemm(int N, int K, int M, int sm_count, bool allow_split);
-cudaError_t launch_tc_gemm(const CUtensorMap& map, const GemmPlan& p, TcGemmArgs a, cudaStream_t s);
+GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split);
+cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
+                           TcGemmArgs a, cudaStream_t s);
 void launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
                        const float2* cs, bf16* out, cudaStream_t s);
-void launch_reduce_resid(const float* part, int ks, int M, int N, float* h, const float* gate,
-                         float* sumsq, cudaStream_t s);
-void launch_inproj_tc(const float* x, const bf16* w_in, const bf16* b_in, float* h, float* sumsq,
-                      int M, int D, int A, cudaStream_t s);
+void launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
+                       const float* scale, const float* shift, float eps, bf16* y, cudaStream_t s);
+void launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
+                        float* h, const float* scale, const float* shift, float eps, bf16* y,
+                        cudaStream_t s);
+void launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s);
 
 // ---- tensor-core attention (ae_attn_tc.cu)
 struct AttnArgs {
