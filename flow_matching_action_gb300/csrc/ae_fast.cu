@@ -85,9 +85,19 @@ cudaError_t fast_setup(ae_ctx* c) {
   if ((e = make_map(&c->map_o, c->w_o, (long)d.L * d.D, d.qdim(), 128)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D, 128)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_d, c->w_d, (long)d.L * d.D, d.F, 128)) != cudaSuccess) return e;
-  if ((e = make_map(&c->map_y, c->y, maxM, d.D, 16)) != cudaSuccess) return e;
-  if ((e = make_map(&c->map_oact, c->o, maxM, d.qdim(), 16)) != cudaSuccess) return e;
-  if ((e = make_map(&c->map_mact, c->m, maxM, d.F, 16)) != cudaSuccess) return e;
+  (void)maxM;
+  return cudaSuccess;
+}
+
+cudaError_t fast_activation_maps(ae_ctx* c, int box_rows) {
+  if (c->act_box_rows == box_rows) return cudaSuccess;
+  const Dims& d = c->d;
+  const long maxM = (long)c->max_batch * d.H;
+  cudaError_t e;
+  if ((e = make_map(&c->map_y, c->y, maxM, d.D, box_rows)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_oact, c->o, maxM, d.qdim(), box_rows)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_mact, c->m, maxM, d.F, box_rows)) != cudaSuccess) return e;
+  c->act_box_rows = box_rows;
   return cudaSuccess;
 }
 
@@ -102,6 +112,9 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const GemmPlan po = plan_gemm(D, qd, M, sm, 2);
   const GemmPlan pg = plan_gemm(2 * F, D, M, sm, 1);
   const GemmPlan pd = plan_gemm(D, F, M, sm, 2);
+  // the four GEMMs share one token tiling (it depends on M only)
+  *err = fast_activation_maps(c, pq.tok_tile);
+  if (*err != cudaSuccess) return 0;
   float* part0 = c->part;
   float* part1 = c->part + c->part_floats;
   bf16* qkv = (bf16*)c->qkv;
@@ -109,7 +122,6 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   bf16* m = (bf16*)c->m;
   bf16* y = (bf16*)c->y;
   int n = 0;
-  *err = cudaSuccess;
   auto ck = [&](cudaError_t e) {
     if (e != cudaSuccess && *err == cudaSuccess) *err = e;
   };

@@ -27,7 +27,6 @@ using namespace tc;
 
 constexpr int kThreads = 192;           // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kATileBytes = 128 * 128;  // 128 weight rows x 64 bf16
-constexpr int kBBoxRows = 16;           // token rows per activation TMA box
 
 __device__ __forceinline__ float gelu_tanh(float g) {
   return 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
@@ -105,9 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kc = (kb_begin + it) * 64;
         mbar_arrive_expect_tx(&full[s], bytes);
         tma_load_2d(smA + (size_t)s * kATileBytes, &wmap, &full[s], kc, row, pol_w);
-        uint8_t* bs = smB + (size_t)s * btile;
-        for (int r = 0; r < a.tok_tile; r += kBBoxRows)
-          tma_load_2d_nohint(bs + r * 128, &amap, &full[s], kc, t0 + r);
+        tma_load_2d_nohint(smB + (size_t)s * btile, &amap, &full[s], kc, t0);
       }
       // drain: no copy may still be in flight when the CTA exits
       for (int j = it - S > 0 ? it - S : 0; j < it; ++j)
@@ -155,6 +152,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int hb = n / a.dh, p = n - hb * a.dh;
           const int pair = p >> 1, odd = p & 1;
           const bool rot = hb < a.n_rot_heads;
+          float2 csv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = t0 + c0 + j;
+            csv[j] = (rot && t < a.M) ? __ldg(a.rope_cs + (size_t)t * half + pair) : make_float2(1.f, 0.f);
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t < a.M) {
               float outv = v[j];
               if (rot) {
-                const float2 cs = a.rope_cs[(size_t)t * half + pair];
+                const float2 cs = csv[j];
                 const float x1 = odd ? other : v[j], x2 = odd ? v[j] : other;
                 outv = odd ? (x2 * cs.x + x1 * cs.y) : (x1 * cs.x - x2 * cs.y);
               }
@@ -221,41 +224,58 @@ __global__ void k_reduce_qkv(const float* __restrict__ part, int ks_n, int M, in
 }
 
 constexpr int kRowThreads = 256;
+constexpr int kNormThreads = 1024;
 
-__device__ float block_sum_256(float v, float* red) {
+template <int NT>
+__device__ float block_sum(float v, float* red) {
   v = warp_sum(v);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   float t = 0.f;
 #pragma unroll
-  for (int w = 0; w < kRowThreads / 32; ++w) t += red[w];
+  for (int w = 0; w < NT / 32; ++w) t += red[w];
   return t;
+}
+
+// Sum of `ks_n` split-K partials p[j * stride] in split order; the loads are
+// issued eight at a time so a thread keeps eight in flight.
+__device__ __forceinline__ float sum_splits(const float* __restrict__ p, int ks_n, size_t stride) {
+  float s = 0.f;
+  int j = 0;
+  for (; j + 8 <= ks_n; j += 8) {
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __ldcg(p + (size_t)(j + e) * stride);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += v[e];
+  }
+  for (; j < ks_n; ++j) s += __ldcg(p + (size_t)j * stride);
+  return s;
 }
 
 // One token row: h += gate * (sum of the split-K partials, in split order);
 // then, if `scale` is given, y = adaRMS(h) with the next sublayer's
 // (scale, shift) as the bf16 operand of the next GEMM.
-__global__ void __launch_bounds__(kRowThreads) k_resid_norm(const float* __restrict__ part, int ks_n,
-                                                           int M, int D, float* __restrict__ h,
-                                                           const float* __restrict__ gate,
-                                                           const float* __restrict__ scale,
-                                                           const float* __restrict__ shift, float eps,
-                                                           bf16* __restrict__ y) {
-  __shared__ float red[kRowThreads / 32];
+__global__ void __launch_bounds__(kNormThreads) k_resid_norm(const float* __restrict__ part, int ks_n,
+                                                            int M, int D, float* __restrict__ h,
+                                                            const float* __restrict__ gate,
+                                                            const float* __restrict__ scale,
+                                                            const float* __restrict__ shift, float eps,
+                                                            bf16* __restrict__ y) {
+  __shared__ float red[kNormThreads / 32];
   const int t = blockIdx.x;
   float* hr = h + (size_t)t * D;
   float ss = 0.f;
-  for (int n = threadIdx.x; n < D; n += kRowThreads) {
-    float s = 0.f;
-    for (int j = 0; j < ks_n; ++j) s += part[((size_t)j * M + t) * D + n];
+  for (int n = threadIdx.x; n < D; n += kNormThreads) {
+    const float s = sum_splits(part + (size_t)t * D + n, ks_n, (size_t)M * D);
     const float hn = hr[n] + gate[n] * s;
     hr[n] = hn;
     ss += hn * hn;
   }
   if (scale == nullptr) return;
-  ss = block_sum_256(ss, red);
+  ss = block_sum<kNormThreads>(ss, red);
   const float r = 1.0f / sqrtf(ss / (float)D + eps);
-  for (int n = threadIdx.x; n < D; n += kRowThreads)
+  for (int n = threadIdx.x; n < D; n += kNormThreads)
     y[(size_t)t * D + n] = __float2bfloat16_rn(hr[n] * r * (1.f + scale[n]) + shift[n]);
 }
 
@@ -282,7 +302,7 @@ __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __rest
     hr[n] = hn;
     ss += hn * hn;
   }
-  ss = block_sum_256(ss, red);
+  ss = block_sum<kRowThreads>(ss, red);
   const float r = 1.0f / sqrtf(ss / (float)D + eps);
   for (int n = threadIdx.x; n < D; n += kRowThreads)
     y[(size_t)t * D + n] = __float2bfloat16_rn(hr[n] * r * (1.f + scale[n]) + shift[n]);
@@ -372,7 +392,7 @@ void launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_ro
 
 void launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
                        const float* scale, const float* shift, float eps, bf16* y, cudaStream_t s) {
-  k_resid_norm<<<M, kRowThreads, 0, s>>>(part, ks, M, D, h, gate, scale, shift, eps, y);
+  k_resid_norm<<<M, kNormThreads, 0, s>>>(part, ks, M, D, h, gate, scale, shift, eps, y);
 }
 
 void launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,

@@ -104,7 +104,8 @@ struct ae_ctx {
   // (rows of layer l start at l * rows-per-layer) and its extra scratch.
   bool fast = false;
   CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
-  CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes 16 rows x 64
+  CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
+  int act_box_rows = 0;
   float* sumsq = nullptr;    // [D/128][M] adaRMS sum of squares per 128-feature tile
   float* part = nullptr;     // split-K partials
   size_t part_floats = 0;
@@ -195,6 +196,7 @@ cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s);
 // ---- bf16 path driver (ae_fast.cu)
 bool fast_path_supported(const Dims& d, std::string* why);
 cudaError_t fast_setup(ae_ctx* c);  // tensor maps and scratch, after the weights are packed
+cudaError_t fast_activation_maps(ae_ctx* c, int box_rows);  // one box = one token tile
 size_t fast_part_floats(const Dims& d, int max_batch, int sm_count);
 int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
                      cudaError_t* err);
