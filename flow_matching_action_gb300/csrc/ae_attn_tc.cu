@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(bar_s + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
 
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int u = blockIdx.x;
   const int sp = u % a.max_splits;
@@ -298,6 +300,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
 // Merge the chunk ranges of every folded query row in range order; write bf16
 // o[token][head * dh + d].  Block = one (folded row of a group, request), dh threads.
 __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
+  pdl_trigger();
+  pdl_wait();
   const int G = a.Hq / a.Hkv;
   const int g = blockIdx.x / (G * a.H), r = blockIdx.x % (G * a.H), b = blockIdx.y;
   const int qt = r / 128, row = r % 128;
@@ -342,19 +346,17 @@ size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int 
   return (size_t)2 * sm_count + (size_t)max_batch * Hkv * q_tiles;
 }
 
-cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s) {
+cudaError_t attn_kernel_setup() {
+  return cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+}
+
+cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s, bool pdl) {
   attn_plan(a, sm_count);
   const size_t smem = attn_smem_bytes(a.dh);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
   const unsigned grid = (unsigned)(a.batch * a.Hkv * a.q_tiles * a.max_splits);
-  k_attn_tc<<<grid, kAttnThreads, smem, s>>>(a);
-  k_attn_combine<<<dim3(a.Hq * a.H, a.batch), a.dh, 0, s>>>(a, o);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(k_attn_tc, dim3(grid), dim3(kAttnThreads), smem, s, pdl, a);
+  if (e != cudaSuccess) return e;
+  return launch_k(k_attn_combine, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
 }
 
 }  // namespace ae

@@ -103,6 +103,7 @@ cudaError_t fast_activation_maps(ae_ctx* c, int box_rows) {
 
 int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
                      cudaError_t* err) {
+  const bool pdl = c->pdl;
   const Dims& d = c->d;
   const int B = c->bind.batch, M = B * d.H, D = d.D, F = d.F, L = d.L;
   const int nqkv = d.qkvdim(), qd = d.qdim();
@@ -133,19 +134,21 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   auto mod = [&](int l, int j) { return t.mod + (((size_t)step * L + l) * 2 + j) * 3 * D; };
 
   // h = x W_in^T + b_in; y = adaRMS1 of layer 0
-  launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0),
-                     mod(0, 0) + D, eps, y, s);
+  ck(launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0),
+                        mod(0, 0) + D, eps, y, s, pdl));
   ++n;
   for (int l = 0; l < L; ++l) {
     dump(l);
     const float* mod1 = mod(l, 0);
     const float* mod2 = mod(l, 1);
+    const int ln = (l + 1) % L;  // whose weights each GEMM pulls into L2 ahead of use
 
     // merged QKV (+ RoPE)
     TcGemmArgs a = {};
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * nqkv;
+    a.w_next_row0 = ln * nqkv;
     a.rope_cs = c->rope_cs;
     a.dh = d.dh;
     a.n_rot_heads = d.Hq + d.Hkv;
@@ -156,10 +159,10 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       a.e_mode = kEPartial;
       a.part = part0;
     }
-    ck(launch_tc_gemm(c->map_qkv, c->map_y, pq, a, s));
+    ck(launch_tc_gemm(c->map_qkv, c->map_y, pq, a, s, pdl));
     ++n;
     if (pq.ksplit > 1) {
-      launch_reduce_qkv(part0, pq.ksplit, M, nqkv, d.dh, d.Hq + d.Hkv, c->rope_cs, qkv, s);
+      ck(launch_reduce_qkv(part0, pq.ksplit, M, nqkv, d.dh, d.Hq + d.Hkv, c->rope_cs, qkv, s, pdl));
       ++n;
     }
 
@@ -184,7 +187,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.part_o = c->attn_o;
       at.part_ml = c->attn_ml;
       at.status = c->status_dev;
-      ck(launch_attn_tc(at, o, sm, s));
+      ck(launch_attn_tc(at, o, sm, s, pdl));
       n += 2;
     }
 
@@ -193,10 +196,11 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * D;
+    a.w_next_row0 = ln * D;
     a.e_mode = kEPartial;
     a.part = part0;
-    ck(launch_tc_gemm(c->map_o, c->map_oact, po, a, s));
-    launch_resid_norm(part0, po.ksplit, M, D, c->h, mod1 + 2 * D, mod2, mod2 + D, eps, y, s);
+    ck(launch_tc_gemm(c->map_o, c->map_oact, po, a, s, pdl));
+    ck(launch_resid_norm(part0, po.ksplit, M, D, c->h, mod1 + 2 * D, mod2, mod2 + D, eps, y, s, pdl));
     n += 2;
 
     // merged gate/up -> GeGLU
@@ -204,6 +208,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * 2 * F;
+    a.w_next_row0 = ln * 2 * F;
     if (pg.ksplit == 1) {
       a.e_mode = kEGeglu;
       a.out_bf16 = m;
@@ -211,10 +216,10 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       a.e_mode = kEPartial;
       a.part = part0;
     }
-    ck(launch_tc_gemm(c->map_gu, c->map_y, pg, a, s));
+    ck(launch_tc_gemm(c->map_gu, c->map_y, pg, a, s, pdl));
     ++n;
     if (pg.ksplit > 1) {
-      launch_geglu_reduce(part0, pg.ksplit, M, F, m, s);
+      ck(launch_geglu_reduce(part0, pg.ksplit, M, F, m, s, pdl));
       ++n;
     }
 
@@ -223,16 +228,18 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.M = M;
     a.status = c->status_dev;
     a.w_row0 = l * D;
+    a.w_next_row0 = ln * D;
     a.e_mode = kEPartial;
     a.part = part1;
-    ck(launch_tc_gemm(c->map_d, c->map_mact, pd, a, s));
+    ck(launch_tc_gemm(c->map_d, c->map_mact, pd, a, s, pdl));
     const float* nxt = l + 1 < L ? mod(l + 1, 0) : nullptr;
-    launch_resid_norm(part1, pd.ksplit, M, D, c->h, mod2 + 2 * D, nxt, nxt ? nxt + D : nullptr, eps,
-                      y, s);
+    ck(launch_resid_norm(part1, pd.ksplit, M, D, c->h, mod2 + 2 * D, nxt, nxt ? nxt + D : nullptr,
+                         eps, y, s, pdl));
     n += 2;
   }
   dump(L);
-  n += launch_final_bf16(c, t, step, x, s);
+  ck(launch_final_bf16(c, t, step, x, s, pdl));
+  ++n;
   ck(cudaGetLastError());
   return n;
 }

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb_end = (int)((long)(ks + 1) * a.kb_total / a.ksplit);
   const int n_it = kb_end - kb_begin;
   const int t0 = tt * a.tok_tile;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -96,7 +97,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       const int row = a.w_row0 + n_tile * 128;
       const uint32_t bytes = kATileBytes + (uint32_t)btile;
-      int it = 0;
+      // Weights do not depend on the previous kernel: fill the first stages and
+      // start pulling this slab of the next layer into L2 before waiting on it.
+      const int pre = n_it < S ? n_it : S;
+      for (int it = 0; it < pre; ++it) {
+        mbar_arrive_expect_tx(&full[it], bytes);
+        tma_load_2d(smA + (size_t)it * kATileBytes, &wmap, &full[it], (kb_begin + it) * 64, row, pol_w);
+      }
+      if (a.w_next_row0 >= 0)
+        for (int it = 0; it < n_it; ++it)
+          tma_prefetch_l2_2d(&wmap, (kb_begin + it) * 64, a.w_next_row0 + n_tile * 128);
+      pdl_wait();
+      for (int it = 0; it < pre; ++it)
+        tma_load_2d_nohint(smB + (size_t)it * btile, &amap, &full[it], (kb_begin + it) * 64, t0);
+      int it = pre;
       for (; it < n_it; ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
@@ -136,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) votes[q] = (mbar_wait(tmem_full, 0, abort_flag, a.status) && !*abort_flag) ? 1 : 0;
     named_bar(1, 128);
     const bool go = votes[0] && votes[1] && votes[2] && votes[3];
+    pdl_wait();
     if (go) {
       tc_fence_after();
       for (int c0 = 0; c0 < a.tok_tile; c0 += 16) {
@@ -200,6 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // RoPE to q and k, store q|k|v in natural head layout.  One thread per rotation pair.
 __global__ void k_reduce_qkv(const float* __restrict__ part, int ks_n, int M, int N, int dh,
                              int n_rot_heads, const float2* __restrict__ cs, bf16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   const int np = N >> 1;
   if (idx >= (long)M * np) return;
@@ -262,6 +279,8 @@ __global__ void __launch_bounds__(kNormThreads) k_resid_norm(const float* __rest
                                                             const float* __restrict__ scale,
                                                             const float* __restrict__ shift, float eps,
                                                             bf16* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[kNormThreads / 32];
   const int t = blockIdx.x;
   float* hr = h + (size_t)t * D;
@@ -288,6 +307,8 @@ __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __rest
                                                             const float* __restrict__ scale,
                                                             const float* __restrict__ shift, float eps,
                                                             bf16* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[kRowThreads / 32];
   extern __shared__ float xs[];
   const int t = blockIdx.x;
@@ -312,6 +333,8 @@ __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __rest
 // m[t][j] = gelu_tanh(sum g) * (sum u), sums in split order.
 __global__ void k_geglu_reduce(const float* __restrict__ part, int ks_n, int M, int F,
                                bf16* __restrict__ m) {
+  pdl_trigger();
+  pdl_wait();
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long)M * F) return;
   const int t = (int)(idx / F), j = (int)(idx - (long)t * F);
@@ -362,8 +385,12 @@ GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split) {
   return p;
 }
 
+cudaError_t gemm_kernel_setup() {
+  return cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+}
+
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
-                           TcGemmArgs a, cudaStream_t s) {
+                           TcGemmArgs a, cudaStream_t s, bool pdl) {
   a.N = p.N;
   a.K = p.K;
   a.tok_tile = p.tok_tile;
@@ -373,37 +400,35 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
   a.kb_total = p.kb_total;
   a.stages = p.stages;
   a.tmem_cols = p.tmem_cols;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         232448);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  k_tc_gemm<<<p.grid, kThreads, p.smem, s>>>(wmap, amap, a);
-  return cudaGetLastError();
+  return launch_k(k_tc_gemm, dim3(p.grid), dim3(kThreads), p.smem, s, pdl, wmap, amap, a);
 }
 
-void launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
-                       const float2* cs, bf16* out, cudaStream_t s) {
+cudaError_t launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
+                              const float2* cs, bf16* out, cudaStream_t s, bool pdl) {
   const long n = (long)M * (N / 2);
-  k_reduce_qkv<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, ks, M, N, dh, n_rot_heads, cs, out);
+  return launch_k(k_reduce_qkv, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl, part, ks, M,
+                  N, dh, n_rot_heads, cs, out);
 }
 
-void launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
-                       const float* scale, const float* shift, float eps, bf16* y, cudaStream_t s) {
-  k_resid_norm<<<M, kNormThreads, 0, s>>>(part, ks, M, D, h, gate, scale, shift, eps, y);
+cudaError_t launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
+                              const float* scale, const float* shift, float eps, bf16* y,
+                              cudaStream_t s, bool pdl) {
+  return launch_k(k_resid_norm, dim3(M), dim3(kNormThreads), 0, s, pdl, part, ks, M, D, h, gate,
+                  scale, shift, eps, y);
 }
 
-void launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
-                        float* h, const float* scale, const float* shift, float eps, bf16* y,
-                        cudaStream_t s) {
-  k_inproj_norm<<<M, kRowThreads, A * sizeof(float), s>>>(x, w_in, b_in, D, A, h, scale, shift, eps, y);
+cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D,
+                               int A, float* h, const float* scale, const float* shift, float eps,
+                               bf16* y, cudaStream_t s, bool pdl) {
+  return launch_k(k_inproj_norm, dim3(M), dim3(kRowThreads), A * sizeof(float), s, pdl, x, w_in,
+                  b_in, D, A, h, scale, shift, eps, y);
 }
 
-void launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s) {
+cudaError_t launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s,
+                                bool pdl) {
   const long n = (long)M * F;
-  k_geglu_reduce<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, ks, M, F, m);
+  return launch_k(k_geglu_reduce, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl, part, ks,
+                  M, F, m);
 }
 
 }  // namespace ae

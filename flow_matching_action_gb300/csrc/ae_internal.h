@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/ae.h"
@@ -103,6 +104,8 @@ struct ae_ctx {
   // bf16 tensor-core path: TMA descriptors of the stacked per-layer weights
   // (rows of layer l start at l * rows-per-layer) and its extra scratch.
   bool fast = false;
+  bool pdl = false;        // chain kernels by programmatic dependent launch
+  bool use_graph = false;  // capture and replay the launch sequence
   CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
   CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
   int act_box_rows = 0;
@@ -111,6 +114,23 @@ struct ae_ctx {
   size_t part_floats = 0;
   float* attn_o = nullptr;   // attention partials
   float2* attn_ml = nullptr;
+  float* x = nullptr;        // [M, A] flow state while a captured graph runs
+
+  // The whole launch sequence of one ae_sample, captured once per binding and
+  // n_steps and replayed (kernels chained by programmatic dependent launch).
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
+  int64_t graph_launches = 0;
+  struct GraphKey {
+    int batch = -1, n_steps = 0, max_phys_rows = 0;
+    const void *pk = nullptr, *pv = nullptr;
+    int64_t total_rows = 0;
+    const float* dump = nullptr;
+    bool operator==(const GraphKey& o) const {
+      return batch == o.batch && n_steps == o.n_steps && max_phys_rows == o.max_phys_rows &&
+             pk == o.pk && pv == o.pv && total_rows == o.total_rows && dump == o.dump;
+    }
+  } graph_key;
 
   int64_t launches_sample = 0, launches_bind = 0, device_bytes = 0;
   std::vector<void*> allocations;
@@ -118,6 +138,24 @@ struct ae_ctx {
 };
 
 namespace ae {
+
+// Launch a kernel; with pdl, as a programmatic dependent of the previous
+// kernel of the stream (it may start early and waits in griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Parameters of the bind kernel; cu_lens travel by value with the launch.
 struct BindArgs {
@@ -138,7 +176,8 @@ int launch_bind(const BindArgs& a, cudaStream_t s);
 int launch_time_table(const ae_ctx* c, TimeTable& t, cudaStream_t s);
 int launch_step_simt(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s);
 int launch_attn_bf16(ae_ctx* c, int layer, cudaStream_t s);
-int launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s);
+cudaError_t launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
+                              bool pdl);
 
 // ---- tensor-core GEMM (ae_gemm_tc.cu)
 enum EMode : int { kEPartial = 0, kEQkvRope = 1, kEGeglu = 2 };
@@ -146,6 +185,7 @@ enum EMode : int { kEPartial = 0, kEQkvRope = 1, kEGeglu = 2 };
 struct TcGemmArgs {
   int M, N, K;          // tokens, output features, reduction length
   int w_row0;           // first row of this layer's matrix in the stacked weight
+  int w_next_row0;      // first row of the matrix to prefetch into L2 (-1: none)
   int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
   int e_mode;
   float* part;          // kEPartial: [ksplit][M][N]
@@ -162,16 +202,19 @@ struct GemmPlan {
 
 size_t tc_gemm_smem_bytes(int stages, int tok_tile);
 GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split);
+cudaError_t gemm_kernel_setup();
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
-                           TcGemmArgs a, cudaStream_t s);
-void launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
-                       const float2* cs, bf16* out, cudaStream_t s);
-void launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
-                       const float* scale, const float* shift, float eps, bf16* y, cudaStream_t s);
-void launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
-                        float* h, const float* scale, const float* shift, float eps, bf16* y,
-                        cudaStream_t s);
-void launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s);
+                           TcGemmArgs a, cudaStream_t s, bool pdl);
+cudaError_t launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
+                              const float2* cs, bf16* out, cudaStream_t s, bool pdl);
+cudaError_t launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
+                              const float* scale, const float* shift, float eps, bf16* y,
+                              cudaStream_t s, bool pdl);
+cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D,
+                               int A, float* h, const float* scale, const float* shift, float eps,
+                               bf16* y, cudaStream_t s, bool pdl);
+cudaError_t launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s,
+                                bool pdl);
 
 // ---- tensor-core attention (ae_attn_tc.cu)
 struct AttnArgs {
@@ -191,7 +234,8 @@ struct AttnArgs {
   int* status;
 };
 size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int sm_count);
-cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s);
+cudaError_t attn_kernel_setup();
+cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s, bool pdl);
 
 // ---- bf16 path driver (ae_fast.cu)
 bool fast_path_supported(const Dims& d, std::string* why);

@@ -310,6 +310,9 @@ __global__ void k_final(const float* __restrict__ h, int D, float eps, const flo
                         const float* shf, const T* __restrict__ w_out, const T* __restrict__ b_out,
                         int A, float delta, float* __restrict__ x) {
   extern __shared__ float yf[];
+  // programmatic dependent launch (no-ops when launched without the attribute)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int m = blockIdx.x;
   const float* hr = h + (size_t)m * D;
   float ss = 0.f;
@@ -440,15 +443,15 @@ int launch_attn_bf16(ae_ctx* c, int layer, cudaStream_t s) {
   return 1;
 }
 
-int launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s) {
+cudaError_t launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
+                              bool pdl) {
   const Dims& d = c->d;
   const int M = c->bind.batch * d.H;
   const float* fin = t.fin + (size_t)step * 2 * d.D;
   const float delta = (float)(-1.0 / (double)t.n_steps);
-  k_final<bf16><<<M, 256, d.D * sizeof(float), s>>>(c->h, d.D, (float)d.eps, fin, fin + d.D,
-                                                    (const bf16*)c->w_out, (const bf16*)c->b_out,
-                                                    d.A, delta, x);
-  return 1;
+  return launch_k(k_final<bf16>, dim3(M), dim3(256), d.D * sizeof(float), s, pdl, (const float*)c->h,
+                  d.D, (float)d.eps, fin, fin + d.D, (const bf16*)c->w_out, (const bf16*)c->b_out,
+                  d.A, delta, x);
 }
 
 }  // namespace ae
