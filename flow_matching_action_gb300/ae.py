@@ -61,6 +61,7 @@ _SIGNATURES = {
     "ae_bind_prefix": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
     "ae_sample": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
+    "ae_sample_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "ae_set_debug_dump": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
     "ae_synchronize": (ctypes.c_int, [ctypes.c_void_p]),
     "ae_last_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_size_t]),
@@ -159,6 +160,12 @@ def ae_bind_prefix(ctx, batch: int, prefix_k, prefix_v, cu_lens: Sequence[int], 
 
 def ae_sample(ctx, noise, n_steps: int, out_actions) -> None:
     _check(lib().ae_sample(ctx, _ptr(noise), n_steps, _ptr(out_actions)), ctx)
+
+
+def ae_sample_noalloc(ctx, noise, n_steps: int, out_actions) -> None:
+    """ae_sample without device-memory allocation (see include/ae.h): for callers
+    that sample inside a stream capture or under a fixed HBM budget."""
+    _check(lib().ae_sample_noalloc(ctx, _ptr(noise), n_steps, _ptr(out_actions)), ctx)
 
 
 def ae_set_debug_dump(ctx, hidden, capacity: int) -> None:

@@ -283,6 +283,14 @@ ae_status sticky(const ae_ctx* c) {
 
 }  // namespace
 
+namespace ae {
+const TimeTable* find_time_table(const ae_ctx* c, int n_steps) {
+  for (const TimeTable& t : c->tables)
+    if (t.n_steps == n_steps) return &t;
+  return nullptr;
+}
+}  // namespace ae
+
 extern "C" {
 
 const char* ae_status_string(ae_status s) {

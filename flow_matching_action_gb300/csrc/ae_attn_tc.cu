@@ -335,6 +335,17 @@ void attn_plan(AttnArgs& a, int sm_count) {
   if (cpc < 1) cpc = 1;
   a.chunks_per_cta = cpc;
   a.max_splits = (max_chunks + cpc - 1) / cpc;
+  // a fixed-size scratch: fewer, longer chunk ranges until the units fit
+  while (a.max_units > 0 && (long)a.batch * a.Hkv * a.q_tiles * a.max_splits > a.max_units &&
+         a.chunks_per_cta < max_chunks) {
+    ++a.chunks_per_cta;
+    a.max_splits = (max_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
+  }
+}
+
+size_t attn_plan_units(AttnArgs a, int sm_count) {
+  attn_plan(a, sm_count);
+  return (size_t)a.batch * a.Hkv * a.q_tiles * a.max_splits;
 }
 
 // Work units never exceed 2 * sm_count + batch * Hkv * q_tiles: a plan with one

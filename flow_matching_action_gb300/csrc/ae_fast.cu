@@ -102,7 +102,7 @@ cudaError_t fast_activation_maps(ae_ctx* c, int box_rows) {
 }
 
 int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
-                     cudaError_t* err) {
+                     cudaError_t* err, const AttnScratch* attn_scratch) {
   const bool pdl = c->pdl;
   const Dims& d = c->d;
   const int B = c->bind.batch, M = B * d.H, D = d.D, F = d.F, L = d.L;
@@ -184,8 +184,9 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.Hkv = d.Hkv;
       at.dh = d.dh;
       at.scale = (float)(1.0 / sqrt((double)d.dh));
-      at.part_o = c->attn_o;
-      at.part_ml = c->attn_ml;
+      at.part_o = attn_scratch ? attn_scratch->part_o : c->attn_o;
+      at.part_ml = attn_scratch ? attn_scratch->part_ml : c->attn_ml;
+      at.max_units = attn_scratch ? attn_scratch->max_units : 0;
       at.status = c->status_dev;
       ck(launch_attn_tc(at, o, sm, s, pdl));
       n += 2;

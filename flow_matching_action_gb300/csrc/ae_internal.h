@@ -229,11 +229,15 @@ struct AttnArgs {
   int batch, H, Hq, Hkv, dh;
   float scale;
   int q_tiles, chunks_per_cta, max_splits;  // set by the planner
+  int max_units;          // cap on work units (0: none), for fixed-size scratch
   float* part_o;          // [units][128][dh]
   float2* part_ml;        // [units][128]
   int* status;
 };
 size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int sm_count);
+// Work units the planner would use (within a.max_units when it is set; a
+// result above a.max_units means the cap cannot be met).
+size_t attn_plan_units(AttnArgs a, int sm_count);
 cudaError_t attn_kernel_setup();
 cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s, bool pdl);
 
@@ -242,7 +246,15 @@ bool fast_path_supported(const Dims& d, std::string* why);
 cudaError_t fast_setup(ae_ctx* c);  // tensor maps and scratch, after the weights are packed
 cudaError_t fast_activation_maps(ae_ctx* c, int box_rows);  // one box = one token tile
 size_t fast_part_floats(const Dims& d, int max_batch, int sm_count);
+// Attention split-KV partials supplied by the caller instead of the context's.
+struct AttnScratch {
+  float* part_o;
+  float2* part_ml;
+  int max_units;
+};
 int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
-                     cudaError_t* err);
+                     cudaError_t* err, const AttnScratch* attn_scratch = nullptr);
+// The cached time table of n_steps, or nullptr (never allocates).
+const TimeTable* find_time_table(const ae_ctx* c, int n_steps);
 
 }  // namespace ae

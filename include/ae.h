@@ -179,6 +179,35 @@ AE_API ae_status ae_bind_prefix(ae_ctx* ctx, int batch, const void* prefix_k,
 AE_API ae_status ae_sample(ae_ctx* ctx, const float* noise, int n_steps, float* out_actions);
 
 /*
+ * ae_sample for callers that cannot allocate device memory while sampling.
+ * The pages have no counterpart to this call; it exists for callers such as
+ * code that samples while a CUDA stream capture is open (an allocation there
+ * breaks the capture), a serving process whose HBM is pre-reserved for its own
+ * caches, or a real-time control loop that forbids allocator calls after
+ * start-up.  ae_sample may allocate on its first call with a new n_steps (the
+ * time-conditioning table) and when it records its CUDA graph; this call runs
+ * the same kernels, launched one by one on the context's stream, and calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *   - The attention kernel's split-KV partial results live in one static
+ *     16 MiB __device__ array of the library (held by every GPU that loads
+ *     the library until the process exits) instead of context memory.  A
+ *     batch whose partials do not fit (about 30 requests at head_dim 256)
+ *     returns AE_ERR_SHAPE.
+ *   - The time-conditioning table of n_steps must already exist: call
+ *     ae_sample once with the same n_steps first, else AE_ERR_NOT_BOUND.
+ *   - The first call on a device looks up the array's device address (a
+ *     module load, not an allocation by this library); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the array and leaves its contents behind;
+ *     calls that overlap on the GPU (different streams or contexts of one
+ *     device) race on it.
+ * bf16 contexts only (AE_ERR_UNSUPPORTED otherwise).  Arguments and other
+ * errors as for ae_sample.
+ */
+AE_API ae_status ae_sample_noalloc(ae_ctx* ctx, const float* noise, int n_steps,
+                                   float* out_actions);
+
+/*
  * Optional per-layer hidden-state dump for parity checks.  When set, every
  * ae_sample writes the fp32 residual stream entering layer l (l = 0..L-1) and
  * leaving the last layer (l = L) of every step s to
