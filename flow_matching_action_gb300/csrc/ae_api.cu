@@ -424,6 +424,16 @@ ae_status ae_bind_prefix(ae_ctx* c, int batch, const void* prefix_k, const void*
   a.half_dh = c->d.dh / 2;
   a.theta = c->d.theta;
   a.status = c->status_dev;
+  if (c->fast && total >= 64) {
+    // TMA views of the borrowed prefix K / V (host-side descriptors, no copy);
+    // only chunks of 64 contiguous valid rows use them
+    const long rows = (long)c->d.L * total;
+    cudaError_t e = ae::make_bf16_map(&c->bind.map_pk, prefix_k, rows, c->d.kvdim(), 64);
+    if (e == cudaSuccess) e = ae::make_bf16_map(&c->bind.map_pv, prefix_v, rows, c->d.kvdim(), 64);
+    if (e != cudaSuccess)
+      return set_msg(c, AE_ERR_INVALID_ARG,
+                     "prefix_k / prefix_v cannot be described for TMA (16-byte alignment needed)");
+  }
   c->launches_bind = ae::launch_bind(a, c->stream);
   AE_CK(c, cudaGetLastError());
   c->bind.batch = batch;

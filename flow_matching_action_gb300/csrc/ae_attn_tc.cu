@@ -2,21 +2,28 @@
 //
 // The query heads of a KV group share one KV head (MQA/GQA, LoongForge Pi0.5
 // blog section 3), so the (Hq / Hkv) x H action queries of a request's group
-// are folded into one tall matrix, row r = head-in-group * H + token, and every
-// K/V block is loaded once for all of them.
-// The key set of request b is its VALID prefix rows (gathered through the bind
-// table: masked and padded rows are never read) followed by its H action rows
-// (actions see every valid prefix token and each other).
+// are folded into one tall matrix and every K/V block is loaded once for all
+// of them.  Each head's H rows are padded to a multiple of 16 in the fold
+// (row r = head-in-group * Hp + token, Hp = H rounded up to 16) so the query
+// tile arrives as 16-row TMA boxes.
+// The key set of request b is its VALID prefix rows (through the bind table:
+// masked and padded rows are never read) followed by its H action rows
+// (actions see every valid prefix token and each other).  A 64-key chunk whose
+// rows form one contiguous run of valid prefix rows (the common case) arrives
+// as TMA boxes; any other chunk is gathered row by row with cp.async.  V is
+// stored exactly like K (rows of 64-dim, 128-byte-swizzled blocks) and read as
+// the MN-major operand of P V.
 //
-// A CTA owns (request, 128-row query tile, range of 64-key chunks) and walks
-// its chunks with an online softmax:
+// A CTA owns (request, KV head, 128-row query tile, range of chunks) and walks
+// its chunks with an online softmax, the next chunk's K/V loading while the
+// current one computes:
 //   S = Q K^T      tcgen05, M = 128 query rows, N = 64 keys, K = dh; S in TMEM
 //   P = exp(S - m) fp32 per query row (one thread per row), bf16 into smem
 //   O += P V       tcgen05, M = 128, N = dh, K = 64 keys; O stays in TMEM
 // The exponent reference m is raised (and O, l rescaled in place) only when a
 // chunk's maximum exceeds it by more than 8, so P <= e^8 and most chunks skip
-// the rescale.  Each CTA writes its unnormalized O with (m, l); a combine
-// kernel merges the ranges of a row in range order (deterministic) and
+// the rescale.  Each CTA stores its unnormalized O (TMA store) with (m, l); a
+// combine kernel merges the ranges of a row in range order (deterministic) and
 // writes the bf16 attention output o[token][head * dh + d].
 #include <math.h>
 
@@ -29,18 +36,18 @@ namespace {
 using namespace tc;
 
 constexpr int kAttnThreads = 128;
-constexpr int kChunk = 64;            // keys per chunk
-constexpr float kRescaleMargin = 8.f; // raise the exponent reference only past this
+constexpr int kChunk = 64;             // keys per chunk
+constexpr float kRescaleMargin = 8.f;  // raise the exponent reference only past this
+constexpr int kSkip = -0x40000000;     // gather code: zero-fill
+
+__host__ __device__ inline int fold_rows_per_head(int H) { return (H + 15) & ~15; }
 
 struct AttnSmem {
-  uint32_t q, k[2], v[2], p, bars, total;  // byte offsets from the 1024-aligned base
+  uint32_t q, k[2], v[2], p, bars, idx, total;  // byte offsets from the 1024-aligned base
 };
 
-// Q: [dh/64][128 rows][128 B] K-major.  K: [dh/64][64 keys][128 B] K-major.
-// V: row-major rows of the chunk as an MN-major operand (MN = dh, K = keys):
-// 1024-byte atoms of 8 keys x 64 dims, dims-atoms 1024 B apart, key-atoms
-// dh/64 * 1024 B apart.  P: [128 rows][128 B] K-major.  K and V are double
-// buffered so the next chunk's gathers overlap this chunk's MMAs.
+// Q: [dh/64][128 rows][128 B].  K and V: [dh/64][64 keys][128 B] (8 KB blocks),
+// double buffered.  P: [128 rows][128 B].  All 128-byte swizzled.
 __host__ __device__ inline AttnSmem attn_smem_layout(int dh) {
   AttnSmem L;
   const uint32_t kv = (uint32_t)dh * kChunk * 2;
@@ -50,8 +57,9 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int dh) {
   L.v[0] = L.k[1] + kv;
   L.v[1] = L.v[0] + kv;
   L.p = L.v[1] + kv;
-  L.bars = L.p + 128 * kChunk * 2;
-  L.total = L.bars + 64;
+  L.bars = L.p + 128 * kChunk * 2;  // bar_s, bar_o, bar_q, bar_kv[2], TMEM base, abort flag
+  L.idx = L.bars + 64;              // [2][kChunk] gather codes of the two K/V buffers
+  L.total = L.idx + 2 * kChunk * 4;
   return L;
 }
 
@@ -61,14 +69,100 @@ __host__ __device__ inline uint32_t attn_tmem_cols(int dh) {
   return c;
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
+// Start loading chunk c of KV head g into buffer `buf`.  Returns true when it
+// travels by TMA (completion on bar_kv), false when by cp.async (one commit
+// group).  Uniform for the CTA.  Gather code of a key: >= 0 physical prefix
+// row, -1 - i action row i, kSkip zero-fill.
+template <int DH>
+__device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorMap* kmap,
+                                              const CUtensorMap* vmap, uint8_t* smem,
+                                              const AttnSmem& L, uint64_t* bar_kv, int b, int g,
+                                              int n_pre, int n_keys, int c, int buf) {
+  constexpr int CPR = DH / 8;                    // 16-byte pieces per row
+  constexpr int RPW = CPR >= 32 ? 1 : 32 / CPR;  // rows per warp instruction
+  constexpr int PPL = CPR >= 32 ? CPR / 32 : 1;  // pieces per lane per row
+  constexpr int kdb = DH / 64;
+  const int key0 = c * kChunk;
+  const int nk = min(kChunk, n_keys - key0);
+  int* ix = reinterpret_cast<int*>(smem + L.idx) + buf * kChunk;
+  if (threadIdx.x < kChunk) {
+    const int j = threadIdx.x, key = key0 + j;
+    int code = kSkip;
+    if (j < nk) {
+      if (key < n_pre) {
+        const int prow = a.valid_idx[(size_t)b * a.max_rows + key];
+        if (prow >= 0 && prow < a.total_rows) code = prow;
+        else report(a.status, kDevBounds);
+      } else {
+        code = -1 - (key - n_pre);
+      }
+    }
+    ix[j] = code;
+  }
+  __syncthreads();
+  uint8_t* ks = smem + L.k[buf];
+  uint8_t* vs = smem + L.v[buf];
+  // codes increase strictly over a chunk's prefix keys: first and last decide
+  const bool contiguous = nk == kChunk && ix[0] >= 0 && ix[kChunk - 1] - ix[0] == kChunk - 1;
+  if (contiguous) {
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(&bar_kv[buf], 2u * kdb * kChunk * 128);
+      const int row = a.layer_row0 + ix[0];
+#pragma unroll
+      for (int kb = 0; kb < kdb; ++kb) {
+        tma_load_2d_nohint(ks + kb * kChunk * 128, kmap, &bar_kv[buf], g * DH + kb * 64, row);
+        tma_load_2d_nohint(vs + kb * kChunk * 128, vmap, &bar_kv[buf], g * DH + kb * 64, row);
+      }
+    }
+    return true;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / (32 / RPW);  // row within this warp instruction
+  const int pl = lane % (32 / RPW);   // piece index of the lane
+  const int kvdim = a.Hkv * DH, qkvdim = (a.Hq + 2 * a.Hkv) * DH;
+  for (int j0 = warp * RPW; j0 < kChunk; j0 += (kAttnThreads / 32) * RPW) {
+    const int j = j0 + sub;
+    const int code = ix[j];
+    const bf16* kr = a.qkv;  // any valid address when zero-filling
+    const bf16* vr = a.qkv;
+    uint32_t bytes = 0;
+    if (code >= 0) {
+      kr = a.pk + (size_t)code * kvdim + g * DH;
+      vr = a.pv + (size_t)code * kvdim + g * DH;
+      bytes = 16;
+    } else if (code != kSkip) {
+      const bf16* base = a.qkv + (size_t)(b * a.H + (-1 - code)) * qkvdim;
+      kr = base + (a.Hq + g) * DH;
+      vr = base + (a.Hq + a.Hkv + g) * DH;
+      bytes = 16;
+    }
+#pragma unroll
+    for (int e = 0; e < PPL; ++e) {
+      const int ch = pl + e * 32;
+      const uint32_t off = (ch >> 3) * kChunk * 128 + sw128_offset(j, ch & 7);
+      cp_async16(ks + off, bytes ? kr + ch * 8 : kr, bytes);
+      cp_async16(vs + off, bytes ? vr + ch * 8 : vr, bytes);
+    }
+  }
+  cp_async_commit();
+  return false;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+              const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+              const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const int dh = a.dh;
+  constexpr int dh = DH;
+  constexpr int kdb = dh / 64;
   const AttnSmem L = attn_smem_layout(dh);
   uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* bar_o = bar_s + 1;
-  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(bar_s + 2);
+  uint64_t* bar_q = bar_s + 2;
+  uint64_t* bar_kv = bar_s + 3;  // [2]
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(bar_s + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
 
   pdl_trigger();
@@ -82,6 +176,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
   const int g = u % a.Hkv;
   const int b = u / a.Hkv;
   const int G = a.Hq / a.Hkv;  // query heads per KV head
+  const int Hp = fold_rows_per_head(a.H);
   const int n_pre = a.n_valid[b];
   const int n_keys = n_pre + a.H;
   const int n_chunks = (n_keys + kChunk - 1) / kChunk;
@@ -89,75 +184,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
   const int c_end = min(c_begin + a.chunks_per_cta, n_chunks);
   if (c_begin >= c_end) return;  // uniform for the CTA
   const int n_my = c_end - c_begin;
-  const int rows = G * a.H;
-  const int qkvdim = (a.Hq + 2 * a.Hkv) * dh;
-  const int kvdim = a.Hkv * dh;
-  const int kdb = dh / 64;
-  const int cpr = dh / 8;  // 16-byte chunks per head row
   const uint32_t tcols = attn_tmem_cols(dh);
-  const uint32_t v_sbo = (uint32_t)kdb * 1024;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&bar_s[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
   }
   if (warp == 0) {
     tmem_alloc(tmem_base_p, tcols);
     tmem_relinquish();
   }
-
-  // gathers of one chunk's K and V rows of KV head g into buffer `buf`
-  auto load_chunk = [&](int c, int buf) {
-    const int key0 = c * kChunk;
-    const int nk = min(kChunk, n_keys - key0);
-    uint8_t* ks = smem + L.k[buf];
-    uint8_t* vs = smem + L.v[buf];
-    for (int i = threadIdx.x; i < kChunk * cpr; i += kAttnThreads) {
-      const int j = i / cpr, ch = i % cpr;
-      const bf16* ksrc = a.qkv;  // any valid address when zero-filling
-      const bf16* vsrc = a.qkv;
-      uint32_t bytes = 0;
-      if (j < nk) {
-        const int key = key0 + j;
-        if (key < n_pre) {
-          const int prow = a.valid_idx[(size_t)b * a.max_rows + key];
-          if (prow >= 0 && prow < a.total_rows) {
-            ksrc = a.pk + (size_t)prow * kvdim + g * dh + ch * 8;
-            vsrc = a.pv + (size_t)prow * kvdim + g * dh + ch * 8;
-            bytes = 16;
-          } else {
-            report(a.status, kDevBounds);
-          }
-        } else {
-          const bf16* base = a.qkv + (size_t)(b * a.H + (key - n_pre)) * qkvdim;
-          ksrc = base + (a.Hq + g) * dh + ch * 8;
-          vsrc = base + (a.Hq + a.Hkv + g) * dh + ch * 8;
-          bytes = 16;
-        }
-      }
-      const int grp = ch >> 3, cc = ch & 7;
-      cp_async16(ks + grp * kChunk * 128 + sw128_offset(j, cc), ksrc, bytes);
-      cp_async16(vs + (j >> 3) * v_sbo + grp * 1024 + sw128_offset(j & 7, cc), vsrc, bytes);
+  __syncthreads();
+  // ---- Q tile by TMA: 16-row groups of the fold (a group never straddles heads)
+  if (threadIdx.x == 0) {
+    int nbox = 0;
+    for (int rg = 0; rg < 8; ++rg)
+      if ((qt * 128 + rg * 16) / Hp < G) ++nbox;
+    mbar_arrive_expect_tx(bar_q, (uint32_t)nbox * kdb * 16 * 128);
+    for (int rg = 0; rg < 8; ++rg) {
+      const int r0 = qt * 128 + rg * 16;
+      const int hh = r0 / Hp;
+      if (hh >= G) continue;
+      const int tok0 = r0 - hh * Hp;
+      const int col = (g * G + hh) * dh;
+#pragma unroll
+      for (int kb = 0; kb < kdb; ++kb)
+        tma_load_2d_nohint(smem + L.q + kb * 128 * 128 + rg * 16 * 128, &qmap, bar_q, col + kb * 64,
+                           b * a.H + tok0);
     }
-  };
-
-  // ---- Q tile (once): folded row r = 128 qt + row  ->  (head, token); then chunk 0
-  for (int i = threadIdx.x; i < 128 * cpr; i += kAttnThreads) {
-    const int row = i / cpr, ch = i % cpr;
-    const int r = qt * 128 + row;
-    const bf16* src = a.qkv;
-    uint32_t bytes = 0;
-    if (r < rows) {
-      const int h = g * G + r / a.H, tok = r % a.H;
-      src = a.qkv + (size_t)(b * a.H + tok) * qkvdim + h * dh + ch * 8;
-      bytes = 16;
-    }
-    cp_async16(smem + L.q + (ch >> 3) * 128 * 128 + sw128_offset(row, ch & 7), src, bytes);
   }
-  load_chunk(c_begin, 0);
-  cp_async_commit();
+  bool tma_cur = load_kv_chunk<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c_begin, 0);
 
   tc_fence_before();
   __syncthreads();
@@ -168,27 +228,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
   const int row = threadIdx.x;
   float m_ref = -INFINITY, l = 0.f;
   bool failed = false;
+  uint32_t kv_phase[2] = {0u, 0u};  // used by thread 0 only
 
   for (int ci = 0; ci < n_my; ++ci) {
     const int c = c_begin + ci;
     const int buf = ci & 1;
     const int nk = min(kChunk, n_keys - c * kChunk);
-    // prefetch the next chunk into the other buffer (its last reader, the
+    // start the next chunk into the other buffer (its last reader, the
     // previous chunk's P V, completed before this iteration began)
-    if (ci + 1 < n_my) {
-      load_chunk(c + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    bool tma_next = false;
+    const bool has_next = ci + 1 < n_my;
+    if (has_next)
+      tma_next = load_kv_chunk<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c + 1, buf ^ 1);
+    int ok = 1;
+    if (!tma_cur) {
+      if (has_next && !tma_next) cp_async_wait<1>();
+      else cp_async_wait<0>();
+      fence_proxy_async_smem();
+    } else if (threadIdx.x == 0) {
+      ok = mbar_wait(&bar_kv[buf], kv_phase[buf], abort_flag, a.status) ? 1 : 0;
+      kv_phase[buf] ^= 1u;
     }
-    fence_proxy_async_smem();
+    if (ci == 0 && threadIdx.x == 0 && ok) ok = mbar_wait(bar_q, 0, abort_flag, a.status) ? 1 : 0;
     tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
     tc_fence_after();
     // ---- S = Q K^T
     if (threadIdx.x == 0) {
-      const uint32_t idesc = idesc_bf16(128, kChunk);
+      constexpr uint32_t idesc = idesc_bf16(128, kChunk);
+#pragma unroll
       for (int kb = 0; kb < kdb; ++kb) {
         const uint64_t ad = sdesc_sw128(smem_u32(smem + L.q + kb * 128 * 128));
         const uint64_t bd = sdesc_sw128(smem_u32(smem + L.k[buf] + kb * kChunk * 128));
@@ -198,7 +269,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
       }
       mma_commit(bar_s);
     }
-    int ok = 1;
+    ok = 1;
     if (lane == 0) ok = mbar_wait(bar_s, (uint32_t)ci & 1u, abort_flag, a.status) ? 1 : 0;
     if (__syncthreads_or(!ok)) {
       failed = true;
@@ -227,6 +298,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
     }
     if (__any_sync(0xffffffffu, factor != 1.f)) {
       l *= factor;
+#pragma unroll 1
       for (int c0 = 0; c0 < dh; c0 += 16) {
         float v[16];
         tmem_ld16(tm_o + lane_off + (uint32_t)c0, v);
@@ -254,13 +326,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // ---- O += P V   (V as the MN-major operand: 16 keys = two 8-key atoms per step)
+    // ---- O += P V: V rows are the MN-major operand (dims along MN in 64-dim
+    //      blocks 8 KB apart, keys along K in 8-key atoms 1 KB apart)
     if (threadIdx.x == 0) {
-      const uint32_t idesc = idesc_bf16(128, dh, true);
+      constexpr uint32_t idesc = idesc_bf16(128, dh, true);
       const uint64_t ad = sdesc_sw128(smem_u32(smem + L.p));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint64_t bd = sdesc_sw128_mn(smem_u32(smem + L.v[buf] + k * 2 * v_sbo), 1024, v_sbo);
+        const uint64_t bd = sdesc_sw128_mn(smem_u32(smem + L.v[buf] + k * 2048), kChunk * 128, 1024);
         mma_bf16(tm_o, ad + 2 * k, bd, idesc, (ci > 0 || k > 0) ? 1u : 0u);
       }
       mma_commit(bar_o);
@@ -272,22 +345,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
       break;
     }
     tc_fence_after();
+    tma_cur = tma_next;
   }
   cp_async_wait<0>();
+  if (failed && threadIdx.x == 0) {
+    // no TMA copy may still be writing shared memory when the CTA exits
+    mbar_wait(bar_q, 0, abort_flag, a.status);
+    mbar_wait(&bar_kv[0], kv_phase[0], abort_flag, a.status);
+    mbar_wait(&bar_kv[1], kv_phase[1], abort_flag, a.status);
+  }
+  __syncthreads();  // every chunk buffer is free: reuse K/V space to stage O
   if (!failed) {
+    // O rows -> 128-byte-swizzled staging boxes of 32 fp32 columns x 128 rows
+    // (the K/V buffers hold exactly 128 x dh floats), then TMA stores
     const int r = qt * 128 + row;
+    const bool valid_row = r / Hp < G && r % Hp < a.H;
     const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;
-    float* po = a.part_o + (unit * 128 + row) * dh;
+    uint8_t* stg = smem + L.k[0];
+#pragma unroll 1
     for (int c0 = 0; c0 < dh; c0 += 16) {
       float v[16];
       tmem_ld16(tm_o + lane_off + (uint32_t)c0, v);
-      if (r < rows) {
+      uint8_t* box = stg + (c0 >> 5) * (128 * 128);
+      const int cc0 = (c0 & 31) >> 2;
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<float4*>(po + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      }
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float4*>(box + sw128_offset(row, cc0 + j)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
-    if (r < rows) a.part_ml[unit * 128 + row] = make_float2(m_ref, l);
+    if (valid_row) a.part_ml[unit * 128 + row] = make_float2(m_ref, l);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int bx = 0; bx < dh / 32; ++bx)
+        tma_store_2d(&omap, stg + bx * (128 * 128), bx * 32, (int)(unit * 128));
+      bulk_commit();
+      bulk_wait_read_all();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -297,13 +391,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tc(const AttnArgs a) {
   }
 }
 
-// Merge the chunk ranges of every folded query row in range order; write bf16
-// o[token][head * dh + d].  Block = one (folded row of a group, request), dh threads.
+// Merge the chunk ranges of every query row in range order; write bf16
+// o[token][head * dh + d].  Block = one (head, token) of a request, dh threads.
 __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
   pdl_trigger();
   pdl_wait();
   const int G = a.Hq / a.Hkv;
-  const int g = blockIdx.x / (G * a.H), r = blockIdx.x % (G * a.H), b = blockIdx.y;
+  const int Hp = fold_rows_per_head(a.H);
+  const int g = blockIdx.x / (G * a.H), hr = blockIdx.x % (G * a.H), b = blockIdx.y;
+  const int hh = hr / a.H, tok = hr % a.H;
+  const int r = hh * Hp + tok;  // folded row
   const int qt = r / 128, row = r % 128;
   const int n_chunks = (a.n_valid[b] + a.H + kChunk - 1) / kChunk;
   const int n_splits = (n_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
@@ -318,7 +415,7 @@ __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
     l += ml.y * w;
     acc += a.part_o[((unit0 + sp) * 128 + row) * a.dh + d] * w;
   }
-  const int h = g * G + r / a.H, tok = r % a.H;
+  const int h = g * G + hh;
   o[(size_t)(b * a.H + tok) * (a.Hq * a.dh) + h * a.dh + d] = __float2bfloat16_rn(acc / l);
 }
 
@@ -328,7 +425,7 @@ size_t attn_smem_bytes(int dh) { return 1024 + attn_smem_layout(dh).total; }
 
 // Work split: aim for about two CTAs per SM over the (upper-bound) chunk count.
 void attn_plan(AttnArgs& a, int sm_count) {
-  a.q_tiles = ((a.Hq / a.Hkv) * a.H + 127) / 128;
+  a.q_tiles = ((a.Hq / a.Hkv) * fold_rows_per_head(a.H) + 127) / 128;
   const int max_chunks = (a.plan_rows + a.H + kChunk - 1) / kChunk;
   const long est = (long)a.batch * a.Hkv * a.q_tiles * max_chunks;
   int cpc = (int)((est + 2L * sm_count - 1) / (2L * sm_count));
@@ -353,19 +450,41 @@ size_t attn_plan_units(AttnArgs a, int sm_count) {
 // up adds at most one unit per (request, KV head, query tile).
 size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int sm_count) {
   (void)max_rows;
-  const int q_tiles = ((Hq / Hkv) * H + 127) / 128;
+  const int q_tiles = ((Hq / Hkv) * fold_rows_per_head(H) + 127) / 128;
   return (size_t)2 * sm_count + (size_t)max_batch * Hkv * q_tiles;
 }
 
-cudaError_t attn_kernel_setup() {
-  return cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+template <int DH>
+cudaError_t attn_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_attn_tc<DH>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
-cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s, bool pdl) {
+cudaError_t attn_kernel_setup() {
+  cudaError_t e = attn_attrs<64>();
+  if (e == cudaSuccess) e = attn_attrs<128>();
+  if (e == cudaSuccess) e = attn_attrs<256>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_attn_combine, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const CUtensorMap& omap, AttnArgs a, bf16* o, int sm_count,
+                           cudaStream_t s, bool pdl) {
   attn_plan(a, sm_count);
   const size_t smem = attn_smem_bytes(a.dh);
   const unsigned grid = (unsigned)(a.batch * a.Hkv * a.q_tiles * a.max_splits);
-  cudaError_t e = launch_k(k_attn_tc, dim3(grid), dim3(kAttnThreads), smem, s, pdl, a);
+  cudaError_t e;
+  switch (a.dh) {
+    case 64: e = launch_k(k_attn_tc<64>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
+    case 128: e = launch_k(k_attn_tc<128>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
+    default: e = launch_k(k_attn_tc<256>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
+  }
   if (e != cudaSuccess) return e;
   return launch_k(k_attn_combine, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
 }

@@ -63,7 +63,7 @@ bool fast_path_supported(const Dims& d, std::string* why) {
   if (d.F % 64) return no("bf16 path needs mlp % 64 == 0");
   if (d.qkvdim() % 128) return no("bf16 path needs (n_q_heads + 2 n_kv_heads) * head_dim % 128 == 0");
   if (d.qdim() % 64) return no("bf16 path needs n_q_heads * head_dim % 64 == 0");
-  if (d.dh % 64) return no("bf16 path needs head_dim % 64 == 0");
+  if (d.dh != 64 && d.dh != 128 && d.dh != 256) return no("bf16 path needs head_dim 64, 128 or 256");
   return true;
 }
 
@@ -85,8 +85,26 @@ cudaError_t fast_setup(ae_ctx* c) {
   if ((e = make_map(&c->map_o, c->w_o, (long)d.L * d.D, d.qdim(), 128)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D, 128)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_d, c->w_d, (long)d.L * d.D, d.F, 128)) != cudaSuccess) return e;
-  (void)maxM;
-  return cudaSuccess;
+  if ((e = make_map(&c->map_qkv_act, c->qkv, maxM, d.qkvdim(), 16)) != cudaSuccess) return e;
+  const size_t units = attn_part_units(c->max_batch, d.H, d.Hq, d.Hkv, c->max_rows, c->sm_count);
+  return make_attn_o_map(&c->map_attn_o, c->attn_o, units, d.dh);
+}
+
+cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows) {
+  return make_map(map, ptr, rows, cols, box_rows);
+}
+
+cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int dh) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)dh, (cuuint64_t)(units * 128)};
+  cuuint64_t strides[1] = {(cuuint64_t)dh * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t fast_activation_maps(ae_ctx* c, int box_rows) {
@@ -173,6 +191,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.qkv = qkv;
       at.pk = (const bf16*)c->bind.pk + lay;
       at.pv = (const bf16*)c->bind.pv + lay;
+      at.layer_row0 = (int)(l * c->bind.total_rows);
       at.total_rows = c->bind.total_rows;
       at.valid_idx = c->valid_idx;
       at.n_valid = c->n_valid;
@@ -188,7 +207,8 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.part_ml = attn_scratch ? attn_scratch->part_ml : c->attn_ml;
       at.max_units = attn_scratch ? attn_scratch->max_units : 0;
       at.status = c->status_dev;
-      ck(launch_attn_tc(at, o, sm, s, pdl));
+      ck(launch_attn_tc(c->map_qkv_act, c->bind.map_pk, c->bind.map_pv,
+                        attn_scratch ? attn_scratch->omap : c->map_attn_o, at, o, sm, s, pdl));
       n += 2;
     }
 

@@ -385,8 +385,22 @@ GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split) {
   return p;
 }
 
+// Every kernel of the bf16 path asks for the same (maximum) shared-memory
+// carve-out, so consecutive kernels never make an SM re-partition L1/shared.
+template <typename K>
+cudaError_t max_carveout(K kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t gemm_kernel_setup() {
-  return cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  cudaError_t e = cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  if (e == cudaSuccess) e = max_carveout(k_tc_gemm);
+  if (e == cudaSuccess) e = max_carveout(k_reduce_qkv);
+  if (e == cudaSuccess) e = max_carveout(k_resid_norm);
+  if (e == cudaSuccess) e = max_carveout(k_inproj_norm);
+  if (e == cudaSuccess) e = max_carveout(k_geglu_reduce);
+  return e;
 }
 
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,

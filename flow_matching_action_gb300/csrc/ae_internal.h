@@ -48,6 +48,7 @@ struct BindState {
   const void* pv = nullptr;             // borrowed prefix V
   int64_t total_rows = 0;               // rows per layer of pk / pv
   int max_phys_rows = 0;                // longest request of the binding
+  CUtensorMap map_pk, map_pv;           // bf16 path: TMA views of pk / pv, boxes 64 rows x 64
   std::vector<int> cu;                  // host copy of cu_lens
 };
 
@@ -108,6 +109,8 @@ struct ae_ctx {
   bool use_graph = false;  // capture and replay the launch sequence
   CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
   CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
+  CUtensorMap map_attn_o;                       // attention O partials (fp32)
+  CUtensorMap map_qkv_act;                      // q|k|v activations, boxes 16 rows x 64
   int act_box_rows = 0;
   float* sumsq = nullptr;    // [D/128][M] adaRMS sum of squares per 128-feature tile
   float* part = nullptr;     // split-K partials
@@ -226,6 +229,7 @@ struct AttnArgs {
   const int* n_valid;     // [batch]
   int max_rows;           // row stride of valid_idx
   int plan_rows;          // longest physical prefix of the bound requests (work split bound)
+  int layer_row0;         // first row of this layer in the prefix K/V maps
   int batch, H, Hq, Hkv, dh;
   float scale;
   int q_tiles, chunks_per_cta, max_splits;  // set by the planner
@@ -239,7 +243,14 @@ size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int 
 // result above a.max_units means the cap cannot be met).
 size_t attn_plan_units(AttnArgs a, int sm_count);
 cudaError_t attn_kernel_setup();
-cudaError_t launch_attn_tc(AttnArgs a, bf16* o, int sm_count, cudaStream_t s, bool pdl);
+// qmap: bf16 [maxM, (Hq + 2 Hkv) dh] view of the q|k|v activations, boxes 16 rows x 64.
+// kmap, vmap: bf16 [L * total_rows, Hkv dh] views of the bound prefix K / V, boxes 64 rows x 64.
+// omap: fp32 [units * 128, dh] view of part_o, boxes of 128 rows x 32 columns, 128-byte swizzle.
+cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const CUtensorMap& omap, AttnArgs a, bf16* o, int sm_count,
+                           cudaStream_t s, bool pdl);
+cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows);
+cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int dh);
 
 // ---- bf16 path driver (ae_fast.cu)
 bool fast_path_supported(const Dims& d, std::string* why);
@@ -251,6 +262,7 @@ struct AttnScratch {
   float* part_o;
   float2* part_ml;
   int max_units;
+  CUtensorMap omap;  // make_attn_o_map of part_o
 };
 int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
                      cudaError_t* err, const AttnScratch* attn_scratch = nullptr);

@@ -114,6 +114,11 @@ extern "C" ae_status ae_sample_noalloc(ae_ctx* c, const float* noise, int n_step
   }
   sc.part_o = base;
   sc.part_ml = reinterpret_cast<float2*>(base + (size_t)sc.max_units * 128 * d.dh);
+  e = ae::make_attn_o_map(&sc.omap, sc.part_o, (size_t)sc.max_units, d.dh);  // host-side encode only
+  if (e != cudaSuccess) {
+    c->last_msg = std::string("TMA descriptor of the static scratch: ") + cudaGetErrorString(e);
+    return AE_ERR_CUDA;
+  }
 
   const size_t xbytes = (size_t)B * d.H * d.A * sizeof(float);
   if (out != noise) {

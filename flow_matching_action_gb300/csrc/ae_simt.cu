@@ -445,6 +445,12 @@ int launch_attn_bf16(ae_ctx* c, int layer, cudaStream_t s) {
 
 cudaError_t launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
                               bool pdl) {
+  static bool carveout = false;  // same shared-memory carve-out as the other bf16-path kernels
+  if (!carveout) {
+    cudaFuncSetAttribute(k_final<bf16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    carveout = true;
+  }
   const Dims& d = c->d;
   const int M = c->bind.batch * d.H;
   const float* fin = t.fin + (size_t)step * 2 * d.D;
