@@ -69,18 +69,19 @@ __host__ __device__ inline uint32_t attn_tmem_cols(int dh) {
   return c;
 }
 
-// Start loading chunk c of KV head g into buffer `buf`.  Returns true when it
-// travels by TMA (completion on bar_kv), false when by cp.async (one commit
-// group).  Uniform for the CTA.  Gather code of a key: >= 0 physical prefix
-// row, -1 - i action row i, kSkip zero-fill.
+// Chunk c of KV head g into buffer `buf`, in two parts.  chunk_codes() reads
+// the chunk's gather codes into shared memory (>= 0 physical prefix row,
+// -1 - i action row i, kSkip zero-fill) and, when the chunk is one contiguous
+// run of 64 valid prefix rows, starts its TMA loads (completion on bar_kv) and
+// returns true.  Otherwise chunk_gather() copies it row by row with cp.async
+// (one commit group).  Both are uniform for the CTA.  Prefix rows and codes
+// come from the binding, so chunk_codes() may run before the preceding kernel
+// has finished; chunk_gather() reads action rows and must run after it.
 template <int DH>
-__device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorMap* kmap,
-                                              const CUtensorMap* vmap, uint8_t* smem,
-                                              const AttnSmem& L, uint64_t* bar_kv, int b, int g,
-                                              int n_pre, int n_keys, int c, int buf) {
-  constexpr int CPR = DH / 8;                    // 16-byte pieces per row
-  constexpr int RPW = CPR >= 32 ? 1 : 32 / CPR;  // rows per warp instruction
-  constexpr int PPL = CPR >= 32 ? CPR / 32 : 1;  // pieces per lane per row
+__device__ __forceinline__ bool chunk_codes(const AttnArgs& a, const CUtensorMap* kmap,
+                                            const CUtensorMap* vmap, uint8_t* smem, const AttnSmem& L,
+                                            uint64_t* bar_kv, int b, int g, int n_pre, int n_keys,
+                                            int c, int buf) {
   constexpr int kdb = DH / 64;
   const int key0 = c * kChunk;
   const int nk = min(kChunk, n_keys - key0);
@@ -100,22 +101,31 @@ __device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorM
     ix[j] = code;
   }
   __syncthreads();
-  uint8_t* ks = smem + L.k[buf];
-  uint8_t* vs = smem + L.v[buf];
   // codes increase strictly over a chunk's prefix keys: first and last decide
   const bool contiguous = nk == kChunk && ix[0] >= 0 && ix[kChunk - 1] - ix[0] == kChunk - 1;
-  if (contiguous) {
-    if (threadIdx.x == 0) {
-      mbar_arrive_expect_tx(&bar_kv[buf], 2u * kdb * kChunk * 128);
-      const int row = a.layer_row0 + ix[0];
+  if (contiguous && threadIdx.x == 0) {
+    uint8_t* ks = smem + L.k[buf];
+    uint8_t* vs = smem + L.v[buf];
+    mbar_arrive_expect_tx(&bar_kv[buf], 2u * kdb * kChunk * 128);
+    const int row = a.layer_row0 + ix[0];
 #pragma unroll
-      for (int kb = 0; kb < kdb; ++kb) {
-        tma_load_2d_nohint(ks + kb * kChunk * 128, kmap, &bar_kv[buf], g * DH + kb * 64, row);
-        tma_load_2d_nohint(vs + kb * kChunk * 128, vmap, &bar_kv[buf], g * DH + kb * 64, row);
-      }
+    for (int kb = 0; kb < kdb; ++kb) {
+      tma_load_2d_nohint(ks + kb * kChunk * 128, kmap, &bar_kv[buf], g * DH + kb * 64, row);
+      tma_load_2d_nohint(vs + kb * kChunk * 128, vmap, &bar_kv[buf], g * DH + kb * 64, row);
     }
-    return true;
   }
+  return contiguous;
+}
+
+template <int DH>
+__device__ __forceinline__ void chunk_gather(const AttnArgs& a, uint8_t* smem, const AttnSmem& L,
+                                             int b, int g, int buf) {
+  constexpr int CPR = DH / 8;                    // 16-byte pieces per row
+  constexpr int RPW = CPR >= 32 ? 1 : 32 / CPR;  // rows per warp instruction
+  constexpr int PPL = CPR >= 32 ? CPR / 32 : 1;  // pieces per lane per row
+  const int* ix = reinterpret_cast<const int*>(smem + L.idx) + buf * kChunk;
+  uint8_t* ks = smem + L.k[buf];
+  uint8_t* vs = smem + L.v[buf];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / (32 / RPW);  // row within this warp instruction
   const int pl = lane % (32 / RPW);   // piece index of the lane
@@ -145,7 +155,16 @@ __device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorM
     }
   }
   cp_async_commit();
-  return false;
+}
+
+template <int DH>
+__device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorMap* kmap,
+                                              const CUtensorMap* vmap, uint8_t* smem,
+                                              const AttnSmem& L, uint64_t* bar_kv, int b, int g,
+                                              int n_pre, int n_keys, int c, int buf) {
+  const bool tma = chunk_codes<DH>(a, kmap, vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c, buf);
+  if (!tma) chunk_gather<DH>(a, smem, L, b, g, buf);
+  return tma;
 }
 
 template <int DH>
@@ -165,8 +184,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(bar_s + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
 
+  // Everything up to the first chunk's prefix loads depends only on the
+  // binding (n_valid, valid_idx, prefix K/V) and may overlap the preceding
+  // kernel; the query tile and action rows are read after pdl_wait().
   pdl_trigger();
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int u = blockIdx.x;
   const int sp = u % a.max_splits;
@@ -182,7 +203,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int n_chunks = (n_keys + kChunk - 1) / kChunk;
   const int c_begin = sp * a.chunks_per_cta;
   const int c_end = min(c_begin + a.chunks_per_cta, n_chunks);
-  if (c_begin >= c_end) return;  // uniform for the CTA
+  if (c_begin >= c_end) {  // uniform for the CTA
+    pdl_wait();
+    return;
+  }
   const int n_my = c_end - c_begin;
   const uint32_t tcols = attn_tmem_cols(dh);
 
@@ -199,6 +223,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tmem_relinquish();
   }
   __syncthreads();
+  bool tma_cur = chunk_codes<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c_begin, 0);
+  pdl_wait();
+  if (!tma_cur) chunk_gather<DH>(a, smem, L, b, g, 0);
   // ---- Q tile by TMA: 16-row groups of the fold (a group never straddles heads)
   if (threadIdx.x == 0) {
     int nbox = 0;
@@ -217,7 +244,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                            b * a.H + tok0);
     }
   }
-  bool tma_cur = load_kv_chunk<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c_begin, 0);
 
   tc_fence_before();
   __syncthreads();
@@ -276,24 +302,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       break;
     }
     tc_fence_after();
+    // scores in the log2 domain: s * scale * log2(e), so exp() becomes one exp2
+    const float sl2 = a.scale * 1.4426950408889634f;
     float s[kChunk];
-#pragma unroll
-    for (int c0 = 0; c0 < kChunk; c0 += 16) {
-      float v[16];
-      tmem_ld16(tm_s + lane_off + (uint32_t)c0, v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) s[c0 + j] = v[j] * a.scale;
-    }
+    tmem_ld64(tm_s + lane_off, s);
     float cmax = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j)
+    for (int j = 0; j < kChunk; ++j) {
+      s[j] *= sl2;
       if (j < nk) cmax = fmaxf(cmax, s[j]);
+    }
     // raise the exponent reference; O (in TMEM) and l follow it
     float factor = 1.f;
     if (ci == 0) {
       m_ref = cmax;
-    } else if (cmax > m_ref + kRescaleMargin) {
-      factor = __expf(m_ref - cmax);
+    } else if (cmax > m_ref + kRescaleMargin * 1.4426950408889634f) {
+      factor = exp2f(m_ref - cmax);
       m_ref = cmax;
     }
     if (__any_sync(0xffffffffu, factor != 1.f)) {
@@ -310,8 +334,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint32_t pk[kChunk / 2];
 #pragma unroll
     for (int j = 0; j < kChunk; j += 2) {
-      const float p0 = (j < nk) ? __expf(s[j] - m_ref) : 0.f;
-      const float p1 = (j + 1 < nk) ? __expf(s[j + 1] - m_ref) : 0.f;
+      const float p0 = (j < nk) ? exp2f(s[j] - m_ref) : 0.f;
+      const float p1 = (j + 1 < nk) ? exp2f(s[j + 1] - m_ref) : 0.f;
       const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
       // the row sum uses the bf16-rounded weights, the values P V multiplies
       const float2 pr = __bfloat1622float2(pb);
@@ -363,16 +387,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;
     uint8_t* stg = smem + L.k[0];
 #pragma unroll 1
-    for (int c0 = 0; c0 < dh; c0 += 16) {
-      float v[16];
-      tmem_ld16(tm_o + lane_off + (uint32_t)c0, v);
-      uint8_t* box = stg + (c0 >> 5) * (128 * 128);
-      const int cc0 = (c0 & 31) >> 2;
+    for (int c0 = 0; c0 < dh; c0 += 64) {
+      float v[64];
+      tmem_ld64(tm_o + lane_off + (uint32_t)c0, v);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<float4*>(box + sw128_offset(row, cc0 + j)) =
-            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      for (int q = 0; q < 16; ++q) {  // 16 float4 = two 32-column boxes
+        const int col = c0 + 4 * q;
+        uint8_t* box = stg + (col >> 5) * (128 * 128);
+        *reinterpret_cast<float4*>(box + sw128_offset(row, (col & 31) >> 2)) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
     }
+    // the stored maximum is in the log2 domain of the scaled scores
     if (valid_row) a.part_ml[unit * 128 + row] = make_float2(m_ref, l);
     fence_proxy_async_smem();
     __syncthreads();
@@ -411,7 +437,7 @@ __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
   float l = 0.f, acc = 0.f;
   for (int sp = 0; sp < n_splits; ++sp) {
     const float2 ml = a.part_ml[(unit0 + sp) * 128 + row];
-    const float w = __expf(ml.x - m);
+    const float w = exp2f(ml.x - m);
     l += ml.y * w;
     acc += a.part_o[((unit0 + sp) * 128 + row) * a.dh + d] * w;
   }

@@ -152,8 +152,12 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   auto mod = [&](int l, int j) { return t.mod + (((size_t)step * L + l) * 2 + j) * 3 * D; };
 
   // h = x W_in^T + b_in; y = adaRMS1 of layer 0
+  // The first kernel of a sample is a full dependency of whatever precedes it
+  // on the stream (the bind kernel among them); every later kernel is chained
+  // to its predecessor, so all of them start after the bind has completed and
+  // may read its tables before griddepcontrol.wait.
   ck(launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0),
-                        mod(0, 0) + D, eps, y, s, pdl));
+                        mod(0, 0) + D, eps, y, s, pdl && step > 0));
   ++n;
   for (int l = 0; l < L; ++l) {
     dump(l);
