@@ -364,6 +364,9 @@ ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
     const char* pd = getenv("AE_PDL");
     c->use_graph = !(g && g[0] == '0');
     c->pdl = !(pd && pd[0] == '0');
+    // AE_KS=q,o,g,d caps the split-K factor of each projection (0 = no cap)
+    if (const char* ks = getenv("AE_KS"))
+      sscanf(ks, "%d,%d,%d,%d", &c->ks_cap[0], &c->ks_cap[1], &c->ks_cap[2], &c->ks_cap[3]);
   }
   if (st == AE_OK) {
     e = cudaStreamSynchronize(c->stream);

@@ -94,6 +94,19 @@ cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long col
   return make_map(map, ptr, rows, cols, box_rows);
 }
 
+cudaError_t make_f32_3d_map(CUtensorMap* map, const void* ptr, long d0, long d1, long d2, int box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)d0 * 4, (cuuint64_t)d0 * d1 * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int dh) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
@@ -127,10 +140,10 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const int nqkv = d.qkvdim(), qd = d.qdim();
   const float eps = (float)d.eps;
   const int sm = c->sm_count;
-  const GemmPlan pq = plan_gemm(nqkv, D, M, sm, 1);
-  const GemmPlan po = plan_gemm(D, qd, M, sm, 2);
-  const GemmPlan pg = plan_gemm(2 * F, D, M, sm, 1);
-  const GemmPlan pd = plan_gemm(D, F, M, sm, 2);
+  const GemmPlan pq = plan_gemm(nqkv, D, M, sm, 1, c->ks_cap[0]);
+  const GemmPlan po = plan_gemm(D, qd, M, sm, 2, c->ks_cap[1]);
+  const GemmPlan pg = plan_gemm(2 * F, D, M, sm, 1, c->ks_cap[2]);
+  const GemmPlan pd = plan_gemm(D, F, M, sm, 2, c->ks_cap[3]);
   // the four GEMMs share one token tiling (it depends on M only)
   *err = fast_activation_maps(c, pq.tok_tile);
   if (*err != cudaSuccess) return 0;
@@ -174,6 +187,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.rope_cs = c->rope_cs;
     a.dh = d.dh;
     a.n_rot_heads = d.Hq + d.Hkv;
+    a.out_rows = c->max_batch * d.H;
     if (pq.ksplit == 1) {
       a.e_mode = kEQkvRope;
       a.out_bf16 = qkv;
@@ -234,6 +248,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.status = c->status_dev;
     a.w_row0 = l * 2 * F;
     a.w_next_row0 = ln * 2 * F;
+    a.out_rows = c->max_batch * d.H;
     if (pg.ksplit == 1) {
       a.e_mode = kEGeglu;
       a.out_bf16 = m;

@@ -16,6 +16,7 @@
 // blog, section 2): split-K sum + gated residual + the NEXT adaRMS (rms over
 // the row, (1 + scale), + shift) into the bf16 operand of the next GEMM.
 #include <math.h>
+#include <string.h>
 
 #include "ae_internal.h"
 #include "ae_tc.cuh"
@@ -44,7 +45,7 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
-              const __grid_constant__ TcGemmArgs a) {
+              const __grid_constant__ CUtensorMap omap, const __grid_constant__ TcGemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int S = a.stages;
@@ -151,7 +152,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar(1, 128);
     const bool go = votes[0] && votes[1] && votes[2] && votes[3];
     pdl_wait();
-    if (go) {
+    if (go && a.tma_out) {
+      // TMEM -> 128-byte-swizzled staging in the drained pipeline buffers -> TMA stores
+      tc_fence_after();
+      uint8_t* stg = smem;
+      const int TT = a.tok_tile;
+      const uint32_t trow = (uint32_t)(32 * q) << 16;
+      if (a.e_mode == kEPartial) {
+        // warp q owns one box: [TT tokens][32 fp32] of output features 32q..32q+31
+        uint8_t* box = stg + (size_t)q * TT * 128;
+        const uint32_t lo = (uint32_t)((lane & 3) << 2);
+        for (int c0 = 0; c0 < TT; c0 += 16) {
+          float v[16];
+          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = c0 + j;
+            *reinterpret_cast<float*>(box + t * 128 + ((((lane >> 2) ^ (t & 7))) << 4) + lo) = v[j];
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&omap, box, n_tile * 128 + 32 * q, t0, ks);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        __syncwarp();
+      } else if (a.e_mode == kEQkvRope) {
+        // two boxes [TT tokens][64 bf16]: first and second members of the tile's 64 pairs
+        const int half = a.dh >> 1;
+        const int n0 = n_tile * 128;
+        const int hb = n0 / a.dh;
+        const int pair0 = (n0 - hb * a.dh) >> 1;
+        const int p = n - hb * a.dh;
+        const int pair = p >> 1, odd = p & 1;
+        const int pl = pair - pair0;
+        const bool rot = hb < a.n_rot_heads;
+        uint8_t* box = stg + (size_t)odd * TT * 128;
+        const uint32_t lo = (uint32_t)((pl & 7) << 1);
+        float2 csn[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t = t0 + j;
+          csn[j] = (rot && t < a.M) ? __ldg(a.rope_cs + (size_t)t * half + pair) : make_float2(1.f, 0.f);
+        }
+        for (int c0 = 0; c0 < TT; c0 += 16) {
+          float2 csv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) csv[j] = csn[j];
+          if (c0 + 16 < TT) {  // table values of the next 16 tokens, loaded one step ahead
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int t = t0 + c0 + 16 + j;
+              csn[j] = (rot && t < a.M) ? __ldg(a.rope_cs + (size_t)t * half + pair) : make_float2(1.f, 0.f);
+            }
+          }
+          float v[16];
+          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            const int t = c0 + j;
+            float outv = v[j];
+            if (rot) {
+              const float x1 = odd ? other : v[j], x2 = odd ? v[j] : other;
+              outv = odd ? (x2 * csv[j].x + x1 * csv[j].y) : (x1 * csv[j].x - x2 * csv[j].y);
+            }
+            *reinterpret_cast<bf16*>(box + t * 128 + (((pl >> 3) ^ (t & 7)) << 4) + lo) =
+                __float2bfloat16_rn(outv);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar(1, 128);
+        if (threadIdx.x == 64) {
+          tma_store_2d(&omap, stg, hb * a.dh + pair0, t0);
+          tma_store_2d(&omap, stg + (size_t)TT * 128, hb * a.dh + half + pair0, t0);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+      } else {  // kEGeglu: one box [TT tokens][64 bf16] of GeGLU outputs n/2
+        const int jl = 16 * q + (lane >> 1);
+        const uint32_t lo = (uint32_t)((jl & 7) << 1);
+        for (int c0 = 0; c0 < TT; c0 += 16) {
+          float v[16];
+          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            const int t = c0 + j;
+            if (!(lane & 1))
+              *reinterpret_cast<bf16*>(stg + t * 128 + (((jl >> 3) ^ (t & 7)) << 4) + lo) =
+                  __float2bfloat16_rn(gelu_tanh(v[j]) * other);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar(1, 128);
+        if (threadIdx.x == 64) {
+          tma_store_2d(&omap, stg, n_tile * 64, t0);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+      }
+    } else if (go) {
       tc_fence_after();
       for (int c0 = 0; c0 < a.tok_tile; c0 += 16) {
         float v[16];
@@ -353,7 +456,7 @@ size_t tc_gemm_smem_bytes(int stages, int tok_tile) {
   return 1024 + (size_t)stages * (kATileBytes + (size_t)tok_tile * 128) + (2 * stages + 1) * 8 + 32;
 }
 
-GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split) {
+GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split) {
   GemmPlan p;
   p.N = N;
   p.K = K;
@@ -367,6 +470,7 @@ GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split) {
   p.kb_total = K / 64;
   const int base = p.n_tiles * p.tok_tiles;
   int ks = sm_count / base;
+  if (max_split > 0 && ks > max_split) ks = max_split;
   if (ks < min_split) ks = min_split;
   if (ks < 1) ks = 1;
   if (ks > p.kb_total) ks = p.kb_total;
@@ -379,6 +483,8 @@ GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split) {
   int stages = per_cta < 8 ? per_cta : 8;
   if (stages < 2) stages = 2;
   while (stages > 2 && tc_gemm_smem_bytes(stages, tt) > 200 * 1024) --stages;
+  // the epilogue stages its output tile (up to tt x 128 fp32) in the drained pipeline buffers
+  while ((size_t)stages * (kATileBytes + (size_t)tt * 128) < (size_t)tt * 512 && stages < 8) ++stages;
   p.stages = stages;
   p.smem = tc_gemm_smem_bytes(stages, tt);
   p.grid = base * ks;
@@ -414,7 +520,22 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
   a.kb_total = p.kb_total;
   a.stages = p.stages;
   a.tmem_cols = p.tmem_cols;
-  return launch_k(k_tc_gemm, dim3(p.grid), dim3(kThreads), p.smem, s, pdl, wmap, amap, a);
+  CUtensorMap omap;
+  memset(&omap, 0, sizeof(omap));
+  a.tma_out = 0;
+  cudaError_t e = cudaSuccess;
+  if (a.e_mode == kEPartial) {
+    e = make_f32_3d_map(&omap, a.part, p.N, a.M, p.ksplit, p.tok_tile);
+    a.tma_out = 1;
+  } else if (a.e_mode == kEQkvRope && a.dh >= 128) {
+    e = make_bf16_map(&omap, a.out_bf16, a.out_rows, p.N, p.tok_tile);
+    a.tma_out = 1;
+  } else if (a.e_mode == kEGeglu) {
+    e = make_bf16_map(&omap, a.out_bf16, a.out_rows, p.N / 2, p.tok_tile);
+    a.tma_out = 1;
+  }
+  if (e != cudaSuccess) return e;
+  return launch_k(k_tc_gemm, dim3(p.grid), dim3(kThreads), p.smem, s, pdl, wmap, amap, omap, a);
 }
 
 cudaError_t launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,

@@ -107,6 +107,7 @@ struct ae_ctx {
   bool fast = false;
   bool pdl = false;        // chain kernels by programmatic dependent launch
   bool use_graph = false;  // capture and replay the launch sequence
+  int ks_cap[4] = {0, 0, 0, 0};  // split-K caps of the QKV, O, gate/up, down GEMMs (0 = none)
   CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
   CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
   CUtensorMap map_attn_o;                       // attention O partials (fp32)
@@ -191,6 +192,8 @@ struct TcGemmArgs {
   int w_next_row0;      // first row of the matrix to prefetch into L2 (-1: none)
   int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
   int e_mode;
+  int tma_out;          // set by the launcher: the epilogue stages its tile and stores it by TMA
+  int out_rows;         // rows of out_bf16's buffer (its TMA view)
   float* part;          // kEPartial: [ksplit][M][N]
   bf16* out_bf16;       // kEQkvRope: [M][N]; kEGeglu: [M][N/2]
   const float2* rope_cs;
@@ -204,7 +207,7 @@ struct GemmPlan {
 };
 
 size_t tc_gemm_smem_bytes(int stages, int tok_tile);
-GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split);
+GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split = 0);
 cudaError_t gemm_kernel_setup();
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
                            TcGemmArgs a, cudaStream_t s, bool pdl);
@@ -250,6 +253,8 @@ cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, con
                            const CUtensorMap& omap, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl);
 cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows);
+// fp32 [d2][d1][d0] view with boxes {32, box1, 1}, 128-byte swizzle (split-K partials)
+cudaError_t make_f32_3d_map(CUtensorMap* map, const void* ptr, long d0, long d1, long d2, int box1);
 cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int dh);
 
 // ---- bf16 path driver (ae_fast.cu)
