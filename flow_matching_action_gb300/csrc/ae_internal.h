@@ -136,6 +136,11 @@ struct ae_ctx {
     }
   } graph_key;
 
+  // Persistent path: the whole sample as one cooperative kernel (ae_persist.cu).
+  bool persist = false;
+  unsigned* grid_sync = nullptr;  // barrier arrival count and abort word (separate 128-byte lines)
+  int persist_spin_ns = 100, persist_l2_pf = 0;
+
   int64_t launches_sample = 0, launches_bind = 0, device_bytes = 0;
   std::vector<void*> allocations;
   std::string last_msg;
@@ -273,5 +278,66 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
                      cudaError_t* err, const AttnScratch* attn_scratch = nullptr);
 // The cached time table of n_steps, or nullptr (never allocates).
 const TimeTable* find_time_table(const ae_ctx* c, int n_steps);
+void attn_plan(AttnArgs& a, int sm_count);
+
+// ---- persistent kernel (ae_persist.cu)
+struct PersistGemm {
+  int n_tiles, ksplit, kb_total;
+  int rows_per_layer;   // rows of one layer's matrix in the stacked weight
+  int e_mode;           // EMode
+  int tma_out;          // kEQkvRope: output by TMA store (head_dim >= 128)
+};
+// Everything one launch needs, passed by value (__grid_constant__).  GEMM
+// index 0..3 = merged QKV, O, merged gate/up, down.
+struct PersistParams {
+  CUtensorMap w[4];     // stacked weights, boxes 128 rows x 64
+  CUtensorMap act[4];   // bf16 activation operands, boxes tok_tile rows x 64
+  CUtensorMap out[4];   // epilogue outputs (bf16 boxes or fp32 split-K partial boxes)
+  CUtensorMap q16;      // q|k|v activations, boxes 16 rows x 64
+  CUtensorMap pk, pv;   // bound prefix K / V, boxes 64 rows x 64 (used when >= 64 rows)
+  CUtensorMap attn_o;   // attention O partials, boxes 128 rows x 32 fp32
+  PersistGemm g[4];
+  const bf16* wptr[4];  // the same stacked weights as w[], for L2 prefetches
+  int L, D, F, A, H, Hq, Hkv, dh, qkvdim, n_rot_heads;
+  int M, batch, tok_tile, tok_tiles, n_steps;
+  float eps, delta, scale;
+  long total_rows;
+  int max_rows, q_tiles, chunks_per_cta, max_splits;
+  uint32_t data_bytes, row_bytes;   // shared-memory layout
+  int stages;                       // GEMM pipeline stages
+  int spin_ns;                      // grid-barrier poll back-off
+  int l2_pf;                        // pull later GEMMs' weights into L2 during row phases
+  const int* valid_idx;
+  const int* n_valid;
+  const bf16* pk_ptr;
+  const bf16* pv_ptr;
+  float* attn_o_ptr;
+  float2* attn_ml;
+  float* x;
+  float* h;
+  bf16* y;
+  bf16* qkv;
+  bf16* o;
+  bf16* m;
+  float* part0;
+  float* part1;
+  const float2* rope_cs;
+  const float* mod;
+  const float* fin;
+  const bf16* w_in;
+  const bf16* b_in;
+  const bf16* w_out;
+  const bf16* b_out;
+  float* dump;
+  int* status;
+  unsigned* bar_count;  // grid-barrier arrivals, zero at launch
+  int* grid_abort;
+};
+size_t persist_smem_bytes(int tok_tile, int dh, int D, int A, uint32_t* data_bytes, uint32_t* row_bytes,
+                          int* stages);
+cudaError_t persist_setup(size_t smem, int* blocks_per_sm);
+cudaError_t launch_persistent(const PersistParams& P, int grid, size_t smem, cudaStream_t s);
+// One ae_sample of n_steps on the persistent path, the flow state in place in x.
+cudaError_t sample_persistent(ae_ctx* c, const TimeTable& t, int n_steps, float* x, cudaStream_t s);
 
 }  // namespace ae
