@@ -26,11 +26,18 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;           // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+// Warp 0 issues TMA, warp 1 MMA, warps 2.. run the epilogue: EW = 4 (one per
+// TMEM lane quarter) for token tiles up to 64, EW = 8 (two per quarter, each
+// taking half of the token columns) for longer tiles, whose epilogue would
+// otherwise be a long serial chain per thread.
+constexpr int kThreadsFor(int ew) { return 64 + 32 * ew; }
 constexpr int kATileBytes = 128 * 128;  // 128 weight rows x 64 bf16
 
+// gelu_tanh(g) = 0.5 g (1 + tanh(u)), u = sqrt(2/pi) (g + 0.044715 g^3), written
+// with 1 + tanh(u) = 2 / (1 + e^{-2u}): one exponential and one division.
 __device__ __forceinline__ float gelu_tanh(float g) {
-  return 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
+  const float u2 = 1.5957691216057308f * (g + 0.044715f * g * g * g);
+  return __fdividef(g, 1.f + __expf(-u2));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -39,13 +46,28 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+// Named barrier with a compile-time id, so the kernel reserves only the
+// barriers it uses (ids 1..5) and co-resident CTAs keep theirs.
+template <int ID>
+__device__ __forceinline__ void named_bar(int n) {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(n) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void quarter_bar(int q) {  // the two epilogue warps of lane quarter q
+  switch (q) {
+    case 0: named_bar<2>(64); break;
+    case 1: named_bar<3>(64); break;
+    case 2: named_bar<4>(64); break;
+    default: named_bar<5>(64); break;
+  }
+}
+
+template <int EW>
+__global__ void __launch_bounds__(kThreadsFor(EW), 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
               const __grid_constant__ CUtensorMap omap, const __grid_constant__ TcGemmArgs a) {
+  constexpr int kEpiWarps = EW;
+  constexpr int kEpiThreads = 32 * EW;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int S = a.stages;
@@ -57,7 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = empty + S;
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(tmem_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
-  volatile int* votes = reinterpret_cast<volatile int*>(tmem_base_p + 2);  // [4]
+  volatile int* votes = reinterpret_cast<volatile int*>(tmem_base_p + 2);  // [kEpiWarps]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int idx = blockIdx.x;
@@ -144,25 +166,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(tmem_full);
     }
   } else {
-    // ---------------- epilogue (warps 2..5: TMEM lanes 32 * (warp % 4) ..)
+    // ---------------- epilogue: warps 2..9, two per TMEM lane quarter (warp w
+    // reads lanes 32 (w % 4)..), splitting the token columns in two halves
     const int q = warp & 3;
+    const int e = warp - 2;       // 0..7
+    const int hf = e >> 2;        // which half of the token columns (EW == 8)
+    const int TT = a.tok_tile;
+    const int c_lo = hf ? a.tok_half : 0, c_hi = (hf || EW == 4) ? TT : a.tok_half;
     const int n = n_tile * 128 + 32 * q + lane;
     // every epilogue warp takes the same decision
-    if (lane == 0) votes[q] = (mbar_wait(tmem_full, 0, abort_flag, a.status) && !*abort_flag) ? 1 : 0;
-    named_bar(1, 128);
-    const bool go = votes[0] && votes[1] && votes[2] && votes[3];
+    if (lane == 0) votes[e] = (mbar_wait(tmem_full, 0, abort_flag, a.status) && !*abort_flag) ? 1 : 0;
+    named_bar<1>(kEpiThreads);
+    bool go = true;
+#pragma unroll
+    for (int i = 0; i < kEpiWarps; ++i) go = go && votes[i];
     pdl_wait();
     if (go && a.tma_out) {
       // TMEM -> 128-byte-swizzled staging in the drained pipeline buffers -> TMA stores
       tc_fence_after();
       uint8_t* stg = smem;
-      const int TT = a.tok_tile;
       const uint32_t trow = (uint32_t)(32 * q) << 16;
       if (a.e_mode == kEPartial) {
-        // warp q owns one box: [TT tokens][32 fp32] of output features 32q..32q+31
+        // lane quarter q owns one box: [TT tokens][32 fp32] of output features 32q..32q+31
         uint8_t* box = stg + (size_t)q * TT * 128;
         const uint32_t lo = (uint32_t)((lane & 3) << 2);
-        for (int c0 = 0; c0 < TT; c0 += 16) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
           float v[16];
           tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
 #pragma unroll
@@ -172,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        if (EW == 8) quarter_bar(q);  // both halves of the box are staged
+        if (hf == 0 && lane == 0) {
           tma_store_3d(&omap, box, n_tile * 128 + 32 * q, t0, ks);
           bulk_commit();
           bulk_wait_read_all();
@@ -194,14 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 csn[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int t = t0 + j;
+          const int t = t0 + c_lo + j;
           csn[j] = (rot && t < a.M) ? __ldg(a.rope_cs + (size_t)t * half + pair) : make_float2(1.f, 0.f);
         }
-        for (int c0 = 0; c0 < TT; c0 += 16) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
           float2 csv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) csv[j] = csn[j];
-          if (c0 + 16 < TT) {  // table values of the next 16 tokens, loaded one step ahead
+          if (c0 + 16 < c_hi) {  // table values of the next 16 tokens, loaded one step ahead
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int t = t0 + c0 + 16 + j;
@@ -224,17 +252,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        named_bar(1, 128);
+        named_bar<1>(kEpiThreads);
         if (threadIdx.x == 64) {
           tma_store_2d(&omap, stg, hb * a.dh + pair0, t0);
           tma_store_2d(&omap, stg + (size_t)TT * 128, hb * a.dh + half + pair0, t0);
           bulk_commit();
           bulk_wait_read_all();
         }
+        __syncwarp();
       } else {  // kEGeglu: one box [TT tokens][64 bf16] of GeGLU outputs n/2
         const int jl = 16 * q + (lane >> 1);
         const uint32_t lo = (uint32_t)((jl & 7) << 1);
-        for (int c0 = 0; c0 < TT; c0 += 16) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
           float v[16];
           tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
 #pragma unroll
@@ -247,16 +276,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        named_bar(1, 128);
+        named_bar<1>(kEpiThreads);
         if (threadIdx.x == 64) {
           tma_store_2d(&omap, stg, n_tile * 64, t0);
           bulk_commit();
           bulk_wait_read_all();
         }
+        __syncwarp();
       }
     } else if (go) {
       tc_fence_after();
-      for (int c0 = 0; c0 < a.tok_tile; c0 += 16) {
+      for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
         float v[16];
         tmem_ld16(tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
         if (a.e_mode == kEPartial) {
@@ -326,10 +356,18 @@ __global__ void k_reduce_qkv(const float* __restrict__ part, int ks_n, int M, in
   const int t = (int)(idx / np), pp = (int)(idx - (long)t * np);
   const int n = 2 * pp;
   float x1 = 0.f, x2 = 0.f;
-  for (int j = 0; j < ks_n; ++j) {
-    const float2 v = *reinterpret_cast<const float2*>(part + ((size_t)j * M + t) * N + n);
-    x1 += v.x;
-    x2 += v.y;
+  for (int j0 = 0; j0 < ks_n; j0 += 8) {  // eight splits in flight, summed in split order
+    float2 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      v[j] = j0 + j < ks_n ? __ldcg(reinterpret_cast<const float2*>(part + ((size_t)(j0 + j) * M + t) * N + n))
+                           : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j0 + j < ks_n) {
+        x1 += v[j].x;
+        x2 += v[j].y;
+      }
   }
   const int half = dh >> 1;
   const int hb = n / dh, pair = (n - hb * dh) >> 1;
@@ -344,7 +382,6 @@ __global__ void k_reduce_qkv(const float* __restrict__ part, int ks_n, int M, in
 }
 
 constexpr int kRowThreads = 256;
-constexpr int kNormThreads = 1024;
 
 template <int NT>
 __device__ float block_sum(float v, float* red) {
@@ -357,52 +394,75 @@ __device__ float block_sum(float v, float* red) {
   return t;
 }
 
-// Sum of `ks_n` split-K partials p[j * stride] in split order; the loads are
-// issued eight at a time so a thread keeps eight in flight.
-__device__ __forceinline__ float sum_splits(const float* __restrict__ p, int ks_n, size_t stride) {
-  float s = 0.f;
-  int j = 0;
-  for (; j + 8 <= ks_n; j += 8) {
-    float v[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = __ldcg(p + (size_t)(j + e) * stride);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s += v[e];
-  }
-  for (; j < ks_n; ++j) s += __ldcg(p + (size_t)j * stride);
-  return s;
-}
-
 // One token row: h += gate * (sum of the split-K partials, in split order);
 // then, if `scale` is given, y = adaRMS(h) with the next sublayer's
-// (scale, shift) as the bf16 operand of the next GEMM.
-__global__ void __launch_bounds__(kNormThreads) k_resid_norm(const float* __restrict__ part, int ks_n,
-                                                            int M, int D, float* __restrict__ h,
-                                                            const float* __restrict__ gate,
-                                                            const float* __restrict__ scale,
-                                                            const float* __restrict__ shift, float eps,
-                                                            bf16* __restrict__ y) {
+// (scale, shift) as the bf16 operand of the next GEMM.  A thread owns COLS
+// columns and issues the loads of SB splits of all of them before it adds
+// (a row costs about ceil(ks / SB) L2 round trips).
+template <int NT, int COLS, int SB>
+__global__ void __launch_bounds__(NT) k_resid_norm(const float* __restrict__ part, int ks_n, int M, int D,
+                                                   float* __restrict__ h, const float* __restrict__ gate,
+                                                   const float* __restrict__ scale,
+                                                   const float* __restrict__ shift, float eps,
+                                                   bf16* __restrict__ y) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[kNormThreads / 32];
+  __shared__ float red[NT / 32];
   const int t = blockIdx.x;
   float* hr = h + (size_t)t * D;
+  const size_t stride = (size_t)M * D;
   float ss = 0.f;
-  for (int n = threadIdx.x; n < D; n += kNormThreads) {
-    const float s = sum_splits(part + (size_t)t * D + n, ks_n, (size_t)M * D);
-    const float hn = hr[n] + gate[n] * s;
-    hr[n] = hn;
-    ss += hn * hn;
+  for (int n0 = threadIdx.x; n0 < D; n0 += NT * COLS) {
+    float acc[COLS];
+    bool in[COLS];
+#pragma unroll
+    for (int e = 0; e < COLS; ++e) {
+      acc[e] = 0.f;
+      in[e] = n0 + e * NT < D;
+    }
+    const float* pp = part + (size_t)t * D + n0;
+    for (int j0 = 0; j0 < ks_n; j0 += SB) {
+      float v[SB][COLS];
+#pragma unroll
+      for (int j = 0; j < SB; ++j)
+#pragma unroll
+        for (int e = 0; e < COLS; ++e)
+          v[j][e] = (j0 + j < ks_n && in[e]) ? __ldcg(pp + (size_t)(j0 + j) * stride + e * NT) : 0.f;
+#pragma unroll
+      for (int j = 0; j < SB; ++j)
+#pragma unroll
+        for (int e = 0; e < COLS; ++e)
+          if (j0 + j < ks_n) acc[e] += v[j][e];
+    }
+#pragma unroll
+    for (int e = 0; e < COLS; ++e) {
+      if (!in[e]) continue;
+      const int n = n0 + e * NT;
+      const float hn = hr[n] + gate[n] * acc[e];
+      hr[n] = hn;
+      ss += hn * hn;
+    }
   }
   if (scale == nullptr) return;
-  ss = block_sum<kNormThreads>(ss, red);
+  ss = block_sum<NT>(ss, red);
   const float r = 1.0f / sqrtf(ss / (float)D + eps);
-  for (int n = threadIdx.x; n < D; n += kNormThreads)
+  for (int n = threadIdx.x; n < D; n += NT)
     y[(size_t)t * D + n] = __float2bfloat16_rn(hr[n] * r * (1.f + scale[n]) + shift[n]);
 }
 
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
+  const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(hv[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+
 // Action input projection h = x W_in^T + b_in of one token row, then the first
-// layer's adaRMS into the bf16 operand of its QKV GEMM.
+// layer's adaRMS into the bf16 operand of its QKV GEMM.  With A % 8 == 0 a
+// thread reads its four W_in rows as 16-byte vectors, four of each at a time.
 __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __restrict__ x,
                                                             const bf16* __restrict__ w_in,
                                                             const bf16* __restrict__ b_in, int D, int A,
@@ -418,13 +478,48 @@ __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __rest
   for (int k = threadIdx.x; k < A; k += kRowThreads) xs[k] = x[(size_t)t * A + k];
   __syncthreads();
   float* hr = h + (size_t)t * D;
+  const int A8 = A / 8;
+  const bool vec = (A & 7) == 0;
   float ss = 0.f;
-  for (int n = threadIdx.x; n < D; n += kRowThreads) {
-    float s = 0.f;
-    for (int k = 0; k < A; ++k) s += xs[k] * __bfloat162float(w_in[(size_t)n * A + k]);
-    const float hn = s + __bfloat162float(b_in[n]);
-    hr[n] = hn;
-    ss += hn * hn;
+  for (int n0 = threadIdx.x; n0 < D; n0 += 4 * kRowThreads) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (vec) {
+      for (int kb = 0; kb < A8; kb += 4) {
+        uint4 q[4][4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int n = n0 + e * kRowThreads;
+            q[e][j] = (n < D && kb + j < A8) ? __ldg(reinterpret_cast<const uint4*>(w_in + (size_t)n * A) + kb + j)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (kb + j >= A8) continue;
+            float f[8];
+            bf16x8_to_f32(q[e][j], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[e] += xs[8 * (kb + j) + i] * f[i];
+          }
+      }
+    } else {
+      for (int e = 0; e < 4; ++e) {
+        const int n = n0 + e * kRowThreads;
+        if (n < D)
+          for (int k = 0; k < A; ++k) acc[e] += xs[k] * __bfloat162float(w_in[(size_t)n * A + k]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = n0 + e * kRowThreads;
+      if (n >= D) continue;
+      const float hn = acc[e] + __bfloat162float(b_in[n]);
+      hr[n] = hn;
+      ss += hn * hn;
+    }
   }
   ss = block_sum<kRowThreads>(ss, red);
   const float r = 1.0f / sqrtf(ss / (float)D + eps);
@@ -442,10 +537,19 @@ __global__ void k_geglu_reduce(const float* __restrict__ part, int ks_n, int M, 
   if (idx >= (long)M * F) return;
   const int t = (int)(idx / F), j = (int)(idx - (long)t * F);
   float g = 0.f, u = 0.f;
-  for (int s = 0; s < ks_n; ++s) {
-    const float2 v = *reinterpret_cast<const float2*>(part + ((size_t)s * M + t) * 2 * F + 2 * j);
-    g += v.x;
-    u += v.y;
+  for (int s0 = 0; s0 < ks_n; s0 += 8) {  // eight splits in flight, summed in split order
+    float2 v[8];
+#pragma unroll
+    for (int j2 = 0; j2 < 8; ++j2)
+      v[j2] = s0 + j2 < ks_n
+                  ? __ldcg(reinterpret_cast<const float2*>(part + ((size_t)(s0 + j2) * M + t) * 2 * F + 2 * j))
+                  : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j2 = 0; j2 < 8; ++j2)
+      if (s0 + j2 < ks_n) {
+        g += v[j2].x;
+        u += v[j2].y;
+      }
   }
   m[idx] = __float2bfloat16_rn(gelu_tanh(g) * u);
 }
@@ -453,7 +557,7 @@ __global__ void k_geglu_reduce(const float* __restrict__ part, int ks_n, int M, 
 }  // namespace
 
 size_t tc_gemm_smem_bytes(int stages, int tok_tile) {
-  return 1024 + (size_t)stages * (kATileBytes + (size_t)tok_tile * 128) + (2 * stages + 1) * 8 + 32;
+  return 1024 + (size_t)stages * (kATileBytes + (size_t)tok_tile * 128) + (2 * stages + 1) * 8 + 64;
 }
 
 GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split) {
@@ -500,10 +604,12 @@ cudaError_t max_carveout(K kern) {
 }
 
 cudaError_t gemm_kernel_setup() {
-  cudaError_t e = cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-  if (e == cudaSuccess) e = max_carveout(k_tc_gemm);
+  cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_tc_gemm<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  if (e == cudaSuccess) e = max_carveout(k_tc_gemm<4>);
+  if (e == cudaSuccess) e = max_carveout(k_tc_gemm<8>);
   if (e == cudaSuccess) e = max_carveout(k_reduce_qkv);
-  if (e == cudaSuccess) e = max_carveout(k_resid_norm);
+  if (e == cudaSuccess) e = max_carveout(k_resid_norm<256, 4, 8>);
   if (e == cudaSuccess) e = max_carveout(k_inproj_norm);
   if (e == cudaSuccess) e = max_carveout(k_geglu_reduce);
   return e;
@@ -520,6 +626,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
   a.kb_total = p.kb_total;
   a.stages = p.stages;
   a.tmem_cols = p.tmem_cols;
+  a.tok_half = ((p.tok_tile / 2 + 15) / 16) * 16;
   CUtensorMap omap;
   memset(&omap, 0, sizeof(omap));
   a.tma_out = 0;
@@ -535,7 +642,9 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
     a.tma_out = 1;
   }
   if (e != cudaSuccess) return e;
-  return launch_k(k_tc_gemm, dim3(p.grid), dim3(kThreads), p.smem, s, pdl, wmap, amap, omap, a);
+  if (p.tok_tile > 64)
+    return launch_k(k_tc_gemm<8>, dim3(p.grid), dim3(kThreadsFor(8)), p.smem, s, pdl, wmap, amap, omap, a);
+  return launch_k(k_tc_gemm<4>, dim3(p.grid), dim3(kThreadsFor(4)), p.smem, s, pdl, wmap, amap, omap, a);
 }
 
 cudaError_t launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
@@ -548,8 +657,9 @@ cudaError_t launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, i
 cudaError_t launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
                               const float* scale, const float* shift, float eps, bf16* y,
                               cudaStream_t s, bool pdl) {
-  return launch_k(k_resid_norm, dim3(M), dim3(kNormThreads), 0, s, pdl, part, ks, M, D, h, gate,
-                  scale, shift, eps, y);
+  // 256 threads x 4 columns a row (measured faster than 1024 x 1 at 50 rows too)
+  return launch_k(k_resid_norm<256, 4, 8>, dim3(M), dim3(256), 0, s, pdl, part, ks, M, D, h, gate, scale, shift,
+                  eps, y);
 }
 
 cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D,

@@ -196,6 +196,7 @@ struct TcGemmArgs {
   int w_row0;           // first row of this layer's matrix in the stacked weight
   int w_next_row0;      // first row of the matrix to prefetch into L2 (-1: none)
   int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
+  int tok_half;         // first token column of the second epilogue half (multiple of 16)
   int e_mode;
   int tma_out;          // set by the launcher: the epilogue stages its tile and stores it by TMA
   int out_rows;         // rows of out_bf16's buffer (its TMA view)

@@ -330,6 +330,66 @@ __global__ void k_final(const float* __restrict__ h, int D, float eps, const flo
   }
 }
 
+// The same for the bf16 path: W_out rows read as 16-byte vectors; warp w
+// computes outputs w, w + 8, w + 16, w + 24 with all their loads in flight.
+__global__ void __launch_bounds__(256) k_final_bf16(const float* __restrict__ h, int D, float eps, const float* sf,
+                                                    const float* shf, const bf16* __restrict__ w_out,
+                                                    const bf16* __restrict__ b_out, int A, float delta,
+                                                    float* __restrict__ x) {
+  extern __shared__ float yf[];
+  __shared__ float red[8];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int m = blockIdx.x;
+  const float* hr = h + (size_t)m * D;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < D; k += 256) ss += hr[k] * hr[k];
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  ss = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) ss += red[w];
+  const float r = 1.0f / sqrtf(ss / (float)D + eps);
+  for (int k = threadIdx.x; k < D; k += 256) yf[k] = hr[k] * r * (1.f + sf[k]) + shf[k];
+  __syncthreads();
+  const int D8 = D / 8;
+  for (int a0 = warp; a0 < A; a0 += 32) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = lane; k0 < D8; k0 += 4 * 32) {
+      uint4 q[4][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int a = a0 + 8 * e, k8 = k0 + 32 * j;
+          q[e][j] = (a < A && k8 < D8) ? __ldg(reinterpret_cast<const uint4*>(w_out + (size_t)a * D) + k8)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int k8 = k0 + 32 * j;
+          if (k8 >= D8) continue;
+          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&q[e][j]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(hv[i]);
+            v[e] += yf[8 * k8 + 2 * i] * f.x + yf[8 * k8 + 2 * i + 1] * f.y;
+          }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int a = a0 + 8 * e;
+      const float sum = warp_sum(v[e]);
+      if (lane == 0 && a < A) x[(size_t)m * A + a] += delta * (sum + __bfloat162float(b_out[a]));
+    }
+  }
+}
+
 inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / per); }
 
 template <typename T>
@@ -447,7 +507,7 @@ cudaError_t launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x,
                               bool pdl) {
   static bool carveout = false;  // same shared-memory carve-out as the other bf16-path kernels
   if (!carveout) {
-    cudaFuncSetAttribute(k_final<bf16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    cudaFuncSetAttribute(k_final_bf16, cudaFuncAttributePreferredSharedMemoryCarveout,
                          (int)cudaSharedmemCarveoutMaxShared);
     carveout = true;
   }
@@ -455,6 +515,9 @@ cudaError_t launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x,
   const int M = c->bind.batch * d.H;
   const float* fin = t.fin + (size_t)step * 2 * d.D;
   const float delta = (float)(-1.0 / (double)t.n_steps);
+  if (d.D % 8 == 0)
+    return launch_k(k_final_bf16, dim3(M), dim3(256), d.D * sizeof(float), s, pdl, (const float*)c->h, d.D,
+                    (float)d.eps, fin, fin + d.D, (const bf16*)c->w_out, (const bf16*)c->b_out, d.A, delta, x);
   return launch_k(k_final<bf16>, dim3(M), dim3(256), d.D * sizeof(float), s, pdl, (const float*)c->h,
                   d.D, (float)d.eps, fin, fin + d.D, (const bf16*)c->w_out, (const bf16*)c->b_out,
                   d.A, delta, x);
