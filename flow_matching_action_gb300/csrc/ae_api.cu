@@ -367,6 +367,9 @@ ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
     // AE_KS=q,o,g,d caps the split-K factor of each projection (0 = no cap)
     if (const char* ks = getenv("AE_KS"))
       sscanf(ks, "%d,%d,%d,%d", &c->ks_cap[0], &c->ks_cap[1], &c->ks_cap[2], &c->ks_cap[3]);
+    // AE_ATTN_PIPE=1: pipelined eight-warp attention kernel
+    const char* ap = getenv("AE_ATTN_PIPE");
+    c->attn_pipe = ap && ap[0] == '1';
     // AE_PERSIST=1: the whole sample as one persistent cooperative kernel
     const char* pe = getenv("AE_PERSIST");
     if (st == AE_OK && pe && pe[0] == '1') {

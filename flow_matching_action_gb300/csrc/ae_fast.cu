@@ -87,6 +87,10 @@ cudaError_t fast_setup(ae_ctx* c) {
   if ((e = make_map(&c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D, 128)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_d, c->w_d, (long)d.L * d.D, d.F, 128)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_qkv_act, c->qkv, maxM, d.qkvdim(), 16)) != cudaSuccess) return e;
+  // query tiles load in boxes of whole padded heads where possible (fewer TMA issues)
+  const int hp = (d.H + 15) & ~15;
+  c->q_box_rows = hp % 64 == 0 ? 64 : (hp % 32 == 0 ? 32 : 16);
+  if ((e = make_map(&c->map_qtile, c->qkv, maxM, d.qkvdim(), c->q_box_rows)) != cudaSuccess) return e;
   const size_t units = attn_part_units(c->max_batch, d.H, d.Hq, d.Hkv, c->max_rows, c->sm_count);
   return make_attn_o_map(&c->map_attn_o, c->attn_o, units, d.dh);
 }
@@ -226,7 +230,9 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.part_ml = attn_scratch ? attn_scratch->part_ml : c->attn_ml;
       at.max_units = attn_scratch ? attn_scratch->max_units : 0;
       at.status = c->status_dev;
-      ck(launch_attn_tc(c->map_qkv_act, c->bind.map_pk, c->bind.map_pv,
+      at.pipe = c->attn_pipe ? 1 : 0;
+      at.q_box = c->q_box_rows;
+      ck(launch_attn_tc(c->map_qtile, c->bind.map_pk, c->bind.map_pv,
                         attn_scratch ? attn_scratch->omap : c->map_attn_o, at, o, sm, s, pdl));
       n += 2;
     }

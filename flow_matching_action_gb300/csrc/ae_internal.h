@@ -112,6 +112,8 @@ struct ae_ctx {
   CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
   CUtensorMap map_attn_o;                       // attention O partials (fp32)
   CUtensorMap map_qkv_act;                      // q|k|v activations, boxes 16 rows x 64
+  CUtensorMap map_qtile;                        // the same, boxes q_box_rows rows x 64 (attention query tiles)
+  int q_box_rows = 16;
   int act_box_rows = 0;
   float* sumsq = nullptr;    // [D/128][M] adaRMS sum of squares per 128-feature tile
   float* part = nullptr;     // split-K partials
@@ -140,6 +142,7 @@ struct ae_ctx {
   bool persist = false;
   unsigned* grid_sync = nullptr;  // barrier arrival count and abort word (separate 128-byte lines)
   int persist_spin_ns = 100, persist_l2_pf = 0;
+  bool attn_pipe = false;  // pipelined attention kernel
 
   int64_t launches_sample = 0, launches_bind = 0, device_bytes = 0;
   std::vector<void*> allocations;
@@ -243,6 +246,8 @@ struct AttnArgs {
   float scale;
   int q_tiles, chunks_per_cta, max_splits;  // set by the planner
   int max_units;          // cap on work units (0: none), for fixed-size scratch
+  int pipe;               // use the pipelined eight-warp kernel when the plan allows it
+  int q_box;              // rows of a query-tile TMA box (64, 32 or 16; divides the padded head length)
   float* part_o;          // [units][128][dh]
   float2* part_ml;        // [units][128]
   int* status;
@@ -252,7 +257,7 @@ size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int 
 // result above a.max_units means the cap cannot be met).
 size_t attn_plan_units(AttnArgs a, int sm_count);
 cudaError_t attn_kernel_setup();
-// qmap: bf16 [maxM, (Hq + 2 Hkv) dh] view of the q|k|v activations, boxes 16 rows x 64.
+// qmap: bf16 [maxM, (Hq + 2 Hkv) dh] view of the q|k|v activations, boxes a.q_box rows x 64.
 // kmap, vmap: bf16 [L * total_rows, Hkv dh] views of the bound prefix K / V, boxes 64 rows x 64.
 // omap: fp32 [units * 128, dh] view of part_o, boxes of 128 rows x 32 columns, 128-byte swizzle.
 cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
