@@ -321,6 +321,34 @@ def peaks():
 
 
 # ----------------------------------------------------------------------------- main
+def source_digest() -> str:
+    """SHA-256 over the CUDA sources and the C header (what the kernels are built from)."""
+    import glob
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(root, "flow_matching_action_gb300", "csrc", "*")))
+    for p in files + [os.path.join(root, "include", "ae.h")]:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per flow step from the committed ncu summary, or None when the
+    kernels changed since those counters were taken."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != source_digest():
+        return None
+    return rec.get("bytes_per_flow_step", {}).get(workload)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,7 +429,8 @@ def main():
         "bind_ms_median": bind_ms,
         "roofline": {"kernel": "ae_sample (all its launches, one flow step = 1 unit)",
                      "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm, "traffic": None,
+                     "frac": achieved_gbs / hbm, "traffic": measured_traffic(args.workload),
+                     "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)",
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_flow_step": bytes_fs},
         "clocks": res["clocks"],
@@ -423,7 +452,9 @@ def main():
                            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
                                         "unit": "TFLOP/s", "frac": tflops / tf_sust,
                                         "peak_kind": f"{peak_kind} sustained cuBLAS bf16",
-                                        "algorithmic_flops_per_flow_step": f2}}
+                                        "algorithmic_flops_per_flow_step": f2,
+                                        "traffic": measured_traffic(args.batched),
+                                        "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"}}
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, w)
     if dist_ctx.rank == 0:

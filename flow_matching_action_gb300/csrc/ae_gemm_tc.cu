@@ -5,7 +5,8 @@
 // are the MMA's M = 128 operand and the token tile is its N operand, so a
 // 50-token chunk costs a 64-wide tile instead of a 128-row one.  Both operands
 // arrive by TMA into 128-byte-swizzled shared memory (weights evict-first in
-// L2: each is read once per flow step); the fp32 accumulator lives in TMEM.
+// L2 when one token tile reads them: each is read once per flow step); the
+// fp32 accumulator lives in TMEM.
 // Merged Q/K/V and gate/up weights follow sglang PR #34599, item 1.
 //
 // Epilogues:
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   const int kb_end = (int)((long)(ks + 1) * a.kb_total / a.ksplit);
   const int n_it = kb_end - kb_begin;
   const int t0 = tt * a.tok_tile;
+  auto kcol = [&](int it) { return (kb_begin + it) * 64; };
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -117,7 +119,10 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     if (lane == 0) {
       prefetch_tensormap(&wmap);
       prefetch_tensormap(&amap);
-      const uint64_t pol_w = policy_evict_first();
+      // a weight slab read by one token tile is not read again this flow step:
+      // evict it first; with several token tiles the other tiles' CTAs read it
+      // moments later, so it keeps the normal policy
+      const uint64_t pol_w = a.tok_tiles > 1 ? policy_evict_normal() : policy_evict_first();
       const int row = a.w_row0 + n_tile * 128;
       const uint32_t bytes = kATileBytes + (uint32_t)btile;
       // Weights do not depend on the previous kernel: fill the first stages and
@@ -125,20 +130,20 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       const int pre = n_it < S ? n_it : S;
       for (int it = 0; it < pre; ++it) {
         mbar_arrive_expect_tx(&full[it], bytes);
-        tma_load_2d(smA + (size_t)it * kATileBytes, &wmap, &full[it], (kb_begin + it) * 64, row, pol_w);
+        tma_load_2d(smA + (size_t)it * kATileBytes, &wmap, &full[it], kcol(it), row, pol_w);
       }
       if (a.w_next_row0 >= 0)
         for (int it = 0; it < n_it; ++it)
           tma_prefetch_l2_2d(&wmap, (kb_begin + it) * 64, a.w_next_row0 + n_tile * 128);
       pdl_wait();
       for (int it = 0; it < pre; ++it)
-        tma_load_2d_nohint(smB + (size_t)it * btile, &amap, &full[it], (kb_begin + it) * 64, t0);
+        tma_load_2d_nohint(smB + (size_t)it * btile, &amap, &full[it], kcol(it), t0);
       int it = pre;
       for (; it < n_it; ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status)) break;
-        const int kc = (kb_begin + it) * 64;
+        const int kc = kcol(it);
         mbar_arrive_expect_tx(&full[s], bytes);
         tma_load_2d(smA + (size_t)s * kATileBytes, &wmap, &full[s], kc, row, pol_w);
         tma_load_2d_nohint(smB + (size_t)s * btile, &amap, &full[s], kc, t0);

@@ -142,6 +142,40 @@ def test_pi05_f32_debug_path_matches_oracle():
     assert rel_l2(dump, ref_dump, axis=(2, 3, 4)).max() <= F32_TOL
 
 
+# ------------------------------------------------------------------ bf16 path, small shapes and edges
+@pytest.fixture(scope="module")
+def tiny_bf16_runner():
+    r = GpuRunner(synth.TINY, weights("tiny"), dtype="bf16", max_batch=4, max_rows=256)
+    yield r
+    r.close()
+
+
+def test_tiny_bf16_ragged_batch_and_empty_prefixes(tiny_bf16_runner):
+    """head_dim 64 on the tensor-core path: a ragged batch with a masked slot
+    and a long request, then a single Euler step with no valid prefix at all."""
+    w = weights("tiny")
+    wl = synth.build_workload("b3", synth.TINY, 3, [[("v", 30)], [("v", 5), ("m", 3)], [("v", 200)]], seed=4)
+    assert np.abs(tiny_bf16_runner.run(wl) - oracle_actions(wl, w)).max() <= BF16_ACT_TOL
+    wl = synth.build_workload("e", synth.TINY, 1, [[("m", 7)], []], seed=5)
+    got = tiny_bf16_runner.run(wl)
+    assert np.isfinite(got).all()
+    assert np.abs(got - oracle_actions(wl, w)).max() <= BF16_ACT_TOL
+
+
+def test_tiny_bf16_in_place_and_rebind_free(tiny_bf16_runner):
+    wl = synth.tiny_variant("masked")
+    a = tiny_bf16_runner.run(wl)
+    np.testing.assert_array_equal(a, tiny_bf16_runner.run(wl, in_place=True))
+    np.testing.assert_array_equal(a, tiny_bf16_runner.run(wl, rebind=False))
+    np.testing.assert_array_equal(a, tiny_bf16_runner.run(synth.tiny_variant("plain")))
+
+
+def test_pi05_bf16_single_euler_step(pi05_runner):
+    wl = synth.pi05_two_camera(n_steps=1)
+    got = pi05_runner.run(wl)
+    assert np.abs(got - oracle_actions(wl, weights("pi05"))).max() <= BF16_ACT_TOL
+
+
 # ------------------------------------------------------------------ errors through the ABI
 def test_abi_errors_on_gpu(tiny_runner):
     from flow_matching_action_gb300 import ae
