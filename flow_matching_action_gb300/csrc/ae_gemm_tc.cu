@@ -266,6 +266,8 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         }
         __syncwarp();
       } else {  // kEGeglu: one box [TT tokens][64 bf16] of GeGLU outputs n/2
+        // lane 2i holds gate j = 16q + i and lane 2i + 1 its up value; lane 4k
+        // packs outputs 2k and 2k + 1 (from lane 4k + 2) into one 4-byte store
         const int jl = 16 * q + (lane >> 1);
         const uint32_t lo = (uint32_t)((jl & 7) << 1);
         for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
@@ -274,10 +276,12 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            const float r = gelu_tanh(v[j]) * other;  // meaningful on even lanes
+            const float r_next = __shfl_down_sync(0xffffffffu, r, 2);
             const int t = c0 + j;
-            if (!(lane & 1))
-              *reinterpret_cast<bf16*>(stg + t * 128 + (((jl >> 3) ^ (t & 7)) << 4) + lo) =
-                  __float2bfloat16_rn(gelu_tanh(v[j]) * other);
+            if ((lane & 3) == 0)
+              *reinterpret_cast<__nv_bfloat162*>(stg + t * 128 + (((jl >> 3) ^ (t & 7)) << 4) + lo) =
+                  __floats2bfloat162_rn(r, r_next);
           }
         }
         fence_proxy_async_smem();
