@@ -308,18 +308,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const float sl2 = a.scale * 1.4426950408889634f;
     float s[kChunk];
     tmem_ld64(tm_s + lane_off, s);
-    float cmax = -INFINITY;
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
       s[j] *= sl2;
-      if (j < nk) cmax = fmaxf(cmax, s[j]);
+      if (j < nk) mx[j & 3] = fmaxf(mx[j & 3], s[j]);
     }
+    const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
     // raise the exponent reference; O (in TMEM) and l follow it
     float factor = 1.f;
     if (ci == 0) {
       m_ref = cmax;
     } else if (cmax > m_ref + kRescaleMargin * 1.4426950408889634f) {
-      factor = exp2f(m_ref - cmax);
+      factor = ex2_fast(m_ref - cmax);
       m_ref = cmax;
     }
     if (__any_sync(0xffffffffu, factor != 1.f)) {
@@ -334,16 +335,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     uint32_t pk[kChunk / 2];
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains, added in a fixed order
 #pragma unroll
     for (int j = 0; j < kChunk; j += 2) {
-      const float p0 = (j < nk) ? exp2f(s[j] - m_ref) : 0.f;
-      const float p1 = (j + 1 < nk) ? exp2f(s[j + 1] - m_ref) : 0.f;
+      const float p0 = (j < nk) ? ex2_fast(s[j] - m_ref) : 0.f;
+      const float p1 = (j + 1 < nk) ? ex2_fast(s[j + 1] - m_ref) : 0.f;
       const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
       // the row sum uses the bf16-rounded weights, the values P V multiplies
       const float2 pr = __bfloat1622float2(pb);
-      l += pr.x + pr.y;
+      ls[(j >> 1) & 3] += pr.x + pr.y;
       pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
     }
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 #pragma unroll
     for (int cc = 0; cc < 8; ++cc)
       *reinterpret_cast<uint4*>(smem + L.p + sw128_offset(row, cc)) =
@@ -744,12 +747,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_sfree[bf]);  // this warp is done with S buffer bf
-      float lmax = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         sv[j] *= sl2;
-        if (32 * ch + j < nk) lmax = fmaxf(lmax, sv[j]);
+        if (32 * ch + j < nk) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
       }
+      const float lmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       xmax[ch * 128 + row] = lmax;
       pipe_quarter_bar(q4);
       const float cmax = fmaxf(lmax, xmax[(ch ^ 1) * 128 + row]);
@@ -758,7 +762,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       if (c == 0) {
         m_ref = cmax;
       } else if (cmax > m_ref + kRescaleMargin * 1.4426950408889634f) {
-        factor = exp2f(m_ref - cmax);
+        factor = ex2_fast(m_ref - cmax);
         m_ref = cmax;
       }
       // P V(c - 1) must be complete before O is rescaled or P is overwritten
@@ -779,8 +783,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float p0 = (32 * ch + j < nk) ? exp2f(sv[j] - m_ref) : 0.f;
-        const float p1 = (32 * ch + j + 1 < nk) ? exp2f(sv[j + 1] - m_ref) : 0.f;
+        const float p0 = (32 * ch + j < nk) ? ex2_fast(sv[j] - m_ref) : 0.f;
+        const float p1 = (32 * ch + j + 1 < nk) ? ex2_fast(sv[j + 1] - m_ref) : 0.f;
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         // the row sum uses the bf16-rounded weights, the values P V multiplies
         const float2 pr = __bfloat1622float2(pb);
@@ -869,7 +873,7 @@ __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
   float l = 0.f, acc = 0.f;
   for (int sp = 0; sp < n_splits; ++sp) {
     const float2 ml = a.part_ml[(unit0 + sp) * 128 + row];
-    const float w = exp2f(ml.x - m);
+    const float w = ex2_fast(ml.x - m);
     l += ml.y * w;
     acc += a.part_o[((unit0 + sp) * 128 + row) * a.dh + d] * w;
   }

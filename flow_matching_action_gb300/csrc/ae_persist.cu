@@ -713,17 +713,18 @@ __device__ void attn_phase(const PersistParams& P, State& st, const Ctx& c, int 
       tc_fence_after();
       float s[kChunk];
       tmem_ld64(tm_s + lane_off, s);
-      float cmax = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
         s[j] *= sl2;
-        if (j < nk) cmax = fmaxf(cmax, s[j]);
+        if (j < nk) mx[j & 3] = fmaxf(mx[j & 3], s[j]);
       }
+      const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       float factor = 1.f;
       if (ci == 0) {
         m_ref = cmax;
       } else if (cmax > m_ref + kRescaleMargin * kLog2e) {
-        factor = exp2f(m_ref - cmax);
+        factor = ex2_fast(m_ref - cmax);
         m_ref = cmax;
       }
       if (__any_sync(0xffffffffu, factor != 1.f)) {
@@ -740,8 +741,8 @@ __device__ void attn_phase(const PersistParams& P, State& st, const Ctx& c, int 
       uint32_t pk2[kChunk / 2];
 #pragma unroll
       for (int j = 0; j < kChunk; j += 2) {
-        const float p0 = (j < nk) ? exp2f(s[j] - m_ref) : 0.f;
-        const float p1 = (j + 1 < nk) ? exp2f(s[j + 1] - m_ref) : 0.f;
+        const float p0 = (j < nk) ? ex2_fast(s[j] - m_ref) : 0.f;
+        const float p1 = (j + 1 < nk) ? ex2_fast(s[j + 1] - m_ref) : 0.f;
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         const float2 pr = __bfloat1622float2(pb);  // the row sum uses the weights P V multiplies
         l += pr.x + pr.y;
@@ -1046,7 +1047,7 @@ __device__ void combine_phase(const PersistParams& P) {
 #pragma unroll
       for (int j = 0; j < kSp; ++j) {
         if (s0 + j >= n_splits) continue;
-        const float wgt = exp2f(ml[j].x - m);
+        const float wgt = ex2_fast(ml[j].x - m);
         l += ml[j].y * wgt;
         acc.x += ov[j].x * wgt;
         acc.y += ov[j].y * wgt;

@@ -21,6 +21,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// 2^x by the hardware's approximate exponential (relative error ~2^-22,
+// results below the normal range flush to zero): one instruction instead of
+// the accurate library routine, for softmax weights that are then rounded to
+// bf16.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void report(int* status, int code) {
   if (status != nullptr) *(volatile int*)status = code;
 }
