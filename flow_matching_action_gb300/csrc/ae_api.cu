@@ -230,6 +230,15 @@ ae_status get_table(ae_ctx* c, int n_steps, const TimeTable** out) {
   AE_TRY(alloc(c, &t.c, S * D * sizeof(float)));
   ae::launch_time_table(c, t, c->stream);
   AE_CK(c, cudaGetLastError());
+  if (c->fast) {
+    // adaRMS's shift folded into the QKV and gate/up GEMMs: shift W^T per step and layer
+    const int nq = d.qkvdim(), ng = 2 * d.F, nf = nq + ng;
+    AE_TRY(alloc(c, &t.fold, S * L * (size_t)nf * sizeof(float)));
+    AE_CK(c, ae::launch_fold_shift((const ae::bf16*)c->w_qkv, nq, d.D, t.mod, n_steps, d.L, 0, t.fold, nf, 0,
+                                   c->stream));
+    AE_CK(c, ae::launch_fold_shift((const ae::bf16*)c->w_gu, ng, d.D, t.mod, n_steps, d.L, 1, t.fold, nf, nq,
+                                   c->stream));
+  }
   c->tables.push_back(t);
   *out = &c->tables.back();
   return AE_OK;

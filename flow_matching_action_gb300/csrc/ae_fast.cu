@@ -2,15 +2,16 @@
 // the launch sequence of one flow step.
 //
 // One flow step (MolmoBot PR, Part 2: only the action queries and t change
-// between steps; the prefix binding is reused):
-//   in-proj (+ sum of squares) ->
-//   per layer: [adaRMS1 -> merged QKV GEMM -> RoPE] -> attention ->
-//              [O GEMM -> gated residual] -> [adaRMS2 -> merged gate/up GEMM]
-//              -> [GeGLU -> down GEMM -> gated residual] ->
+// between steps; the prefix binding is reused), six kernels per layer:
+//   in-proj (+ sums of squares) ->
+//   per layer: [adaRMS1 folded -> merged QKV GEMM -> RoPE] -> attention ->
+//              chunk combine -> [O GEMM -> gated residual] ->
+//              [adaRMS2 folded -> merged gate/up GEMM -> GeGLU] ->
+//              [down GEMM -> gated residual] ->
 //   final adaRMS + out-proj + Euler update.
-// A GEMM whose output tiles cannot fill the GPU splits K; its fp32 partials
-// are summed in split order (deterministic) by a reduce kernel or by the
-// next GEMM's operand producer.
+// A GEMM whose output tiles cannot fill the GPU splits K over the CTAs of a
+// cluster, which sum their partials in rank order (deterministic) through
+// distributed shared memory inside the same kernel.
 #include <math.h>
 #include <string.h>
 
@@ -145,19 +146,18 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const int nqkv = d.qkvdim(), qd = d.qdim();
   const float eps = (float)d.eps;
   const int sm = c->sm_count;
-  const GemmPlan pq = plan_gemm(nqkv, D, M, sm, 1, c->ks_cap[0]);
-  const GemmPlan po = plan_gemm(D, qd, M, sm, 2, c->ks_cap[1]);
-  const GemmPlan pg = plan_gemm(2 * F, D, M, sm, 1, c->ks_cap[2]);
-  const GemmPlan pd = plan_gemm(D, F, M, sm, 2, c->ks_cap[3]);
+  const GemmPlan pq = plan_gemm_cl(nqkv, D, M, sm, c->ks_cap[0]);
+  const GemmPlan po = plan_gemm_cl(D, qd, M, sm, c->ks_cap[1]);
+  const GemmPlan pg = plan_gemm_cl(2 * F, D, M, sm, c->ks_cap[2]);
+  const GemmPlan pd = plan_gemm_cl(D, F, M, sm, c->ks_cap[3]);
   // the four GEMMs share one token tiling (it depends on M only)
   *err = fast_activation_maps(c, pq.tok_tile);
   if (*err != cudaSuccess) return 0;
-  float* part0 = c->part;
-  float* part1 = c->part + c->part_floats;
   bf16* qkv = (bf16*)c->qkv;
   bf16* o = (bf16*)c->o;
   bf16* m = (bf16*)c->m;
   bf16* y = (bf16*)c->y;
+  const int nf = nqkv + 2 * F;
   int n = 0;
   auto ck = [&](cudaError_t e) {
     if (e != cudaSuccess && *err == cudaSuccess) *err = e;
@@ -168,14 +168,31 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     ck(cudaMemcpyAsync(dst, c->h, (size_t)M * D * sizeof(float), cudaMemcpyDeviceToDevice, s));
   };
   auto mod = [&](int l, int j) { return t.mod + (((size_t)step * L + l) * 2 + j) * 3 * D; };
+  auto fold = [&](int l) { return t.fold + ((size_t)step * L + l) * nf; };
+  // fields shared by every GEMM of the step
+  auto base_args = [&](int w_row0, int w_next_row0) {
+    TcGemmArgs a = {};
+    a.M = M;
+    a.status = c->status_dev;
+    a.w_row0 = w_row0;
+    a.w_next_row0 = w_next_row0;
+    a.ss_in = c->sumsq;
+    a.n_ss = D / 128;
+    a.norm_dim = D;
+    a.eps = eps;
+    a.rope_cs = c->rope_cs;
+    a.dh = d.dh;
+    a.n_rot_heads = d.Hq + d.Hkv;
+    return a;
+  };
 
-  // h = x W_in^T + b_in; y = adaRMS1 of layer 0
+  // h = x W_in^T + b_in; operand of layer 0's QKV GEMM
   // The first kernel of a sample is a full dependency of whatever precedes it
   // on the stream (the bind kernel among them); every later kernel is chained
   // to its predecessor, so all of them start after the bind has completed and
   // may read its tables before griddepcontrol.wait.
-  ck(launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0),
-                        mod(0, 0) + D, eps, y, s, pdl && step > 0));
+  ck(launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0), y,
+                        c->sumsq, s, pdl && step > 0));
   ++n;
   for (int l = 0; l < L; ++l) {
     dump(l);
@@ -183,29 +200,13 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     const float* mod2 = mod(l, 1);
     const int ln = (l + 1) % L;  // whose weights each GEMM pulls into L2 ahead of use
 
-    // merged QKV (+ RoPE)
-    TcGemmArgs a = {};
-    a.M = M;
-    a.status = c->status_dev;
-    a.w_row0 = l * nqkv;
-    a.w_next_row0 = ln * nqkv;
-    a.rope_cs = c->rope_cs;
-    a.dh = d.dh;
-    a.n_rot_heads = d.Hq + d.Hkv;
-    a.out_rows = c->max_batch * d.H;
-    if (pq.ksplit == 1) {
-      a.e_mode = kEQkvRope;
-      a.out_bf16 = qkv;
-    } else {
-      a.e_mode = kEPartial;
-      a.part = part0;
-    }
+    // adaRMS1 (folded) -> merged QKV -> RoPE
+    TcGemmArgs a = base_args(l * nqkv, ln * nqkv);
+    a.e_mode = kEQkvRope;
+    a.fold = fold(l);
+    a.out_bf16 = qkv;
     ck(launch_tc_gemm(c->map_qkv, c->map_y, pq, a, s, pdl));
     ++n;
-    if (pq.ksplit > 1) {
-      ck(launch_reduce_qkv(part0, pq.ksplit, M, nqkv, d.dh, d.Hq + d.Hkv, c->rope_cs, qkv, s, pdl));
-      ++n;
-    }
 
     // attention over [valid prefix || actions]
     {
@@ -237,52 +238,35 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       n += 2;
     }
 
-    // O projection -> gated residual -> adaRMS2
-    a = TcGemmArgs{};
-    a.M = M;
-    a.status = c->status_dev;
-    a.w_row0 = l * D;
-    a.w_next_row0 = ln * D;
-    a.e_mode = kEPartial;
-    a.part = part0;
+    // O projection -> gated residual -> operand of the gate/up GEMM (adaRMS2)
+    a = base_args(l * D, ln * D);
+    a.e_mode = kEResid;
+    a.h = c->h;
+    a.gate = mod1 + 2 * D;
+    a.scale_next = mod2;
+    a.a_out = y;
+    a.ss_out = c->sumsq;
     ck(launch_tc_gemm(c->map_o, c->map_oact, po, a, s, pdl));
-    ck(launch_resid_norm(part0, po.ksplit, M, D, c->h, mod1 + 2 * D, mod2, mod2 + D, eps, y, s, pdl));
-    n += 2;
+    ++n;
 
-    // merged gate/up -> GeGLU
-    a = TcGemmArgs{};
-    a.M = M;
-    a.status = c->status_dev;
-    a.w_row0 = l * 2 * F;
-    a.w_next_row0 = ln * 2 * F;
-    a.out_rows = c->max_batch * d.H;
-    if (pg.ksplit == 1) {
-      a.e_mode = kEGeglu;
-      a.out_bf16 = m;
-    } else {
-      a.e_mode = kEPartial;
-      a.part = part0;
-    }
+    // adaRMS2 (folded) -> merged gate/up -> GeGLU
+    a = base_args(l * 2 * F, ln * 2 * F);
+    a.e_mode = kEGeglu;
+    a.fold = fold(l) + nqkv;
+    a.out_bf16 = m;
     ck(launch_tc_gemm(c->map_gu, c->map_y, pg, a, s, pdl));
     ++n;
-    if (pg.ksplit > 1) {
-      ck(launch_geglu_reduce(part0, pg.ksplit, M, F, m, s, pdl));
-      ++n;
-    }
 
-    // down projection -> gated residual -> adaRMS1 of the next layer
-    a = TcGemmArgs{};
-    a.M = M;
-    a.status = c->status_dev;
-    a.w_row0 = l * D;
-    a.w_next_row0 = ln * D;
-    a.e_mode = kEPartial;
-    a.part = part1;
+    // down projection -> gated residual -> operand of the next layer's QKV GEMM
+    a = base_args(l * D, ln * D);
+    a.e_mode = kEResid;
+    a.h = c->h;
+    a.gate = mod2 + 2 * D;
+    a.scale_next = l + 1 < L ? mod(l + 1, 0) : nullptr;
+    a.a_out = y;
+    a.ss_out = c->sumsq;
     ck(launch_tc_gemm(c->map_d, c->map_mact, pd, a, s, pdl));
-    const float* nxt = l + 1 < L ? mod(l + 1, 0) : nullptr;
-    ck(launch_resid_norm(part1, pd.ksplit, M, D, c->h, mod2 + 2 * D, nxt, nxt ? nxt + D : nullptr,
-                         eps, y, s, pdl));
-    n += 2;
+    ++n;
   }
   dump(L);
   ck(launch_final_bf16(c, t, step, x, s, pdl));

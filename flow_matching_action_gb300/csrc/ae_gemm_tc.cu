@@ -1,4 +1,5 @@
-// tcgen05 GEMMs of the bf16 path and the elementwise kernels between them.
+// tcgen05 GEMMs of the bf16 path, with the rest of the layer fused into their
+// epilogues.
 //
 // Swap-AB: a CTA computes a 128-row slab of a weight matrix against a tile of
 // up to 256 action tokens, D[n, t] = sum_k W[n, k] X[t, k].  The weight rows
@@ -9,15 +10,32 @@
 // fp32 accumulator lives in TMEM.
 // Merged Q/K/V and gate/up weights follow sglang PR #34599, item 1.
 //
-// Epilogues:
-//   kEQkvRope   RoPE (rotate_half pairs) on q and k, bf16 q|k|v store
-//   kEGeglu     gelu_tanh(g) * u of the interleaved gate/up rows, bf16 store
-//   kEPartial   fp32 split-K partials, summed in split order later
-// The kernels after the GEMMs fuse the rest of the layer (LoongForge Pi0.5
-// blog, section 2): split-K sum + gated residual + the NEXT adaRMS (rms over
-// the row, (1 + scale), + shift) into the bf16 operand of the next GEMM.
+// Split K without a reduce kernel: the K splits of one output tile are the
+// CTAs of one thread-block cluster.  Each stages its fp32 partial tile in its
+// own shared memory; after a cluster barrier every CTA sums a slice of the
+// tile's tokens over all the cluster's partials (distributed shared memory,
+// in rank order, so the result does not depend on timing) and runs the
+// epilogue on it:
+//   kEQkvRope   adaRMS folded in (below), RoPE (rotate_half pairs) on q and k,
+//               bf16 q|k|v store
+//   kEGeglu     adaRMS folded in, gelu_tanh(g) * u of the interleaved gate/up
+//               rows, bf16 store
+//   kEResid     gated residual h += gate * acc (LoongForge Pi0.5 blog,
+//               section 2), then the next GEMM's operand bf16(h * (1 + scale))
+//               and the tile's share of sum(h^2) per token
+// adaRMS folded into the consumer: with y = h r (1 + scale) + shift and r the
+// per-token reciprocal RMS, y W^T = r * ((h * (1 + scale)) W^T) + shift W^T.
+// The producer of h writes h * (1 + scale) and per-128-feature sums of h^2;
+// the consumer's epilogue forms r from those sums, scales its accumulator by
+// r and adds the per-feature constant shift W^T, which the time table holds
+// for every (flow step, layer).  No kernel waits for a whole-row norm.
 #include <math.h>
 #include <string.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <type_traits>
 
 #include "ae_internal.h"
 #include "ae_tc.cuh"
@@ -29,10 +47,10 @@ using namespace tc;
 
 // Warp 0 issues TMA, warp 1 MMA, warps 2.. run the epilogue: EW = 4 (one per
 // TMEM lane quarter) for token tiles up to 64, EW = 8 (two per quarter, each
-// taking half of the token columns) for longer tiles, whose epilogue would
-// otherwise be a long serial chain per thread.
+// taking half of the token columns) for longer tiles.
 constexpr int kThreadsFor(int ew) { return 64 + 32 * ew; }
 constexpr int kATileBytes = 128 * 128;  // 128 weight rows x 64 bf16
+constexpr int kMaxCluster = 16;
 
 // gelu_tanh(g) = 0.5 g (1 + tanh(u)), u = sqrt(2/pi) (g + 0.044715 g^3), written
 // with 1 + tanh(u) = 2 / (1 + e^{-2u}): one exponential and one division.
@@ -54,44 +72,241 @@ __device__ __forceinline__ void named_bar(int n) {
   asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ void quarter_bar(int q) {  // the two epilogue warps of lane quarter q
-  switch (q) {
-    case 0: named_bar<2>(64); break;
-    case 1: named_bar<3>(64); break;
-    case 2: named_bar<4>(64); break;
-    default: named_bar<5>(64); break;
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits; shared-memory
+// writes before it are visible to the whole cluster after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a0, float a1, float a2, float a3) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a0), "f"(a1), "f"(a2),
+               "f"(a3));
+}
+
+// Split-K receive buffer: for each of ks source ranks, 128 feature rows of
+// `pad` floats (this rank's tokens, padded to an odd multiple of 4 so that
+// 16-byte accesses of consecutive feature rows hit distinct bank groups).
+__host__ __device__ inline int recv_pad(int n_tok, int ks) {
+  const int g = ((n_tok + 3) / 4 + ks - 1) / ks;  // 4-token groups per rank
+  return 4 * (g | 1);
+}
+
+__host__ __device__ inline uint32_t recv_bytes(int tt, int ks) {
+  return ks > 1 ? (uint32_t)ks * 128u * (uint32_t)recv_pad(tt, ks) * 4u : 0u;
+}
+
+// Shared-memory layout of k_tc_gemm, byte offsets from the 1024-aligned base:
+// pipeline stages (weights, token tiles), the split-K receive buffer, mbarriers
+// and flags, the owner of each 4-token group, the per-token reciprocal RMS of
+// the emitted tokens and the per-quarter sums of squares.
+struct GemmSmem {
+  uint32_t a, b, recv, bars, own, rn, red, total;
+};
+
+__host__ __device__ inline GemmSmem gemm_smem_layout(int stages, int tt, int ks) {
+  GemmSmem L;
+  L.a = 0;
+  L.b = (uint32_t)stages * kATileBytes;
+  L.recv = L.b + (uint32_t)(stages * tt * 128);
+  L.bars = L.recv + recv_bytes(tt, ks);
+  L.own = L.bars + (uint32_t)(2 * stages + 1) * 8u + 64u;  // + TMEM base, abort flag, votes[8]
+  L.rn = L.own + 64u * 4u;
+  L.red = L.rn + (256u + 16u) * 4u;
+  L.total = L.red + 4u * 256u * 4u;
+  return L;
+}
+
+// What the epilogue needs, copied out of the kernel arguments into registers.
+struct Epi {
+  int mode, M, N, n_ss, norm_dim, dh, half, n_rot_heads, TT;
+  float eps;
+  const float* ss_in;
+  const float* fold;
+  bf16* out;
+  const float2* rope_cs;
+  float* h;
+  const float* gate;
+  const float* scale_next;
+  bf16* a_out;
+  float* red;      // shared [4][TT]
+  const float* rn; // shared, per emitted token
+};
+
+// Per-token inputs of one 16-token chunk that the epilogue of MODE reads from
+// global memory (RoPE (cos, sin) of the thread's pair, or the residual h),
+// loaded one chunk ahead of use.
+template <int MODE>
+__device__ __forceinline__ void pre16(const Epi& E, int n, int tok0, int cnt, float2 (&aux)[16]) {
+  if (MODE == kEQkvRope) {
+    const int hb = n / E.dh, pair = (n - hb * E.dh) >> 1;
+    const bool rot = hb < E.n_rot_heads;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      aux[j] = (rot && j < cnt) ? __ldg(E.rope_cs + (size_t)(tok0 + j) * E.half + pair) : make_float2(1.f, 0.f);
+  } else if (MODE == kEResid) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) aux[j].x = j < cnt ? E.h[(size_t)(tok0 + j) * E.N + n] : 0.f;
+  }
+}
+
+// Epilogue of up to 16 consecutive emitted tokens of feature row n (token
+// tok0.., index i0.. among this CTA's emitted tokens), values v = sums over K,
+// aux = pre16 of the chunk.  All lanes of the warp call it with the same i0,
+// tok0 and cnt (shuffles inside); every load precedes every store.
+template <int MODE>
+__device__ __forceinline__ void emit16(const Epi& E, int n, int q, int lane, int i0, int tok0,
+                                       const float (&v)[16], int cnt, float cf, float gt, float sc,
+                                       const float2 (&aux)[16]) {
+  if (MODE == kEResid) {
+    float hn[16], sq[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      hn[j] = aux[j].x + gt * v[j];
+      sq[j] = j < cnt ? hn[j] * hn[j] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < cnt) {
+        E.h[(size_t)(tok0 + j) * E.N + n] = hn[j];
+        if (E.scale_next != nullptr) E.a_out[(size_t)(tok0 + j) * E.N + n] = __float2bfloat16_rn(hn[j] * (1.f + sc));
+      }
+    // sum of sq over the warp for each of the 16 tokens by a transposed
+    // butterfly: after the step with mask m, lanes with bit m clear keep the
+    // lower half of their vector; lane l ends with token 8b4 + 4b3 + 2b2 + b1
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const bool up = lane & 16;
+      const float send = up ? sq[k] : sq[8 + k];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+      sq[k] = (up ? sq[8 + k] : sq[k]) + got;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool up = lane & 8;
+      const float send = up ? sq[k] : sq[4 + k];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 8);
+      sq[k] = (up ? sq[4 + k] : sq[k]) + got;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const bool up = lane & 4;
+      const float send = up ? sq[k] : sq[2 + k];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 4);
+      sq[k] = (up ? sq[2 + k] : sq[k]) + got;
+    }
+    {
+      const bool up = lane & 2;
+      const float send = up ? sq[0] : sq[1];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 2);
+      sq[0] = (up ? sq[1] : sq[0]) + got;
+    }
+    const float tot = sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
+    const int t = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+    if (!(lane & 1) && t < cnt) E.red[q * E.TT + i0 + t] = tot;
+  } else if (MODE == kEGeglu) {
+    // lane 2i holds gate row i, lane 2i + 1 its up row, for 16 tokens; the
+    // pair splits the tokens: the even lane takes tokens 0..7, the odd one 8..15
+    float x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = E.rn[i0 + j];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = x[j] * v[j] + cf;
+    const bool odd = lane & 1;
+    float r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float got = __shfl_xor_sync(0xffffffffu, odd ? x[k] : x[8 + k], 1);
+      const float g = odd ? got : x[k], u = odd ? x[8 + k] : got;
+      r[k] = gelu_tanh(g) * u;
+    }
+    bf16* ocol = E.out + (n >> 1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int j = odd ? 8 + k : k;
+      if (j < cnt) ocol[(size_t)(tok0 + j) * (E.N >> 1)] = __float2bfloat16_rn(r[k]);
+    }
+  } else {  // kEQkvRope: packed rows 2j, 2j + 1 of a head are its dims j, j + dh/2
+    const int hb = n / E.dh, p = n - hb * E.dh;
+    const int pair = p >> 1, odd = p & 1;
+    const bool rot = hb < E.n_rot_heads;
+    float x[16], o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = E.rn[i0 + j];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = x[j] * v[j] + cf;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[j], 1);
+      o[j] = x[j];
+      if (rot) o[j] = odd ? (x[j] * aux[j].x + other * aux[j].y) : (x[j] * aux[j].x - other * aux[j].y);
+    }
+    bf16* ocol = E.out + hb * E.dh + pair + odd * E.half;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < cnt) ocol[(size_t)(tok0 + j) * E.N] = __float2bfloat16_rn(o[j]);
   }
 }
 
 template <int EW>
 __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
-              const __grid_constant__ CUtensorMap omap, const __grid_constant__ TcGemmArgs a) {
+              const __grid_constant__ TcGemmArgs a) {
   constexpr int kEpiWarps = EW;
   constexpr int kEpiThreads = 32 * EW;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = a.stages;
-  const int btile = a.tok_tile * 128;
-  uint8_t* smA = smem;
-  uint8_t* smB = smA + (size_t)S * kATileBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smB + (size_t)S * btile);
+  const int TT = a.tok_tile;
+  const int btile = TT * 128;
+  const int ksn = a.ksplit;
+  const GemmSmem L = gemm_smem_layout(S, TT, ksn);
+  uint8_t* smA = smem + L.a;
+  uint8_t* smB = smem + L.b;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
   uint64_t* tmem_full = empty + S;
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(tmem_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
   volatile int* votes = reinterpret_cast<volatile int*>(tmem_base_p + 2);  // [kEpiWarps]
+  int* own_s = reinterpret_cast<int*>(smem + L.own);                        // [64]
+  float* rn_s = reinterpret_cast<float*>(smem + L.rn);                      // [<= 256 + 16]
+  float* red_s = reinterpret_cast<float*>(smem + L.red);                    // [4][TT]
+  const float* recv = reinterpret_cast<const float*>(smem + L.recv);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int idx = blockIdx.x;
+  // the K splits of one output tile are consecutive CTAs forming one cluster
+  const int ks = ksn > 1 ? (int)cluster_rank() : 0;
+  const int idx = blockIdx.x / ksn;
   const int n_tile = idx % a.n_tiles;
-  idx /= a.n_tiles;
-  const int tt = idx % a.tok_tiles;
-  const int ks = idx / a.tok_tiles;
-  const int kb_begin = (int)((long)ks * a.kb_total / a.ksplit);
-  const int kb_end = (int)((long)(ks + 1) * a.kb_total / a.ksplit);
+  const int tt = idx / a.n_tiles;
+  const int kb_begin = (int)((long)ks * a.kb_total / ksn);
+  const int kb_end = (int)((long)(ks + 1) * a.kb_total / ksn);
   const int n_it = kb_end - kb_begin;
-  const int t0 = tt * a.tok_tile;
+  const int t0 = tt * TT;
+  const int nv = min(TT, a.M - t0);  // valid tokens of the tile
+  // Tokens this CTA emits: the whole tile when unsplit, else its rank's run
+  // of 4-token groups.
+  const int ng = (nv + 3) >> 2;
+  const int e_lo = 4 * (ks * ng / ksn);
+  const int e_hi = min(4 * ((ks + 1) * ng / ksn), nv);
+  const int pad = recv_pad(nv, ksn);
   auto kcol = [&](int it) { return (kb_begin + it) * 64; };
   pdl_trigger();
 
@@ -113,6 +328,45 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_d = *tmem_base_p;
+  bool go = false;
+  // epilogue role (warps 2..): TMEM lane quarter, column half, feature row
+  const int q = warp & 3;
+  const int hf = (warp - 2) >> 2;
+  const int f = 32 * q + lane;
+  const int n = n_tile * 128 + f;
+  Epi E;
+  E.mode = a.e_mode;
+  E.M = a.M;
+  E.N = a.N;
+  E.n_ss = a.n_ss;
+  E.norm_dim = a.norm_dim;
+  E.dh = a.dh;
+  E.half = a.dh >> 1;
+  E.n_rot_heads = a.n_rot_heads;
+  E.TT = TT;
+  E.eps = a.eps;
+  E.ss_in = a.ss_in;
+  E.fold = a.fold;
+  E.out = a.out_bf16;
+  E.rope_cs = a.rope_cs;
+  E.h = a.h;
+  E.gate = a.gate;
+  E.scale_next = a.scale_next;
+  E.a_out = a.a_out;
+  E.red = red_s;
+  E.rn = rn_s;
+  float* const ss_out = a.ss_out;
+  int* const status = a.status;
+  float cf = 0.f, gt = 0.f, sc = 0.f;
+  float2 aux[16];  // per-token inputs of the next chunk (epilogue warps)
+  // token columns this warp reads from TMEM (unsplit: also the ones it emits)
+  const int c_lo = hf ? a.tok_half : 0;
+  const int c_hi = min((hf || EW == 4) ? TT : a.tok_half, nv);
+  // split K: tokens of this rank's run that this warp emits after the reduction
+  const int ns = e_hi - e_lo;
+  const int p_mid = EW == 8 ? 4 * ((ns + 7) / 8) : ns;
+  const int p_lo = hf ? p_mid : 0, p_hi = hf ? ns : p_mid;
+  const uint32_t trow = (uint32_t)(32 * q) << 16;
 
   if (warp == 0) {
     // ---------------- TMA producer: weight slab + token tile per 64-wide K block
@@ -155,7 +409,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, a.tok_tile);
+      const uint32_t idesc = idesc_bf16(128, TT);
       for (int it = 0; it < n_it; ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
@@ -171,175 +425,130 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       mma_commit(tmem_full);
     }
   } else {
-    // ---------------- epilogue: warps 2..9, two per TMEM lane quarter (warp w
-    // reads lanes 32 (w % 4)..), splitting the token columns in two halves
-    const int q = warp & 3;
-    const int e = warp - 2;       // 0..7
-    const int hf = e >> 2;        // which half of the token columns (EW == 8)
-    const int TT = a.tok_tile;
-    const int c_lo = hf ? a.tok_half : 0, c_hi = (hf || EW == 4) ? TT : a.tok_half;
-    const int n = n_tile * 128 + 32 * q + lane;
-    // every epilogue warp takes the same decision
-    if (lane == 0) votes[e] = (mbar_wait(tmem_full, 0, abort_flag, a.status) && !*abort_flag) ? 1 : 0;
+    // ---------------- epilogue warps 2..: warp w reads TMEM lanes 32 (w % 4)..
+    // (feature rows f); with EW == 8 the two warps of a lane quarter take the
+    // two halves of the token columns.
+    const int e = warp - 2;
+    const int et = threadIdx.x - 64;
+    // per-feature constants come from the time table (ready before this kernel)
+    if (E.mode == kEResid) {
+      gt = E.gate[n];
+      if (E.scale_next != nullptr) sc = E.scale_next[n];
+    } else {
+      cf = E.fold[n];
+    }
+    // owner rank and local group of every 4-token group of the tile
+    if (ksn > 1)
+      for (int g = et; g < ng; g += kEpiThreads) {
+        const int r = ((g + 1) * ksn - 1) / ng;  // r * ng / ks <= g < (r + 1) * ng / ks
+        own_s[g] = (r << 16) | (g - r * ng / ksn);
+      }
+    pdl_wait();
+    // reciprocal RMS of the emitted tokens, while the mainloop runs
+    if (E.mode != kEResid)
+      for (int i = et; i < e_hi - e_lo; i += kEpiThreads) {
+        const int tok = t0 + e_lo + i;
+        float ss = 0.f;
+        for (int j = 0; j < E.n_ss; ++j) ss += E.ss_in[(size_t)j * E.M + tok];
+        rn_s[i] = 1.0f / sqrtf(ss / (float)E.norm_dim + E.eps);
+      }
+    // the first chunk's per-token inputs, issued before the accumulator is ready
+    if (ksn == 1) {
+      if (c_lo < c_hi) {
+        if (E.mode == kEQkvRope) pre16<kEQkvRope>(E, n, t0 + c_lo, min(16, c_hi - c_lo), aux);
+        else if (E.mode == kEResid) pre16<kEResid>(E, n, t0 + c_lo, min(16, c_hi - c_lo), aux);
+      }
+    } else if (p_lo < p_hi) {
+      if (E.mode == kEQkvRope) pre16<kEQkvRope>(E, n, t0 + e_lo + p_lo, min(16, p_hi - p_lo), aux);
+      else if (E.mode == kEResid) pre16<kEResid>(E, n, t0 + e_lo + p_lo, min(16, p_hi - p_lo), aux);
+    }
+    if (lane == 0) votes[e] = (mbar_wait(tmem_full, 0, abort_flag, status) && !*abort_flag) ? 1 : 0;
     named_bar<1>(kEpiThreads);
-    bool go = true;
+    go = true;
 #pragma unroll
     for (int i = 0; i < kEpiWarps; ++i) go = go && votes[i];
-    pdl_wait();
-    if (go && a.tma_out) {
-      // TMEM -> 128-byte-swizzled staging in the drained pipeline buffers -> TMA stores
+    if (go) {
       tc_fence_after();
-      uint8_t* stg = smem;
-      const uint32_t trow = (uint32_t)(32 * q) << 16;
-      if (a.e_mode == kEPartial) {
-        // lane quarter q owns one box: [TT tokens][32 fp32] of output features 32q..32q+31
-        uint8_t* box = stg + (size_t)q * TT * 128;
-        const uint32_t lo = (uint32_t)((lane & 3) << 2);
+      if (ksn == 1) {
+        // unsplit: the accumulator is the sum; emit straight from TMEM
+        auto run = [&](auto mode_tag) {
+          constexpr int MODE = decltype(mode_tag)::value;
+          for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+            float2 cur[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) cur[j] = aux[j];
+            if (c0 + 16 < c_hi) pre16<MODE>(E, n, t0 + c0 + 16, min(16, c_hi - c0 - 16), aux);
+            float v[16];
+            tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+            emit16<MODE>(E, n, q, lane, c0, t0 + c0, v, min(16, c_hi - c0), cf, gt, sc, cur);
+          }
+        };
+        if (E.mode == kEQkvRope) run(std::integral_constant<int, kEQkvRope>());
+        else if (E.mode == kEGeglu) run(std::integral_constant<int, kEGeglu>());
+        else run(std::integral_constant<int, kEResid>());
+      } else {
+        // split K: push this partial to each 4-token group's owner in the
+        // cluster, recv[this rank][feature][token], 16 bytes per store; a
+        // remote store needs no round trip
+        const uint32_t recv_u = smem_u32(smem + L.recv) + (uint32_t)((ks * 128 + f) * pad) * 4u;
         for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
           float v[16];
           tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = c0 + j;
-            *reinterpret_cast<float*>(box + t * 128 + ((((lane >> 2) ^ (t & 7))) << 4) + lo) = v[j];
-          }
-        }
-        fence_proxy_async_smem();
-        if (EW == 8) quarter_bar(q);  // both halves of the box are staged
-        if (hf == 0 && lane == 0) {
-          tma_store_3d(&omap, box, n_tile * 128 + 32 * q, t0, ks);
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-        __syncwarp();
-      } else if (a.e_mode == kEQkvRope) {
-        // two boxes [TT tokens][64 bf16]: first and second members of the tile's 64 pairs
-        const int half = a.dh >> 1;
-        const int n0 = n_tile * 128;
-        const int hb = n0 / a.dh;
-        const int pair0 = (n0 - hb * a.dh) >> 1;
-        const int p = n - hb * a.dh;
-        const int pair = p >> 1, odd = p & 1;
-        const int pl = pair - pair0;
-        const bool rot = hb < a.n_rot_heads;
-        uint8_t* box = stg + (size_t)odd * TT * 128;
-        const uint32_t lo = (uint32_t)((pl & 7) << 1);
-        float2 csn[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = t0 + c_lo + j;
-          csn[j] = (rot && t < a.M) ? __ldg(a.rope_cs + (size_t)t * half + pair) : make_float2(1.f, 0.f);
-        }
-        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-          float2 csv[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) csv[j] = csn[j];
-          if (c0 + 16 < c_hi) {  // table values of the next 16 tokens, loaded one step ahead
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int t = t0 + c0 + 16 + j;
-              csn[j] = (rot && t < a.M) ? __ldg(a.rope_cs + (size_t)t * half + pair) : make_float2(1.f, 0.f);
+          for (int i = 0; i < 4; ++i) {
+            const int g = (c0 >> 2) + i;
+            if (4 * g < c_hi) {
+              const int o = own_s[g];
+              st_cluster_v4(mapa(recv_u + (uint32_t)(o & 0xffff) * 16u, (uint32_t)(o >> 16)), v[4 * i],
+                            v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             }
-          }
-          float v[16];
-          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-            const int t = c0 + j;
-            float outv = v[j];
-            if (rot) {
-              const float x1 = odd ? other : v[j], x2 = odd ? v[j] : other;
-              outv = odd ? (x2 * csv[j].x + x1 * csv[j].y) : (x1 * csv[j].x - x2 * csv[j].y);
-            }
-            *reinterpret_cast<bf16*>(box + t * 128 + (((pl >> 3) ^ (t & 7)) << 4) + lo) =
-                __float2bfloat16_rn(outv);
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar<1>(kEpiThreads);
-        if (threadIdx.x == 64) {
-          tma_store_2d(&omap, stg, hb * a.dh + pair0, t0);
-          tma_store_2d(&omap, stg + (size_t)TT * 128, hb * a.dh + half + pair0, t0);
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-        __syncwarp();
-      } else {  // kEGeglu: one box [TT tokens][64 bf16] of GeGLU outputs n/2
-        // lane 2i holds gate j = 16q + i and lane 2i + 1 its up value; lane 4k
-        // packs outputs 2k and 2k + 1 (from lane 4k + 2) into one 4-byte store
-        const int jl = 16 * q + (lane >> 1);
-        const uint32_t lo = (uint32_t)((jl & 7) << 1);
-        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-          float v[16];
-          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-            const float r = gelu_tanh(v[j]) * other;  // meaningful on even lanes
-            const float r_next = __shfl_down_sync(0xffffffffu, r, 2);
-            const int t = c0 + j;
-            if ((lane & 3) == 0)
-              *reinterpret_cast<__nv_bfloat162*>(stg + t * 128 + (((jl >> 3) ^ (t & 7)) << 4) + lo) =
-                  __floats2bfloat162_rn(r, r_next);
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar<1>(kEpiThreads);
-        if (threadIdx.x == 64) {
-          tma_store_2d(&omap, stg, n_tile * 64, t0);
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-        __syncwarp();
-      }
-    } else if (go) {
-      tc_fence_after();
-      for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-        if (a.e_mode == kEPartial) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = t0 + c0 + j;
-            if (t < a.M) a.part[((size_t)ks * a.M + t) * a.N + n] = v[j];
-          }
-        } else if (a.e_mode == kEQkvRope) {
-          const int half = a.dh >> 1;
-          const int hb = n / a.dh, p = n - hb * a.dh;
-          const int pair = p >> 1, odd = p & 1;
-          const bool rot = hb < a.n_rot_heads;
-          float2 csv[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = t0 + c0 + j;
-            csv[j] = (rot && t < a.M) ? __ldg(a.rope_cs + (size_t)t * half + pair) : make_float2(1.f, 0.f);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-            const int t = t0 + c0 + j;
-            if (t < a.M) {
-              float outv = v[j];
-              if (rot) {
-                const float2 cs = csv[j];
-                const float x1 = odd ? other : v[j], x2 = odd ? v[j] : other;
-                outv = odd ? (x2 * cs.x + x1 * cs.y) : (x1 * cs.x - x2 * cs.y);
-              }
-              a.out_bf16[(size_t)t * a.N + hb * a.dh + pair + odd * half] = __float2bfloat16_rn(outv);
-            }
-          }
-        } else {  // kEGeglu
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-            const int t = t0 + c0 + j;
-            if (t < a.M && !(n & 1))
-              a.out_bf16[(size_t)t * (a.N >> 1) + (n >> 1)] = __float2bfloat16_rn(gelu_tanh(v[j]) * other);
           }
         }
       }
     }
+  }
+  __syncwarp();
+  if (ksn > 1) {
+    cluster_sync();  // every partial has landed in its owner
+    if (warp >= 2 && go) {
+      // sum this rank's tokens over the cluster's partials in rank order, emit them
+      auto run = [&](auto mode_tag) {
+        constexpr int MODE = decltype(mode_tag)::value;
+        for (int c0 = p_lo; c0 < p_hi; c0 += 16) {
+          float2 cur[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cur[j] = aux[j];
+          if (c0 + 16 < p_hi) pre16<MODE>(E, n, t0 + e_lo + c0 + 16, min(16, p_hi - c0 - 16), aux);
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          for (int src = 0; src < ksn; ++src) {
+            const float* rp = recv + (size_t)(src * 128 + f) * pad + c0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (c0 + 4 * i < p_hi) {
+                const float4 x = *reinterpret_cast<const float4*>(rp + 4 * i);
+                v[4 * i] += x.x;
+                v[4 * i + 1] += x.y;
+                v[4 * i + 2] += x.z;
+                v[4 * i + 3] += x.w;
+              }
+          }
+          emit16<MODE>(E, n, q, lane, c0, t0 + e_lo + c0, v, min(16, p_hi - c0), cf, gt, sc, cur);
+        }
+      };
+      if (E.mode == kEQkvRope) run(std::integral_constant<int, kEQkvRope>());
+      else if (E.mode == kEGeglu) run(std::integral_constant<int, kEGeglu>());
+      else run(std::integral_constant<int, kEResid>());
+    }
+  }
+  if (E.mode == kEResid && warp >= 2) {
+    // per-token sum of h^2 over the tile's 128 features (four lane quarters, in order)
+    named_bar<2>(kEpiThreads);
+    if (go && ss_out != nullptr)
+      for (int i = threadIdx.x - 64; i < e_hi - e_lo; i += kEpiThreads)
+        ss_out[(size_t)n_tile * E.M + t0 + e_lo + i] =
+            (red_s[i] + red_s[TT + i]) + (red_s[2 * TT + i] + red_s[3 * TT + i]);
   }
   tc_fence_before();
   __syncthreads();
@@ -352,113 +561,6 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   }
 }
 
-// ---------------------------------------------------------------- between the GEMMs
-// Sum the split-K partials of the merged QKV projection in split order, apply
-// RoPE to q and k, store q|k|v in natural head layout.  One thread per rotation pair.
-__global__ void k_reduce_qkv(const float* __restrict__ part, int ks_n, int M, int N, int dh,
-                             int n_rot_heads, const float2* __restrict__ cs, bf16* __restrict__ out) {
-  pdl_trigger();
-  pdl_wait();
-  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int np = N >> 1;
-  if (idx >= (long)M * np) return;
-  const int t = (int)(idx / np), pp = (int)(idx - (long)t * np);
-  const int n = 2 * pp;
-  float x1 = 0.f, x2 = 0.f;
-  for (int j0 = 0; j0 < ks_n; j0 += 8) {  // eight splits in flight, summed in split order
-    float2 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      v[j] = j0 + j < ks_n ? __ldcg(reinterpret_cast<const float2*>(part + ((size_t)(j0 + j) * M + t) * N + n))
-                           : make_float2(0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j0 + j < ks_n) {
-        x1 += v[j].x;
-        x2 += v[j].y;
-      }
-  }
-  const int half = dh >> 1;
-  const int hb = n / dh, pair = (n - hb * dh) >> 1;
-  float o1 = x1, o2 = x2;
-  if (hb < n_rot_heads) {
-    const float2 c = cs[(size_t)t * half + pair];
-    o1 = x1 * c.x - x2 * c.y;
-    o2 = x2 * c.x + x1 * c.y;
-  }
-  out[(size_t)t * N + hb * dh + pair] = __float2bfloat16_rn(o1);
-  out[(size_t)t * N + hb * dh + pair + half] = __float2bfloat16_rn(o2);
-}
-
-constexpr int kRowThreads = 256;
-
-template <int NT>
-__device__ float block_sum(float v, float* red) {
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) t += red[w];
-  return t;
-}
-
-// One token row: h += gate * (sum of the split-K partials, in split order);
-// then, if `scale` is given, y = adaRMS(h) with the next sublayer's
-// (scale, shift) as the bf16 operand of the next GEMM.  A thread owns COLS
-// columns and issues the loads of SB splits of all of them before it adds
-// (a row costs about ceil(ks / SB) L2 round trips).
-template <int NT, int COLS, int SB>
-__global__ void __launch_bounds__(NT) k_resid_norm(const float* __restrict__ part, int ks_n, int M, int D,
-                                                   float* __restrict__ h, const float* __restrict__ gate,
-                                                   const float* __restrict__ scale,
-                                                   const float* __restrict__ shift, float eps,
-                                                   bf16* __restrict__ y) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float red[NT / 32];
-  const int t = blockIdx.x;
-  float* hr = h + (size_t)t * D;
-  const size_t stride = (size_t)M * D;
-  float ss = 0.f;
-  for (int n0 = threadIdx.x; n0 < D; n0 += NT * COLS) {
-    float acc[COLS];
-    bool in[COLS];
-#pragma unroll
-    for (int e = 0; e < COLS; ++e) {
-      acc[e] = 0.f;
-      in[e] = n0 + e * NT < D;
-    }
-    const float* pp = part + (size_t)t * D + n0;
-    for (int j0 = 0; j0 < ks_n; j0 += SB) {
-      float v[SB][COLS];
-#pragma unroll
-      for (int j = 0; j < SB; ++j)
-#pragma unroll
-        for (int e = 0; e < COLS; ++e)
-          v[j][e] = (j0 + j < ks_n && in[e]) ? __ldcg(pp + (size_t)(j0 + j) * stride + e * NT) : 0.f;
-#pragma unroll
-      for (int j = 0; j < SB; ++j)
-#pragma unroll
-        for (int e = 0; e < COLS; ++e)
-          if (j0 + j < ks_n) acc[e] += v[j][e];
-    }
-#pragma unroll
-    for (int e = 0; e < COLS; ++e) {
-      if (!in[e]) continue;
-      const int n = n0 + e * NT;
-      const float hn = hr[n] + gate[n] * acc[e];
-      hr[n] = hn;
-      ss += hn * hn;
-    }
-  }
-  if (scale == nullptr) return;
-  ss = block_sum<NT>(ss, red);
-  const float r = 1.0f / sqrtf(ss / (float)D + eps);
-  for (int n = threadIdx.x; n < D; n += NT)
-    y[(size_t)t * D + n] = __float2bfloat16_rn(hr[n] * r * (1.f + scale[n]) + shift[n]);
-}
-
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
   const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
@@ -469,27 +571,29 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
   }
 }
 
-// Action input projection h = x W_in^T + b_in of one token row, then the first
-// layer's adaRMS into the bf16 operand of its QKV GEMM.  With A % 8 == 0 a
-// thread reads its four W_in rows as 16-byte vectors, four of each at a time.
+constexpr int kRowThreads = 256;
+
+// Action input projection h = x W_in^T + b_in of one token row (MolmoBot PR,
+// Part 2; LoongForge Pi0.5 blog, section 5.3), then the first QKV GEMM's
+// operand bf16(h * (1 + scale)) and the row's sums of h^2 per 128 features.
+// With A % 8 == 0 a thread reads its four W_in rows as 16-byte vectors.
 __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __restrict__ x,
                                                             const bf16* __restrict__ w_in,
-                                                            const bf16* __restrict__ b_in, int D, int A,
-                                                            float* __restrict__ h,
+                                                            const bf16* __restrict__ b_in, int M, int D,
+                                                            int A, float* __restrict__ h,
                                                             const float* __restrict__ scale,
-                                                            const float* __restrict__ shift, float eps,
-                                                            bf16* __restrict__ y) {
+                                                            bf16* __restrict__ aout,
+                                                            float* __restrict__ ss_out) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[kRowThreads / 32];
-  extern __shared__ float xs[];
+  extern __shared__ float xs[];  // [A] then the row of h [D]
+  float* hs = xs + A;
   const int t = blockIdx.x;
   for (int k = threadIdx.x; k < A; k += kRowThreads) xs[k] = x[(size_t)t * A + k];
   __syncthreads();
   float* hr = h + (size_t)t * D;
   const int A8 = A / 8;
   const bool vec = (A & 7) == 0;
-  float ss = 0.f;
   for (int n0 = threadIdx.x; n0 < D; n0 += 4 * kRowThreads) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (vec) {
@@ -527,40 +631,48 @@ __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __rest
       if (n >= D) continue;
       const float hn = acc[e] + __bfloat162float(b_in[n]);
       hr[n] = hn;
-      ss += hn * hn;
+      hs[n] = hn;
+      aout[(size_t)t * D + n] = __float2bfloat16_rn(hn * (1.f + scale[n]));
     }
   }
-  ss = block_sum<kRowThreads>(ss, red);
-  const float r = 1.0f / sqrtf(ss / (float)D + eps);
-  for (int n = threadIdx.x; n < D; n += kRowThreads)
-    y[(size_t)t * D + n] = __float2bfloat16_rn(hr[n] * r * (1.f + scale[n]) + shift[n]);
+  __syncthreads();
+  // sums of squares per 128-feature tile, one warp per tile, fixed order
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int tile = warp; tile < D / 128; tile += kRowThreads / 32) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v = hs[tile * 128 + 32 * j + lane];
+      ss += v * v;
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) ss_out[(size_t)tile * M + t] = ss;
+  }
 }
 
-// GeGLU of the split-K partials of the interleaved gate/up projection:
-// m[t][j] = gelu_tanh(sum g) * (sum u), sums in split order.
-__global__ void k_geglu_reduce(const float* __restrict__ part, int ks_n, int M, int F,
-                               bf16* __restrict__ m) {
-  pdl_trigger();
-  pdl_wait();
-  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long)M * F) return;
-  const int t = (int)(idx / F), j = (int)(idx - (long)t * F);
-  float g = 0.f, u = 0.f;
-  for (int s0 = 0; s0 < ks_n; s0 += 8) {  // eight splits in flight, summed in split order
-    float2 v[8];
+// fold[s][l][off + n] = sum_k W[l][n][k] * shift[s][l][k]: the constant that
+// adaRMS's shift adds to every output feature n of a GEMM, for each flow step
+// s and layer l (shift of norm `j` of the modulation table).  One warp per
+// weight row; the row stays in registers across the steps.
+__global__ void __launch_bounds__(256) k_fold_shift(const bf16* __restrict__ W, int N, int D,
+                                                    const float* __restrict__ mod, int S, int L, int j,
+                                                    float* __restrict__ fold, int nf, int off) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + warp, l = blockIdx.y;
+  if (n >= N) return;
+  const bf16* wr = W + ((size_t)l * N + n) * D;
+  for (int s = 0; s < S; ++s) {
+    const float* sh = mod + (((size_t)s * L + l) * 2 + j) * 3 * D + D;
+    float acc = 0.f;
+    for (int k0 = 8 * lane; k0 < D; k0 += 256) {
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(wr + k0), f);
 #pragma unroll
-    for (int j2 = 0; j2 < 8; ++j2)
-      v[j2] = s0 + j2 < ks_n
-                  ? __ldcg(reinterpret_cast<const float2*>(part + ((size_t)(s0 + j2) * M + t) * 2 * F + 2 * j))
-                  : make_float2(0.f, 0.f);
-#pragma unroll
-    for (int j2 = 0; j2 < 8; ++j2)
-      if (s0 + j2 < ks_n) {
-        g += v[j2].x;
-        u += v[j2].y;
-      }
+      for (int i = 0; i < 8; ++i) acc += f[i] * sh[k0 + i];
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) fold[((size_t)s * L + l) * nf + off + n] = acc;
   }
-  m[idx] = __float2bfloat16_rn(gelu_tanh(g) * u);
 }
 
 }  // namespace
@@ -569,8 +681,8 @@ size_t tc_gemm_smem_bytes(int stages, int tok_tile) {
   return 1024 + (size_t)stages * (kATileBytes + (size_t)tok_tile * 128) + (2 * stages + 1) * 8 + 64;
 }
 
-GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split) {
-  GemmPlan p;
+// Token tiling and pipeline depth shared by both planners.
+static void plan_tiles(GemmPlan& p, int N, int K, int M) {
   p.N = N;
   p.K = K;
   p.n_tiles = N / 128;
@@ -581,6 +693,28 @@ GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_spl
   if (tt < 16) tt = 16;
   p.tok_tile = tt;
   p.kb_total = K / 64;
+  int cols = 32;
+  while (cols < tt) cols <<= 1;
+  p.tmem_cols = cols;
+}
+
+static void plan_stages(GemmPlan& p) {
+  const int tt = p.tok_tile;
+  // as many stages as a CTA has K blocks, within the shared-memory budget
+  const int per_cta = (p.kb_total + p.ksplit - 1) / p.ksplit;
+  int stages = per_cta < 8 ? per_cta : 8;
+  if (stages < 2) stages = 2;
+  while (stages > 2 && tc_gemm_smem_bytes(stages, tt) > 200 * 1024) --stages;
+  // the epilogue stages its fp32 tile (tt x 128) in the drained pipeline buffers
+  while ((size_t)stages * (kATileBytes + (size_t)tt * 128) < (size_t)tt * 512 && stages < 8) ++stages;
+  p.stages = stages;
+  p.smem = tc_gemm_smem_bytes(stages, tt);
+  p.grid = p.n_tiles * p.tok_tiles * p.ksplit;
+}
+
+GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split) {
+  GemmPlan p;
+  plan_tiles(p, N, K, M);
   const int base = p.n_tiles * p.tok_tiles;
   int ks = sm_count / base;
   if (max_split > 0 && ks > max_split) ks = max_split;
@@ -588,39 +722,87 @@ GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_spl
   if (ks < 1) ks = 1;
   if (ks > p.kb_total) ks = p.kb_total;
   p.ksplit = ks;
-  int cols = 32;
-  while (cols < tt) cols <<= 1;
-  p.tmem_cols = cols;
-  // as many stages as a CTA has K blocks, within the shared-memory budget
-  const int per_cta = (p.kb_total + ks - 1) / ks;
-  int stages = per_cta < 8 ? per_cta : 8;
-  if (stages < 2) stages = 2;
-  while (stages > 2 && tc_gemm_smem_bytes(stages, tt) > 200 * 1024) --stages;
-  // the epilogue stages its output tile (up to tt x 128 fp32) in the drained pipeline buffers
-  while ((size_t)stages * (kATileBytes + (size_t)tt * 128) < (size_t)tt * 512 && stages < 8) ++stages;
-  p.stages = stages;
-  p.smem = tc_gemm_smem_bytes(stages, tt);
-  p.grid = base * ks;
+  plan_stages(p);
   return p;
 }
 
-// Every kernel of the bf16 path asks for the same (maximum) shared-memory
-// carve-out, so consecutive kernels never make an SM re-partition L1/shared.
-template <typename K>
-cudaError_t max_carveout(K kern) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              (int)cudaSharedmemCarveoutMaxShared);
+namespace {
+// Clusters of `ks` CTAs of this configuration the GPU holds at once (cached
+// per device and configuration).
+int max_active_clusters(int ew, int ks, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, ew, ks, smem);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(ks * 64));
+  cfg.blockDim = dim3((unsigned)kThreadsFor(ew));
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)ks;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const cudaError_t e = ew == 8 ? cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<8>, &cfg)
+                                : cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<4>, &cfg);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+}  // namespace
+
+GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split) {
+  GemmPlan p;
+  plan_tiles(p, N, K, M);
+  const int ew = p.tok_tile > 64 ? 8 : 4;
+  const int base = p.n_tiles * p.tok_tiles;
+  int ks = sm_count / base;
+  if (max_split > 0 && ks > max_split) ks = max_split;
+  if (ks > kMaxCluster) ks = kMaxCluster;
+  if (ks > p.kb_total) ks = p.kb_total;
+  if (ks < 1) ks = 1;
+  // a split costs nothing only while every cluster of the launch is resident at once
+  for (;; --ks) {
+    p.ksplit = ks;
+    // as many stages as a CTA has K blocks, within the shared-memory budget
+    const int per_cta = (p.kb_total + ks - 1) / ks;
+    int stages = per_cta < 8 ? per_cta : 8;
+    if (stages < 2) stages = 2;
+    while (stages > 2 && 1024 + gemm_smem_layout(stages, p.tok_tile, ks).total > 220 * 1024) --stages;
+    p.stages = stages;
+    p.smem = 1024 + gemm_smem_layout(stages, p.tok_tile, ks).total;
+    p.grid = base * ks;
+    if (ks == 1 || max_active_clusters(ew, ks, p.smem) >= base) break;
+  }
+  return p;
 }
 
 cudaError_t gemm_kernel_setup() {
-  cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_tc_gemm<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-  if (e == cudaSuccess) e = max_carveout(k_tc_gemm<4>);
-  if (e == cudaSuccess) e = max_carveout(k_tc_gemm<8>);
-  if (e == cudaSuccess) e = max_carveout(k_reduce_qkv);
-  if (e == cudaSuccess) e = max_carveout(k_resid_norm<256, 4, 8>);
-  if (e == cudaSuccess) e = max_carveout(k_inproj_norm);
-  if (e == cudaSuccess) e = max_carveout(k_geglu_reduce);
+  cudaError_t e = cudaSuccess;
+  auto attrs = [&](auto kern) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  };
+  attrs(k_tc_gemm<4>);
+  attrs(k_tc_gemm<8>);
+  // every kernel of the bf16 path asks for the same (maximum) shared-memory
+  // carve-out, so consecutive kernels never make an SM re-partition L1/shared
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_inproj_norm, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
@@ -636,53 +818,43 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
   a.stages = p.stages;
   a.tmem_cols = p.tmem_cols;
   a.tok_half = ((p.tok_tile / 2 + 15) / 16) * 16;
-  CUtensorMap omap;
-  memset(&omap, 0, sizeof(omap));
-  a.tma_out = 0;
-  cudaError_t e = cudaSuccess;
-  if (a.e_mode == kEPartial) {
-    e = make_f32_3d_map(&omap, a.part, p.N, a.M, p.ksplit, p.tok_tile);
-    a.tma_out = 1;
-  } else if (a.e_mode == kEQkvRope && a.dh >= 128) {
-    e = make_bf16_map(&omap, a.out_bf16, a.out_rows, p.N, p.tok_tile);
-    a.tma_out = 1;
-  } else if (a.e_mode == kEGeglu) {
-    e = make_bf16_map(&omap, a.out_bf16, a.out_rows, p.N / 2, p.tok_tile);
-    a.tma_out = 1;
+  const int ew = p.tok_tile > 64 ? 8 : 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.blockDim = dim3((unsigned)kThreadsFor(ew));
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
-  if (e != cudaSuccess) return e;
-  if (p.tok_tile > 64)
-    return launch_k(k_tc_gemm<8>, dim3(p.grid), dim3(kThreadsFor(8)), p.smem, s, pdl, wmap, amap, omap, a);
-  return launch_k(k_tc_gemm<4>, dim3(p.grid), dim3(kThreadsFor(4)), p.smem, s, pdl, wmap, amap, omap, a);
+  if (p.ksplit > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = (unsigned)p.ksplit;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  if (ew == 8) return cudaLaunchKernelEx(&cfg, k_tc_gemm<8>, wmap, amap, a);
+  return cudaLaunchKernelEx(&cfg, k_tc_gemm<4>, wmap, amap, a);
 }
 
-cudaError_t launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
-                              const float2* cs, bf16* out, cudaStream_t s, bool pdl) {
-  const long n = (long)M * (N / 2);
-  return launch_k(k_reduce_qkv, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl, part, ks, M,
-                  N, dh, n_rot_heads, cs, out);
+cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
+                               float* h, const float* scale, bf16* aout, float* ss_out, cudaStream_t s,
+                               bool pdl) {
+  return launch_k(k_inproj_norm, dim3(M), dim3(kRowThreads), (size_t)(A + D) * sizeof(float), s, pdl, x,
+                  w_in, b_in, M, D, A, h, scale, aout, ss_out);
 }
 
-cudaError_t launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
-                              const float* scale, const float* shift, float eps, bf16* y,
-                              cudaStream_t s, bool pdl) {
-  // 256 threads x 4 columns a row (measured faster than 1024 x 1 at 50 rows too)
-  return launch_k(k_resid_norm<256, 4, 8>, dim3(M), dim3(256), 0, s, pdl, part, ks, M, D, h, gate, scale, shift,
-                  eps, y);
-}
-
-cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D,
-                               int A, float* h, const float* scale, const float* shift, float eps,
-                               bf16* y, cudaStream_t s, bool pdl) {
-  return launch_k(k_inproj_norm, dim3(M), dim3(kRowThreads), A * sizeof(float), s, pdl, x, w_in,
-                  b_in, D, A, h, scale, shift, eps, y);
-}
-
-cudaError_t launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s,
-                                bool pdl) {
-  const long n = (long)M * F;
-  return launch_k(k_geglu_reduce, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl, part, ks,
-                  M, F, m);
+cudaError_t launch_fold_shift(const bf16* W, int N, int D, const float* mod, int S, int L, int j, float* fold,
+                              int nf, int off, cudaStream_t s) {
+  return launch_k(k_fold_shift, dim3((unsigned)((N + 7) / 8), (unsigned)L), dim3(256), 0, s, false, W, N, D,
+                  mod, S, L, j, fold, nf, off);
 }
 
 }  // namespace ae

@@ -40,6 +40,7 @@ struct TimeTable {
   float* fin = nullptr;  // [S][2D]
   float* act = nullptr;  // [S][2][D] sinusoid / hidden of the time MLP (scratch)
   float* c = nullptr;    // [S][D] time-MLP output
+  float* fold = nullptr; // bf16 path: [S][L][(Hq+2Hkv)dh + 2F] shift W^T of the QKV and gate/up GEMMs
 };
 
 struct BindState {
@@ -115,8 +116,8 @@ struct ae_ctx {
   CUtensorMap map_qtile;                        // the same, boxes q_box_rows rows x 64 (attention query tiles)
   int q_box_rows = 16;
   int act_box_rows = 0;
-  float* sumsq = nullptr;    // [D/128][M] adaRMS sum of squares per 128-feature tile
-  float* part = nullptr;     // split-K partials
+  float* sumsq = nullptr;    // [D/128][M] sums of h^2 per 128-feature tile (adaRMS folded into GEMMs)
+  float* part = nullptr;     // split-K partials (persistent kernel)
   size_t part_floats = 0;
   float* attn_o = nullptr;   // attention partials
   float2* attn_ml = nullptr;
@@ -192,45 +193,50 @@ cudaError_t launch_final_bf16(ae_ctx* c, const TimeTable& t, int step, float* x,
                               bool pdl);
 
 // ---- tensor-core GEMM (ae_gemm_tc.cu)
-enum EMode : int { kEPartial = 0, kEQkvRope = 1, kEGeglu = 2 };
-
+enum EMode : int { kEPartial = 0, kEQkvRope = 1, kEGeglu = 2, kEResid = 3 };
 struct TcGemmArgs {
   int M, N, K;          // tokens, output features, reduction length
   int w_row0;           // first row of this layer's matrix in the stacked weight
   int w_next_row0;      // first row of the matrix to prefetch into L2 (-1: none)
   int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
   int tok_half;         // first token column of the second epilogue half (multiple of 16)
-  int e_mode;
-  int tma_out;          // set by the launcher: the epilogue stages its tile and stores it by TMA
-  int out_rows;         // rows of out_bf16's buffer (its TMA view)
-  float* part;          // kEPartial: [ksplit][M][N]
+  int e_mode;           // kEQkvRope, kEGeglu or kEResid
+  // kEQkvRope / kEGeglu: the operand is bf16(h * (1 + scale)); adaRMS is folded in
+  const float* ss_in;   // [n_ss][M] sums of h^2 per 128 features of the operand's rows
+  int n_ss, norm_dim;   // D / 128, D
+  float eps;
+  const float* fold;    // [N] shift W^T of this layer and flow step
   bf16* out_bf16;       // kEQkvRope: [M][N]; kEGeglu: [M][N/2]
   const float2* rope_cs;
   int dh, n_rot_heads;
+  // kEResid: h += gate * acc, then the next GEMM's operand and its sums of squares
+  float* h;                 // [M][N] residual stream, updated in place
+  const float* gate;        // [N]
+  const float* scale_next;  // [N], or nullptr when no GEMM follows
+  bf16* a_out;              // [M][N] bf16(h * (1 + scale_next))
+  float* ss_out;            // [N/128][M]
   int* status;
 };
-
 struct GemmPlan {
   int N, K, n_tiles, tok_tiles, tok_tile, kb_total, ksplit, tmem_cols, stages, grid;
   size_t smem;
 };
-
 size_t tc_gemm_smem_bytes(int stages, int tok_tile);
+// Split-K plan of the persistent kernel (partials through global memory).
 GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split = 0);
+// Split-K plan of k_tc_gemm: the splits of a tile form one cluster (<= 16 CTAs),
+// no more splits than keep every cluster of the launch resident at once.
+GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split = 0);
 cudaError_t gemm_kernel_setup();
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
                            TcGemmArgs a, cudaStream_t s, bool pdl);
-cudaError_t launch_reduce_qkv(const float* part, int ks, int M, int N, int dh, int n_rot_heads,
-                              const float2* cs, bf16* out, cudaStream_t s, bool pdl);
-cudaError_t launch_resid_norm(const float* part, int ks, int M, int D, float* h, const float* gate,
-                              const float* scale, const float* shift, float eps, bf16* y,
-                              cudaStream_t s, bool pdl);
-cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D,
-                               int A, float* h, const float* scale, const float* shift, float eps,
-                               bf16* y, cudaStream_t s, bool pdl);
-cudaError_t launch_geglu_reduce(const float* part, int ks, int M, int F, bf16* m, cudaStream_t s,
-                                bool pdl);
-
+// h = x W_in^T + b_in; aout = bf16(h * (1 + scale)); ss_out [D/128][M] sums of h^2.
+cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
+                               float* h, const float* scale, bf16* aout, float* ss_out, cudaStream_t s,
+                               bool pdl);
+// fold[s][l][off + n] = sum_k W[l][n][k] * mod[s][l][j][shift][k] for every step and layer.
+cudaError_t launch_fold_shift(const bf16* W, int N, int D, const float* mod, int S, int L, int j, float* fold,
+                              int nf, int off, cudaStream_t s);
 // ---- tensor-core attention (ae_attn_tc.cu)
 struct AttnArgs {
   const bf16* qkv;        // [M][(Hq + 2 Hkv) dh] after RoPE
