@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
               const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // keeps the shared address space
   constexpr int dh = DH;
   constexpr int kdb = dh / 64;
   const AttnSmem L = attn_smem_layout(dh);
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     k_attn_pipe(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap, const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // keeps the shared address space
   constexpr int kdb = DH / 64;
   constexpr uint32_t kTmemCols = DH + 2 * kChunk <= 256 ? 256 : 512;
   const PipeSmem L = pipe_smem_layout(DH);

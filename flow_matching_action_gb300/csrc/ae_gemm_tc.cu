@@ -79,15 +79,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
-// Every thread of every CTA of the cluster arrives and waits; shared-memory
-// writes before it are visible to the whole cluster after it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
-
 // Address of the same shared-memory location in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -95,29 +86,42 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a0, float a1, float a2, float a3) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a0), "f"(a1), "f"(a2),
-               "f"(a3));
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v));
 }
 
-// Split-K receive buffer: for each of ks source ranks, 128 feature rows of
-// `pad` floats (this rank's tokens, padded to an odd multiple of 4 so that
-// 16-byte accesses of consecutive feature rows hit distinct bank groups).
-__host__ __device__ inline int recv_pad(int n_tok, int ks) {
-  const int g = ((n_tok + 3) / 4 + ks - 1) / ks;  // 4-token groups per rank
-  return 4 * (g | 1);
+// Bulk copy of `bytes` from this CTA's shared memory to a cluster peer's
+// (`dst`, `mbar` mapped to the peer), counted in bytes on the peer's mbarrier.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(src), "r"(bytes), "r"(mbar)
+               : "memory");
 }
+
+// Split-K: the tokens of a tile are dealt to the ranks of its cluster in runs
+// of whole 4-token groups; rank r emits tokens [run_lo(r), run_hi(r)).
+__host__ __device__ inline int run_lo(int r, int ng, int ks) { return 4 * (r * ng / ks); }
+// Tokens of the longest run: a rank's receive buffer holds the partials of its
+// run from each rank, token-major: recv[src][token][128 features].
+__host__ __device__ inline int recv_slice(int n_tok, int ks) { return 4 * (((n_tok + 3) / 4 + ks - 1) / ks); }
 
 __host__ __device__ inline uint32_t recv_bytes(int tt, int ks) {
-  return ks > 1 ? (uint32_t)ks * 128u * (uint32_t)recv_pad(tt, ks) * 4u : 0u;
+  return ks > 1 ? (uint32_t)ks * (uint32_t)recv_slice(tt, ks) * 512u : 0u;
 }
 
 // Shared-memory layout of k_tc_gemm, byte offsets from the 1024-aligned base:
-// pipeline stages (weights, token tiles), the split-K receive buffer, mbarriers
-// and flags, the owner of each 4-token group, the per-token reciprocal RMS of
-// the emitted tokens and the per-quarter sums of squares.
+// pipeline stages (weights, token tiles; after the mainloop they stage the
+// fp32 partial tile), the split-K receive buffer, mbarriers and flags, the
+// per-token reciprocal RMS of the emitted tokens and the per-quarter sums of
+// squares.
 struct GemmSmem {
-  uint32_t a, b, recv, bars, own, rn, red, total;
+  uint32_t a, b, recv, bars, rn, red, total;
 };
 
 __host__ __device__ inline GemmSmem gemm_smem_layout(int stages, int tt, int ks) {
@@ -126,8 +130,7 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int stages, int tt, int ks)
   L.b = (uint32_t)stages * kATileBytes;
   L.recv = L.b + (uint32_t)(stages * tt * 128);
   L.bars = L.recv + recv_bytes(tt, ks);
-  L.own = L.bars + (uint32_t)(2 * stages + 1) * 8u + 64u;  // + TMEM base, abort flag, votes[8]
-  L.rn = L.own + 64u * 4u;
+  L.rn = L.bars + (uint32_t)(2 * stages + 2) * 8u + 64u;  // + TMEM base, abort flag, votes[8]
   L.red = L.rn + (256u + 16u) * 4u;
   L.total = L.red + 4u * 256u * 4u;
   return L;
@@ -282,10 +285,10 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
   uint64_t* tmem_full = empty + S;
-  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  uint64_t* recv_bar = tmem_full + 1;  // split K: this rank's partials from every rank have landed
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(recv_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
   volatile int* votes = reinterpret_cast<volatile int*>(tmem_base_p + 2);  // [kEpiWarps]
-  int* own_s = reinterpret_cast<int*>(smem + L.own);                        // [64]
   float* rn_s = reinterpret_cast<float*>(smem + L.rn);                      // [<= 256 + 16]
   float* red_s = reinterpret_cast<float*>(smem + L.red);                    // [4][TT]
   const float* recv = reinterpret_cast<const float*>(smem + L.recv);
@@ -304,9 +307,9 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   // Tokens this CTA emits: the whole tile when unsplit, else its rank's run
   // of 4-token groups.
   const int ng = (nv + 3) >> 2;
-  const int e_lo = 4 * (ks * ng / ksn);
-  const int e_hi = min(4 * ((ks + 1) * ng / ksn), nv);
-  const int pad = recv_pad(nv, ksn);
+  const int e_lo = run_lo(ks, ng, ksn);
+  const int e_hi = min(run_lo(ks + 1, ng, ksn), nv);
+  const int slice = recv_slice(nv, ksn);
   auto kcol = [&](int it) { return (kb_begin + it) * 64; };
   pdl_trigger();
 
@@ -316,6 +319,9 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
+    mbar_init(recv_bar, 1);
+    // bulk exchange: every rank sends this rank its partials of our run
+    if (ksn > 1 && a.xbulk) mbar_arrive_expect_tx(recv_bar, (uint32_t)(ksn * (e_hi - e_lo) * 512));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -327,6 +333,9 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // peers may write into this CTA once its receive barrier is initialised
+  const bool xbulk = a.xbulk != 0;
+  if (ksn > 1) cluster_arrive();
   const uint32_t tmem_d = *tmem_base_p;
   bool go = false;
   // epilogue role (warps 2..): TMEM lane quarter, column half, feature row
@@ -437,12 +446,6 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     } else {
       cf = E.fold[n];
     }
-    // owner rank and local group of every 4-token group of the tile
-    if (ksn > 1)
-      for (int g = et; g < ng; g += kEpiThreads) {
-        const int r = ((g + 1) * ksn - 1) / ng;  // r * ng / ks <= g < (r + 1) * ng / ks
-        own_s[g] = (r << 16) | (g - r * ng / ksn);
-      }
     pdl_wait();
     // reciprocal RMS of the emitted tokens, while the mainloop runs
     if (E.mode != kEResid)
@@ -486,30 +489,80 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         if (E.mode == kEQkvRope) run(std::integral_constant<int, kEQkvRope>());
         else if (E.mode == kEGeglu) run(std::integral_constant<int, kEGeglu>());
         else run(std::integral_constant<int, kEResid>());
-      } else {
-        // split K: push this partial to each 4-token group's owner in the
-        // cluster, recv[this rank][feature][token], 16 bytes per store; a
-        // remote store needs no round trip
-        const uint32_t recv_u = smem_u32(smem + L.recv) + (uint32_t)((ks * 128 + f) * pad) * 4u;
+      } else if (xbulk) {
+        // split K: stage this partial token-major in the drained pipeline
+        // buffers, then send each rank its run of tokens with one bulk copy
+        float* stg = reinterpret_cast<float*>(smem);
         for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
           float v[16];
           tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int g = (c0 >> 2) + i;
-            if (4 * g < c_hi) {
-              const int o = own_s[g];
-              st_cluster_v4(mapa(recv_u + (uint32_t)(o & 0xffff) * 16u, (uint32_t)(o >> 16)), v[4 * i],
-                            v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int j = 0; j < 16; ++j) stg[(c0 + j) * 128 + f] = v[j];
+        }
+        fence_proxy_async_smem();
+      }
+    }
+    if (ksn > 1) {
+      cluster_wait();  // every rank of the cluster has started and initialised its barrier
+      if (xbulk) {
+        named_bar<1>(kEpiThreads);
+        if (go && threadIdx.x == 64) {
+          const uint32_t stg_u = smem_u32(smem);
+          const uint32_t dst0 = smem_u32(smem + L.recv) + (uint32_t)(ks * slice) * 512u;
+          const uint32_t bar_u = smem_u32(recv_bar);
+          for (int r = 0; r < ksn; ++r) {
+            const int lo = run_lo(r, ng, ksn), hi = min(run_lo(r + 1, ng, ksn), nv);
+            if (hi <= lo) continue;
+            bulk_to_peer(mapa(dst0, (uint32_t)r), stg_u + (uint32_t)lo * 512u, (uint32_t)(hi - lo) * 512u,
+                         mapa(bar_u, (uint32_t)r));
+          }
+          bulk_commit();
+        }
+      } else {
+        // the fp32 tile does not fit the pipeline buffers: each thread stores
+        // its partials straight into the owners' receive buffers, 128
+        // contiguous bytes per token and warp
+        if (go) {
+          const uint32_t recv_u = smem_u32(smem + L.recv) + (uint32_t)(ks * slice * 128 + f) * 4u;
+          for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int t = c0 + 4 * i;
+              if (t < c_hi) {
+                const int g = t >> 2;
+                const int r = ((g + 1) * ksn - 1) / ng;  // run_lo(r) <= t < run_lo(r + 1)
+                const uint32_t a0 = mapa(recv_u + (uint32_t)(t - run_lo(r, ng, ksn)) * 512u, (uint32_t)r);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) st_cluster_f32(a0 + 512u * k, v[4 * i + k]);
+              }
             }
           }
         }
+        cluster_arrive();  // this rank's partials are written
       }
     }
   }
-  __syncwarp();
+  if (warp < 2) {
+    __syncwarp();
+    if (ksn > 1) {
+      cluster_wait();
+      if (!xbulk) {
+        cluster_arrive();
+        cluster_wait();
+      }
+    }
+  }
   if (ksn > 1) {
-    cluster_sync();  // every partial has landed in its owner
+    if (warp >= 2 && !xbulk) cluster_wait();  // every rank's partials have been written
+    if (warp >= 2 && go && xbulk) {
+      // this rank's run from every rank (bounded wait)
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(recv_bar, 0, abort_flag, status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      go = ok != 0;
+    }
     if (warp >= 2 && go) {
       // sum this rank's tokens over the cluster's partials in rank order, emit them
       auto run = [&](auto mode_tag) {
@@ -523,16 +576,10 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = 0.f;
           for (int src = 0; src < ksn; ++src) {
-            const float* rp = recv + (size_t)(src * 128 + f) * pad + c0;
+            const float* rp = recv + (size_t)(src * slice + c0) * 128 + f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (c0 + 4 * i < p_hi) {
-                const float4 x = *reinterpret_cast<const float4*>(rp + 4 * i);
-                v[4 * i] += x.x;
-                v[4 * i + 1] += x.y;
-                v[4 * i + 2] += x.z;
-                v[4 * i + 3] += x.w;
-              }
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < p_hi) v[j] += rp[j * 128];
           }
           emit16<MODE>(E, n, q, lane, c0, t0 + e_lo + c0, v, min(16, p_hi - c0), cf, gt, sc, cur);
         }
@@ -550,6 +597,8 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         ss_out[(size_t)n_tile * E.M + t0 + e_lo + i] =
             (red_s[i] + red_s[TT + i]) + (red_s[2 * TT + i] + red_s[3 * TT + i]);
   }
+  // the bulk copies out of the staging must have read it before the CTA exits
+  if (ksn > 1 && xbulk && threadIdx.x == 64) bulk_wait_read_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -693,6 +742,7 @@ static void plan_tiles(GemmPlan& p, int N, int K, int M) {
   if (tt < 16) tt = 16;
   p.tok_tile = tt;
   p.kb_total = K / 64;
+  p.xbulk = 0;
   int cols = 32;
   while (cols < tt) cols <<= 1;
   p.tmem_cols = cols;
@@ -779,10 +829,26 @@ GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split) {
     int stages = per_cta < 8 ? per_cta : 8;
     if (stages < 2) stages = 2;
     while (stages > 2 && 1024 + gemm_smem_layout(stages, p.tok_tile, ks).total > 220 * 1024) --stages;
+    // split K by bulk copies stages the fp32 partial tile (tt x 128) in the
+    // drained pipeline buffers; where it cannot fit, per-thread remote stores
+    const size_t stage_need = (size_t)p.tok_tile * 512;
+    auto fits = [&](int st) {
+      return (size_t)st * (kATileBytes + (size_t)p.tok_tile * 128) >= stage_need &&
+             1024 + gemm_smem_layout(st, p.tok_tile, ks).total <= 232448;
+    };
+    p.xbulk = 0;
+    if (ks > 1)
+      for (int st = stages; st <= 8; ++st)
+        if (fits(st)) {
+          stages = st;
+          p.xbulk = 1;
+          break;
+        }
     p.stages = stages;
     p.smem = 1024 + gemm_smem_layout(stages, p.tok_tile, ks).total;
     p.grid = base * ks;
-    if (ks == 1 || max_active_clusters(ew, ks, p.smem) >= base) break;
+    if (ks == 1) break;
+    if (p.smem <= 232448 && max_active_clusters(ew, ks, p.smem) >= base) break;
   }
   return p;
 }
@@ -818,6 +884,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
   a.stages = p.stages;
   a.tmem_cols = p.tmem_cols;
   a.tok_half = ((p.tok_tile / 2 + 15) / 16) * 16;
+  a.xbulk = p.xbulk;
   const int ew = p.tok_tile > 64 ? 8 : 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);

@@ -200,6 +200,7 @@ struct TcGemmArgs {
   int w_next_row0;      // first row of the matrix to prefetch into L2 (-1: none)
   int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
   int tok_half;         // first token column of the second epilogue half (multiple of 16)
+  int xbulk;            // split K: partials sent by bulk copies (1) or per-thread remote stores (0)
   int e_mode;           // kEQkvRope, kEGeglu or kEResid
   // kEQkvRope / kEGeglu: the operand is bf16(h * (1 + scale)); adaRMS is folded in
   const float* ss_in;   // [n_ss][M] sums of h^2 per 128 features of the operand's rows
@@ -219,6 +220,7 @@ struct TcGemmArgs {
 };
 struct GemmPlan {
   int N, K, n_tiles, tok_tiles, tok_tile, kb_total, ksplit, tmem_cols, stages, grid;
+  int xbulk;  // split K: the fp32 tile fits the drained pipeline buffers, partials go by bulk copy
   size_t smem;
 };
 size_t tc_gemm_smem_bytes(int stages, int tok_tile);

@@ -1126,7 +1126,7 @@ __device__ void l2_warm(const void* p, size_t bytes) {
 __global__ void __launch_bounds__(kPT, 1) k_persistent(const __grid_constant__ PersistParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Ctx c;
-  c.smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  c.smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // keeps the shared address space
   c.rows = reinterpret_cast<float*>(c.smem + P.data_bytes);
   c.ctrl = reinterpret_cast<Ctrl*>(c.smem + P.data_bytes + P.row_bytes);
   const int warp = threadIdx.x >> 5;
