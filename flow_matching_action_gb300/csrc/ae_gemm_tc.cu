@@ -72,38 +72,6 @@ __device__ __forceinline__ void named_bar(int n) {
   asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(n) : "memory");
 }
 
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address of the same shared-memory location in cluster CTA `rank`.
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v));
-}
-
-// Bulk copy of `bytes` from this CTA's shared memory to a cluster peer's
-// (`dst`, `mbar` mapped to the peer), counted in bytes on the peer's mbarrier.
-__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst),
-               "r"(src), "r"(bytes), "r"(mbar)
-               : "memory");
-}
-
 // Split-K: the tokens of a tile are dealt to the ranks of its cluster in runs
 // of whole 4-token groups; rank r emits tokens [run_lo(r), run_hi(r)).
 __host__ __device__ inline int run_lo(int r, int ng, int ks) { return 4 * (r * ng / ks); }
