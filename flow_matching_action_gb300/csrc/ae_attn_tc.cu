@@ -868,14 +868,27 @@ __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
   const int n_splits = (n_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
   const int d = threadIdx.x;
   const size_t unit0 = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits;
-  float m = -INFINITY;
-  for (int sp = 0; sp < n_splits; ++sp) m = fmaxf(m, a.part_ml[(unit0 + sp) * 128 + row].x);
-  float l = 0.f, acc = 0.f;
-  for (int sp = 0; sp < n_splits; ++sp) {
-    const float2 ml = a.part_ml[(unit0 + sp) * 128 + row];
-    const float w = ex2_fast(ml.x - m);
-    l += ml.y * w;
-    acc += a.part_o[((unit0 + sp) * 128 + row) * a.dh + d] * w;
+  // one pass: the loads of up to 16 ranges are issued together, then merged
+  // in range order with an online rescale (deterministic)
+  float m = -INFINITY, l = 0.f, acc = 0.f;
+  for (int s0 = 0; s0 < n_splits; s0 += 16) {
+    float2 ml[16];
+    float pv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const bool in = s0 + j < n_splits;
+      ml[j] = in ? __ldcg(a.part_ml + (unit0 + s0 + j) * 128 + row) : make_float2(-INFINITY, 0.f);
+      pv[j] = in ? __ldcg(a.part_o + ((unit0 + s0 + j) * 128 + row) * a.dh + d) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (s0 + j >= n_splits) break;
+      const float mn = fmaxf(m, ml[j].x);
+      const float ra = ex2_fast(m - mn), rb = ex2_fast(ml[j].x - mn);
+      l = l * ra + ml[j].y * rb;
+      acc = acc * ra + pv[j] * rb;
+      m = mn;
+    }
   }
   const int h = g * G + hh;
   o[(size_t)(b * a.H + tok) * (a.Hq * a.dh) + h * a.dh + d] = __float2bfloat16_rn(acc / l);

@@ -120,7 +120,93 @@ struct Epi {
   const float* rn; // shared, per emitted token
 };
 
-// Per-token inputs of one 16-token chunk that the epilogue of MODE reads from
+// Per-token inputs of one 4-token group that the epilogue of MODE reads from
+// global memory (RoPE (cos, sin) of the thread's pair, or the residual h);
+// loaded two groups ahead of use.
+template <int MODE>
+__device__ __forceinline__ void pre4(const Epi& E, int n, int tok0, int cnt, float2 (&aux)[4]) {
+  if (MODE == kEQkvRope) {
+    const int hb = n / E.dh, pair = (n - hb * E.dh) >> 1;
+    const bool rot = hb < E.n_rot_heads;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      aux[j] = (rot && j < cnt) ? __ldg(E.rope_cs + (size_t)(tok0 + j) * E.half + pair) : make_float2(1.f, 0.f);
+  } else if (MODE == kEResid) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) aux[j].x = j < cnt ? E.h[(size_t)(tok0 + j) * E.N + n] : 0.f;
+  }
+}
+
+// Epilogue of up to 4 consecutive emitted tokens of feature row n (token
+// tok0.., index i0.. among this CTA's emitted tokens), values v = sums over K,
+// aux = pre4 of the group.  All lanes of the warp call it with the same i0,
+// tok0 and cnt (shuffles inside).  Small on purpose: it runs in a rolled loop.
+template <int MODE>
+__device__ __forceinline__ void emit4(const Epi& E, int n, int q, int lane, int i0, int tok0, const float (&v)[4],
+                                      int cnt, float cf, float gt, float sc, const float2 (&aux)[4]) {
+  if (MODE == kEResid) {
+    float hn[4], sq[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      hn[j] = aux[j].x + gt * v[j];
+      sq[j] = j < cnt ? hn[j] * hn[j] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < cnt) {
+        E.h[(size_t)(tok0 + j) * E.N + n] = hn[j];
+        if (E.scale_next != nullptr) E.a_out[(size_t)(tok0 + j) * E.N + n] = __float2bfloat16_rn(hn[j] * (1.f + sc));
+      }
+    // per-token sum over the warp by a transposed butterfly: lanes with bit 4
+    // clear keep tokens 0, 1, then lanes with bit 3 clear keep the first of
+    // the two; lane l ends with token 2 b4 + b3
+    {
+      const bool up = lane & 16;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float got = __shfl_xor_sync(0xffffffffu, up ? sq[k] : sq[2 + k], 16);
+        sq[k] = (up ? sq[2 + k] : sq[k]) + got;
+      }
+    }
+    const bool up8 = lane & 8;
+    float s = (up8 ? sq[1] : sq[0]) + __shfl_xor_sync(0xffffffffu, up8 ? sq[0] : sq[1], 8);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    const int t = 2 * ((lane >> 4) & 1) + ((lane >> 3) & 1);
+    if ((lane & 7) == 0 && t < cnt) E.red[q * E.TT + i0 + t] = s;
+  } else if (MODE == kEGeglu) {
+    // lane 2i holds gate row i, lane 2i + 1 its up row; the even lane takes
+    // tokens 0, 1 of the group, the odd lane tokens 2, 3
+    float x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = E.rn[i0 + j] * v[j] + cf;
+    const bool odd = lane & 1;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float got = __shfl_xor_sync(0xffffffffu, odd ? x[k] : x[2 + k], 1);
+      const float g = odd ? got : x[k], u = odd ? x[2 + k] : got;
+      const int j = odd ? 2 + k : k;
+      if (j < cnt) E.out[(size_t)(tok0 + j) * (E.N >> 1) + (n >> 1)] = __float2bfloat16_rn(gelu_tanh(g) * u);
+    }
+  } else {  // kEQkvRope: packed rows 2j, 2j + 1 of a head are its dims j, j + dh/2
+    const int hb = n / E.dh, p = n - hb * E.dh;
+    const int pair = p >> 1, odd = p & 1;
+    const bool rot = hb < E.n_rot_heads;
+    bf16* ocol = E.out + hb * E.dh + pair + odd * E.half;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float x = E.rn[i0 + j] * v[j] + cf;
+      const float other = __shfl_xor_sync(0xffffffffu, x, 1);
+      float o = x;
+      if (rot) o = odd ? (x * aux[j].x + other * aux[j].y) : (x * aux[j].x - other * aux[j].y);
+      if (j < cnt) ocol[(size_t)(tok0 + j) * E.N] = __float2bfloat16_rn(o);
+    }
+  }
+}
+
+// The same for a 16-token chunk (more independent work per warp for long
+// token runs).  Per-token inputs of one 16-token chunk that the epilogue of MODE reads from
 // global memory (RoPE (cos, sin) of the thread's pair, or the residual h),
 // loaded one chunk ahead of use.
 template <int MODE>
@@ -335,7 +421,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   float* const ss_out = a.ss_out;
   int* const status = a.status;
   float cf = 0.f, gt = 0.f, sc = 0.f;
-  float2 aux[16];  // per-token inputs of the next chunk (epilogue warps)
+  float2 aux0[4], aux1[4];  // per-token inputs of the next two 4-token groups (epilogue warps)
   // token columns this warp reads from TMEM (unsplit: also the ones it emits)
   const int c_lo = hf ? a.tok_half : 0;
   const int c_hi = min((hf || EW == 4) ? TT : a.tok_half, nv);
@@ -423,15 +509,16 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         for (int j = 0; j < E.n_ss; ++j) ss += E.ss_in[(size_t)j * E.M + tok];
         rn_s[i] = 1.0f / sqrtf(ss / (float)E.norm_dim + E.eps);
       }
-    // the first chunk's per-token inputs, issued before the accumulator is ready
-    if (ksn == 1) {
-      if (c_lo < c_hi) {
-        if (E.mode == kEQkvRope) pre16<kEQkvRope>(E, n, t0 + c_lo, min(16, c_hi - c_lo), aux);
-        else if (E.mode == kEResid) pre16<kEResid>(E, n, t0 + c_lo, min(16, c_hi - c_lo), aux);
+    // the first two groups' per-token inputs, issued before the accumulator is ready
+    {
+      const int lo = ksn == 1 ? c_lo : e_lo + p_lo, hi = ksn == 1 ? c_hi : e_lo + p_hi;
+      if (E.mode == kEQkvRope) {
+        if (lo < hi) pre4<kEQkvRope>(E, n, t0 + lo, min(4, hi - lo), aux0);
+        if (lo + 4 < hi) pre4<kEQkvRope>(E, n, t0 + lo + 4, min(4, hi - lo - 4), aux1);
+      } else if (E.mode == kEResid) {
+        if (lo < hi) pre4<kEResid>(E, n, t0 + lo, min(4, hi - lo), aux0);
+        if (lo + 4 < hi) pre4<kEResid>(E, n, t0 + lo + 4, min(4, hi - lo - 4), aux1);
       }
-    } else if (p_lo < p_hi) {
-      if (E.mode == kEQkvRope) pre16<kEQkvRope>(E, n, t0 + e_lo + p_lo, min(16, p_hi - p_lo), aux);
-      else if (E.mode == kEResid) pre16<kEResid>(E, n, t0 + e_lo + p_lo, min(16, p_hi - p_lo), aux);
     }
     if (lane == 0) votes[e] = (mbar_wait(tmem_full, 0, abort_flag, status) && !*abort_flag) ? 1 : 0;
     named_bar<1>(kEpiThreads);
@@ -441,17 +528,37 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     if (go) {
       tc_fence_after();
       if (ksn == 1) {
-        // unsplit: the accumulator is the sum; emit straight from TMEM
+        // unsplit: the accumulator is the sum; emit straight from TMEM, 4 tokens a step
         auto run = [&](auto mode_tag) {
           constexpr int MODE = decltype(mode_tag)::value;
-          for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-            float2 cur[16];
+          if (c_hi - c_lo >= 32) {
+            // long run: 16 tokens a step, next chunk's inputs one step ahead
+            float2 nx[16];
+            pre16<MODE>(E, n, t0 + c_lo, min(16, c_hi - c_lo), nx);
+#pragma unroll 1
+            for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+              float2 cur[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) cur[j] = aux[j];
-            if (c0 + 16 < c_hi) pre16<MODE>(E, n, t0 + c0 + 16, min(16, c_hi - c0 - 16), aux);
-            float v[16];
-            tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
-            emit16<MODE>(E, n, q, lane, c0, t0 + c0, v, min(16, c_hi - c0), cf, gt, sc, cur);
+              for (int j = 0; j < 16; ++j) cur[j] = nx[j];
+              if (c0 + 16 < c_hi) pre16<MODE>(E, n, t0 + c0 + 16, min(16, c_hi - c0 - 16), nx);
+              float v[16];
+              tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+              emit16<MODE>(E, n, q, lane, c0, t0 + c0, v, min(16, c_hi - c0), cf, gt, sc, cur);
+            }
+            return;
+          }
+#pragma unroll 1
+          for (int c0 = c_lo; c0 < c_hi; c0 += 4) {
+            float2 cur[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              cur[j] = aux0[j];
+              aux0[j] = aux1[j];
+            }
+            if (c0 + 8 < c_hi) pre4<MODE>(E, n, t0 + c0 + 8, min(4, c_hi - c0 - 8), aux1);
+            float v[4];
+            tmem_ld4(tmem_d + trow + (uint32_t)c0, v);
+            emit4<MODE>(E, n, q, lane, c0, t0 + c0, v, min(4, c_hi - c0), cf, gt, sc, cur);
           }
         };
         if (E.mode == kEQkvRope) run(std::integral_constant<int, kEQkvRope>());
@@ -461,11 +568,12 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         // split K: stage this partial token-major in the drained pipeline
         // buffers, then send each rank its run of tokens with one bulk copy
         float* stg = reinterpret_cast<float*>(smem);
-        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-          float v[16];
-          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+#pragma unroll 1
+        for (int c0 = c_lo; c0 < c_hi; c0 += 4) {
+          float v[4];
+          tmem_ld4(tmem_d + trow + (uint32_t)c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg[(c0 + j) * 128 + f] = v[j];
+          for (int j = 0; j < 4; ++j) stg[(c0 + j) * 128 + f] = v[j];
         }
         fence_proxy_async_smem();
       }
@@ -492,20 +600,14 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         // contiguous bytes per token and warp
         if (go) {
           const uint32_t recv_u = smem_u32(smem + L.recv) + (uint32_t)(ks * slice * 128 + f) * 4u;
-          for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+#pragma unroll 1
+          for (int c0 = c_lo; c0 < c_hi; c0 += 4) {
+            float v[4];
+            tmem_ld4(tmem_d + trow + (uint32_t)c0, v);
+            const int r = ((c0 / 4 + 1) * ksn - 1) / ng;  // run_lo(r) <= c0 < run_lo(r + 1)
+            const uint32_t a0 = mapa(recv_u + (uint32_t)(c0 - run_lo(r, ng, ksn)) * 512u, (uint32_t)r);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int t = c0 + 4 * i;
-              if (t < c_hi) {
-                const int g = t >> 2;
-                const int r = ((g + 1) * ksn - 1) / ng;  // run_lo(r) <= t < run_lo(r + 1)
-                const uint32_t a0 = mapa(recv_u + (uint32_t)(t - run_lo(r, ng, ksn)) * 512u, (uint32_t)r);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) st_cluster_f32(a0 + 512u * k, v[4 * i + k]);
-              }
-            }
+            for (int k = 0; k < 4; ++k) st_cluster_f32(a0 + 512u * k, v[k]);
           }
         }
         cluster_arrive();  // this rank's partials are written
@@ -535,21 +637,67 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       // sum this rank's tokens over the cluster's partials in rank order, emit them
       auto run = [&](auto mode_tag) {
         constexpr int MODE = decltype(mode_tag)::value;
-        for (int c0 = p_lo; c0 < p_hi; c0 += 16) {
-          float2 cur[16];
+        if (MODE != kEResid && p_hi - p_lo >= 16) {
+          // long run: 16 tokens a step, four ranks' loads in flight
+          float2 nx[16];
+          pre16<MODE>(E, n, t0 + e_lo + p_lo, min(16, p_hi - p_lo), nx);
+#pragma unroll 1
+          for (int c0 = p_lo; c0 < p_hi; c0 += 16) {
+            float2 cur[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) cur[j] = aux[j];
-          if (c0 + 16 < p_hi) pre16<MODE>(E, n, t0 + e_lo + c0 + 16, min(16, p_hi - c0 - 16), aux);
-          float v[16];
+            for (int j = 0; j < 16; ++j) cur[j] = nx[j];
+            if (c0 + 16 < p_hi) pre16<MODE>(E, n, t0 + e_lo + c0 + 16, min(16, p_hi - c0 - 16), nx);
+            const int cnt = min(16, p_hi - c0);
+            float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.f;
-          for (int src = 0; src < ksn; ++src) {
-            const float* rp = recv + (size_t)(src * slice + c0) * 128 + f;
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            const float* rp = recv + (size_t)c0 * 128 + f;
+            const size_t sstride = (size_t)slice * 128;
+#pragma unroll 1
+            for (int src = 0; src < ksn; src += 2) {
+              float x[2][16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < p_hi) v[j] += rp[j * 128];
+              for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[u][j] = (src + u < ksn && j < cnt) ? rp[(src + u) * sstride + j * 128] : 0.f;
+#pragma unroll
+              for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += x[u][j];
+            }
+            emit16<MODE>(E, n, q, lane, c0, t0 + e_lo + c0, v, cnt, cf, gt, sc, cur);
           }
-          emit16<MODE>(E, n, q, lane, c0, t0 + e_lo + c0, v, min(16, p_hi - c0), cf, gt, sc, cur);
+          return;
+        }
+#pragma unroll 1
+        for (int c0 = p_lo; c0 < p_hi; c0 += 4) {
+          float2 cur[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            cur[j] = aux0[j];
+            aux0[j] = aux1[j];
+          }
+          if (c0 + 8 < p_hi) pre4<MODE>(E, n, t0 + e_lo + c0 + 8, min(4, p_hi - c0 - 8), aux1);
+          const int cnt = min(4, p_hi - c0);
+          float v[4] = {0.f, 0.f, 0.f, 0.f};
+          const float* rp = recv + (size_t)c0 * 128 + f;
+          const size_t sstride = (size_t)slice * 128;
+          int src = 0;
+          for (; src + 4 <= ksn; src += 4) {  // four ranks' loads in flight, added in rank order
+            float x[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) x[u][j] = j < cnt ? rp[(src + u) * sstride + j * 128] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] += x[u][j];
+          }
+          for (; src < ksn; ++src)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] += j < cnt ? rp[src * sstride + j * 128] : 0.f;
+          emit4<MODE>(E, n, q, lane, c0, t0 + e_lo + c0, v, cnt, cf, gt, sc, cur);
         }
       };
       if (E.mode == kEQkvRope) run(std::integral_constant<int, kEQkvRope>());
