@@ -116,6 +116,7 @@ struct Epi {
   const float* gate;
   const float* scale_next;
   bf16* a_out;
+  uint64_t keep;   // L2 evict-last policy for the RoPE table and the residual stream
   float* red;      // shared [4][TT]
   const float* rn; // shared, per emitted token
 };
@@ -130,10 +131,10 @@ __device__ __forceinline__ void pre4(const Epi& E, int n, int tok0, int cnt, flo
     const bool rot = hb < E.n_rot_heads;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      aux[j] = (rot && j < cnt) ? __ldg(E.rope_cs + (size_t)(tok0 + j) * E.half + pair) : make_float2(1.f, 0.f);
+      aux[j] = (rot && j < cnt) ? ld_keep_f2(E.rope_cs + (size_t)(tok0 + j) * E.half + pair, E.keep) : make_float2(1.f, 0.f);
   } else if (MODE == kEResid) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) aux[j].x = j < cnt ? E.h[(size_t)(tok0 + j) * E.N + n] : 0.f;
+    for (int j = 0; j < 4; ++j) aux[j].x = j < cnt ? ld_keep_f32(E.h + (size_t)(tok0 + j) * E.N + n, E.keep) : 0.f;
   }
 }
 
@@ -216,10 +217,10 @@ __device__ __forceinline__ void pre16(const Epi& E, int n, int tok0, int cnt, fl
     const bool rot = hb < E.n_rot_heads;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      aux[j] = (rot && j < cnt) ? __ldg(E.rope_cs + (size_t)(tok0 + j) * E.half + pair) : make_float2(1.f, 0.f);
+      aux[j] = (rot && j < cnt) ? ld_keep_f2(E.rope_cs + (size_t)(tok0 + j) * E.half + pair, E.keep) : make_float2(1.f, 0.f);
   } else if (MODE == kEResid) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) aux[j].x = j < cnt ? E.h[(size_t)(tok0 + j) * E.N + n] : 0.f;
+    for (int j = 0; j < 16; ++j) aux[j].x = j < cnt ? ld_keep_f32(E.h + (size_t)(tok0 + j) * E.N + n, E.keep) : 0.f;
   }
 }
 
@@ -418,6 +419,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   E.a_out = a.a_out;
   E.red = red_s;
   E.rn = rn_s;
+  E.keep = policy_evict_last();
   float* const ss_out = a.ss_out;
   int* const status = a.status;
   float cf = 0.f, gt = 0.f, sc = 0.f;
