@@ -322,7 +322,10 @@ __device__ __forceinline__ void emit16(const Epi& E, int n, int q, int lane, int
   }
 }
 
-template <int EW>
+// One instantiation per epilogue MODE and split-K exchange XP (0 unsplit,
+// 1 bulk copies, 2 per-thread remote stores): each launch carries only the
+// code it runs, which at batch 1 runs once per CTA from a cold instruction cache.
+template <int EW, int MODE, int XP>
 __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
               const __grid_constant__ TcGemmArgs a) {
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     mbar_init(tmem_full, 1);
     mbar_init(recv_bar, 1);
     // bulk exchange: every rank sends this rank its partials of our run
-    if (ksn > 1 && a.xbulk) mbar_arrive_expect_tx(recv_bar, (uint32_t)(ksn * (e_hi - e_lo) * 512));
+    if (XP == 1) mbar_arrive_expect_tx(recv_bar, (uint32_t)(ksn * (e_hi - e_lo) * 512));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -389,8 +392,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   __syncthreads();
   tc_fence_after();
   // peers may write into this CTA once its receive barrier is initialised
-  const bool xbulk = a.xbulk != 0;
-  if (ksn > 1) cluster_arrive();
+  if constexpr (XP != 0) cluster_arrive();
   const uint32_t tmem_d = *tmem_base_p;
   bool go = false;
   // epilogue role (warps 2..): TMEM lane quarter, column half, feature row
@@ -496,7 +498,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     const int e = warp - 2;
     const int et = threadIdx.x - 64;
     // per-feature constants come from the time table (ready before this kernel)
-    if (E.mode == kEResid) {
+    if constexpr (MODE == kEResid) {
       gt = E.gate[n];
       if (E.scale_next != nullptr) sc = E.scale_next[n];
     } else {
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     }
     pdl_wait();
     // reciprocal RMS of the emitted tokens, while the mainloop runs
-    if (E.mode != kEResid)
+    if constexpr (MODE != kEResid)
       for (int i = et; i < e_hi - e_lo; i += kEpiThreads) {
         const int tok = t0 + e_lo + i;
         float ss = 0.f;
@@ -513,11 +515,11 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       }
     // the first two groups' per-token inputs, issued before the accumulator is ready
     {
-      const int lo = ksn == 1 ? c_lo : e_lo + p_lo, hi = ksn == 1 ? c_hi : e_lo + p_hi;
-      if (E.mode == kEQkvRope) {
+      const int lo = XP == 0 ? c_lo : e_lo + p_lo, hi = XP == 0 ? c_hi : e_lo + p_hi;
+      if constexpr (MODE == kEQkvRope) {
         if (lo < hi) pre4<kEQkvRope>(E, n, t0 + lo, min(4, hi - lo), aux0);
         if (lo + 4 < hi) pre4<kEQkvRope>(E, n, t0 + lo + 4, min(4, hi - lo - 4), aux1);
-      } else if (E.mode == kEResid) {
+      } else if constexpr (MODE == kEResid) {
         if (lo < hi) pre4<kEResid>(E, n, t0 + lo, min(4, hi - lo), aux0);
         if (lo + 4 < hi) pre4<kEResid>(E, n, t0 + lo + 4, min(4, hi - lo - 4), aux1);
       }
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     for (int i = 0; i < kEpiWarps; ++i) go = go && votes[i];
     if (go) {
       tc_fence_after();
-      if (ksn == 1) {
+      if constexpr (XP == 0) {
         // unsplit: the accumulator is the sum; emit straight from TMEM, 4 tokens a step
         auto run = [&](auto mode_tag) {
           constexpr int MODE = decltype(mode_tag)::value;
@@ -563,10 +565,8 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
             emit4<MODE>(E, n, q, lane, c0, t0 + c0, v, min(4, c_hi - c0), cf, gt, sc, cur);
           }
         };
-        if (E.mode == kEQkvRope) run(std::integral_constant<int, kEQkvRope>());
-        else if (E.mode == kEGeglu) run(std::integral_constant<int, kEGeglu>());
-        else run(std::integral_constant<int, kEResid>());
-      } else if (xbulk) {
+        run(std::integral_constant<int, MODE>());
+      } else if constexpr (XP == 1) {
         // split K: stage this partial token-major in the drained pipeline
         // buffers, then send each rank its run of tokens with one bulk copy
         float* stg = reinterpret_cast<float*>(smem);
@@ -580,9 +580,9 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         fence_proxy_async_smem();
       }
     }
-    if (ksn > 1) {
+    if constexpr (XP != 0) {
       cluster_wait();  // every rank of the cluster has started and initialised its barrier
-      if (xbulk) {
+      if constexpr (XP == 1) {
         named_bar<1>(kEpiThreads);
         if (go && threadIdx.x == 64) {
           const uint32_t stg_u = smem_u32(smem);
@@ -618,17 +618,17 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   }
   if (warp < 2) {
     __syncwarp();
-    if (ksn > 1) {
+    if constexpr (XP != 0) {
       cluster_wait();
-      if (!xbulk) {
+      if constexpr (XP == 2) {
         cluster_arrive();
         cluster_wait();
       }
     }
   }
-  if (ksn > 1) {
-    if (warp >= 2 && !xbulk) cluster_wait();  // every rank's partials have been written
-    if (warp >= 2 && go && xbulk) {
+  if constexpr (XP != 0) {
+    if (XP == 2 && warp >= 2) cluster_wait();  // every rank's partials have been written
+    if (XP == 1 && warp >= 2 && go) {
       // this rank's run from every rank (bounded wait)
       int ok = 1;
       if (lane == 0) ok = mbar_wait(recv_bar, 0, abort_flag, status) ? 1 : 0;
@@ -702,12 +702,10 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
           emit4<MODE>(E, n, q, lane, c0, t0 + e_lo + c0, v, cnt, cf, gt, sc, cur);
         }
       };
-      if (E.mode == kEQkvRope) run(std::integral_constant<int, kEQkvRope>());
-      else if (E.mode == kEGeglu) run(std::integral_constant<int, kEGeglu>());
-      else run(std::integral_constant<int, kEResid>());
+      run(std::integral_constant<int, MODE>());
     }
   }
-  if (E.mode == kEResid && warp >= 2) {
+  if (MODE == kEResid && warp >= 2) {
     // per-token sum of h^2 over the tile's 128 features (four lane quarters, in order)
     named_bar<2>(kEpiThreads);
     if (go && ss_out != nullptr)
@@ -716,7 +714,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
             (red_s[i] + red_s[TT + i]) + (red_s[2 * TT + i] + red_s[3 * TT + i]);
   }
   // the bulk copies out of the staging must have read it before the CTA exits
-  if (ksn > 1 && xbulk && threadIdx.x == 64) bulk_wait_read_all();
+  if (XP == 1 && threadIdx.x == 64) bulk_wait_read_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -918,8 +916,8 @@ int max_active_clusters(int ew, int ks, size_t smem) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  const cudaError_t e = ew == 8 ? cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<8>, &cfg)
-                                : cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<4>, &cfg);
+  const cudaError_t e = ew == 8 ? cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<8, kEResid, 2>, &cfg)
+                                : cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<4, kEResid, 2>, &cfg);
   if (e != cudaSuccess) {
     cudaGetLastError();
     n = 0;
@@ -971,6 +969,27 @@ GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split) {
   return p;
 }
 
+// Every instantiation of k_tc_gemm, in the order of gemm_kernel(ew, mode, xp).
+template <typename F>
+void for_each_gemm(F&& f) {
+  f(k_tc_gemm<4, kEQkvRope, 0>); f(k_tc_gemm<4, kEQkvRope, 1>); f(k_tc_gemm<4, kEQkvRope, 2>);
+  f(k_tc_gemm<4, kEGeglu, 0>); f(k_tc_gemm<4, kEGeglu, 1>); f(k_tc_gemm<4, kEGeglu, 2>);
+  f(k_tc_gemm<4, kEResid, 0>); f(k_tc_gemm<4, kEResid, 1>); f(k_tc_gemm<4, kEResid, 2>);
+  f(k_tc_gemm<8, kEQkvRope, 0>); f(k_tc_gemm<8, kEQkvRope, 1>); f(k_tc_gemm<8, kEQkvRope, 2>);
+  f(k_tc_gemm<8, kEGeglu, 0>); f(k_tc_gemm<8, kEGeglu, 1>); f(k_tc_gemm<8, kEGeglu, 2>);
+  f(k_tc_gemm<8, kEResid, 0>); f(k_tc_gemm<8, kEResid, 1>); f(k_tc_gemm<8, kEResid, 2>);
+}
+
+typedef void (*GemmKernel)(const CUtensorMap, const CUtensorMap, const TcGemmArgs);
+
+GemmKernel gemm_kernel(int ew, int mode, int xp) {
+  GemmKernel table[18];
+  int i = 0;
+  for_each_gemm([&](auto kern) { table[i++] = kern; });
+  const int m = mode == kEQkvRope ? 0 : (mode == kEGeglu ? 1 : 2);
+  return table[(ew == 8 ? 9 : 0) + 3 * m + xp];
+}
+
 cudaError_t gemm_kernel_setup() {
   cudaError_t e = cudaSuccess;
   auto attrs = [&](auto kern) {
@@ -980,8 +999,7 @@ cudaError_t gemm_kernel_setup() {
                                (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   };
-  attrs(k_tc_gemm<4>);
-  attrs(k_tc_gemm<8>);
+  for_each_gemm([&](auto kern) { attrs(kern); });
   // every kernel of the bf16 path asks for the same (maximum) shared-memory
   // carve-out, so consecutive kernels never make an SM re-partition L1/shared
   if (e == cudaSuccess)
@@ -1025,8 +1043,8 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  if (ew == 8) return cudaLaunchKernelEx(&cfg, k_tc_gemm<8>, wmap, amap, a);
-  return cudaLaunchKernelEx(&cfg, k_tc_gemm<4>, wmap, amap, a);
+  const int xp = p.ksplit == 1 ? 0 : (p.xbulk ? 1 : 2);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel(ew, a.e_mode, xp), wmap, amap, a);
 }
 
 cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
