@@ -26,6 +26,9 @@
 // combine kernel merges the ranges of a row in range order (deterministic) and
 // writes the bf16 attention output o[token][head * dh + d].
 #include <math.h>
+#include <string.h>
+
+#include <type_traits>
 
 #include "ae_internal.h"
 #include "ae_tc.cuh"
@@ -41,6 +44,14 @@ constexpr float kRescaleMargin = 8.f;  // raise the exponent reference only past
 constexpr int kSkip = -0x40000000;     // gather code: zero-fill
 
 __host__ __device__ inline int fold_rows_per_head(int H) { return (H + 15) & ~15; }
+
+// Two floats rounded to bf16 and packed (first in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
 
 struct AttnSmem {
   uint32_t q, k[2], v[2], p, bars, idx, total;  // byte offsets from the 1024-aligned base
@@ -167,7 +178,9 @@ __device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorM
   return tma;
 }
 
-template <int DH>
+// O16: partials stored as bf16 rows of O / l (else fp32 O); one instantiation
+// each, so a launch carries only the store it runs.
+template <int DH, bool O16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -392,15 +405,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;
     uint8_t* stg = smem + L.k[0];
 #pragma unroll 1
-    for (int c0 = 0; c0 < dh; c0 += 64) {
-      float v[64];
-      tmem_ld64(tm_o + lane_off + (uint32_t)c0, v);
+    if constexpr (O16) {
+      // bf16 rows of O / l (half the bytes of fp32 partials): boxes of 64 columns
+      const float inv_l = 1.f / l;
+#pragma unroll 1
+      for (int c0 = 0; c0 < dh; c0 += 64) {
+        float v[64];
+        tmem_ld64(tm_o + lane_off + (uint32_t)c0, v);
+        uint8_t* box = stg + (c0 >> 6) * (128 * 128);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {  // 16 float4 = two 32-column boxes
-        const int col = c0 + 4 * q;
-        uint8_t* box = stg + (col >> 5) * (128 * 128);
-        *reinterpret_cast<float4*>(box + sw128_offset(row, (col & 31) >> 2)) =
-            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(box + sw128_offset(row, q)) =
+              make_uint4(pack_bf16x2(v[8 * q] * inv_l, v[8 * q + 1] * inv_l),
+                         pack_bf16x2(v[8 * q + 2] * inv_l, v[8 * q + 3] * inv_l),
+                         pack_bf16x2(v[8 * q + 4] * inv_l, v[8 * q + 5] * inv_l),
+                         pack_bf16x2(v[8 * q + 6] * inv_l, v[8 * q + 7] * inv_l));
+      }
+    } else {
+#pragma unroll 1
+      for (int c0 = 0; c0 < dh; c0 += 64) {
+        float v[64];
+        tmem_ld64(tm_o + lane_off + (uint32_t)c0, v);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {  // 16 float4 = two 32-column boxes
+          const int col = c0 + 4 * q;
+          uint8_t* box = stg + (col >> 5) * (128 * 128);
+          *reinterpret_cast<float4*>(box + sw128_offset(row, (col & 31) >> 2)) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
       }
     }
     // the stored maximum is in the log2 domain of the scaled scores
@@ -408,8 +440,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0) {
-      for (int bx = 0; bx < dh / 32; ++bx)
-        tma_store_2d(&omap, stg + bx * (128 * 128), bx * 32, (int)(unit * 128));
+      if constexpr (O16)
+        for (int bx = 0; bx < dh / 64; ++bx) tma_store_2d(&omap, stg + bx * (128 * 128), bx * 64, (int)(unit * 128));
+      else
+        for (int bx = 0; bx < dh / 32; ++bx) tma_store_2d(&omap, stg + bx * (128 * 128), bx * 32, (int)(unit * 128));
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -855,6 +889,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 
 // Merge the chunk ranges of every query row in range order; write bf16
 // o[token][head * dh + d].  Block = one (head, token) of a request, dh threads.
+template <bool O16>
 __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
   pdl_trigger();
   pdl_wait();
@@ -878,7 +913,13 @@ __global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
     for (int j = 0; j < 16; ++j) {
       const bool in = s0 + j < n_splits;
       ml[j] = in ? __ldcg(a.part_ml + (unit0 + s0 + j) * 128 + row) : make_float2(-INFINITY, 0.f);
-      pv[j] = in ? __ldcg(a.part_o + ((unit0 + s0 + j) * 128 + row) * a.dh + d) : 0.f;
+      const size_t at = ((unit0 + s0 + j) * 128 + row) * a.dh + d;
+      if constexpr (O16)  // rows of O / l: weight l back in
+        pv[j] = in ? __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(a.part_o) + at) << 16) *
+                         ml[j].y
+                   : 0.f;
+      else
+        pv[j] = in ? __ldcg(a.part_o + at) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -931,10 +972,12 @@ size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int 
 
 template <int DH>
 cudaError_t attn_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_attn_tc<DH>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = cudaSuccess;
+  for (auto kern : {k_attn_tc<DH, false>, k_attn_tc<DH, true>}) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  }
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_pipe<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_attn_pipe<DH>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -946,16 +989,20 @@ cudaError_t attn_kernel_setup() {
   cudaError_t e = attn_attrs<64>();
   if (e == cudaSuccess) e = attn_attrs<128>();
   if (e == cudaSuccess) e = attn_attrs<256>();
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_attn_combine, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+  for (auto kern : {k_attn_combine<false>, k_attn_combine<true>})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
 cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const CUtensorMap& omap, AttnArgs a, bf16* o, int sm_count,
+                           const CUtensorMap& omap_f32, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl) {
   attn_plan(a, sm_count);
+  // bf16 rows of O / l halve the partials' bytes; measured faster where each
+  // CTA covers several chunks, slower for many one-chunk partials (batch 1)
+  a.o16 = (omap16 != nullptr && a.chunks_per_cta > 1) ? 1 : 0;
+  const CUtensorMap& omap = a.o16 ? *omap16 : omap_f32;
   const unsigned grid = (unsigned)(a.batch * a.Hkv * a.q_tiles * a.max_splits);
   cudaError_t e;
   if (a.pipe && a.chunks_per_cta <= kPipeMaxChunks) {
@@ -966,16 +1013,21 @@ cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, con
       default: e = launch_k(k_attn_pipe<256>, dim3(grid), dim3(kPipeThreads), ps, s, pdl, qmap, kmap, vmap, omap, a); break;
     }
     if (e != cudaSuccess) return e;
-    return launch_k(k_attn_combine, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
+    return launch_k(k_attn_combine<false>, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
   }
   const size_t smem = attn_smem_bytes(a.dh);
-  switch (a.dh) {
-    case 64: e = launch_k(k_attn_tc<64>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
-    case 128: e = launch_k(k_attn_tc<128>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
-    default: e = launch_k(k_attn_tc<256>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
-  }
-  if (e != cudaSuccess) return e;
-  return launch_k(k_attn_combine, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
+  auto go = [&](auto o16_tag) {
+    constexpr bool O16 = decltype(o16_tag)::value;
+    cudaError_t r;
+    switch (a.dh) {
+      case 64: r = launch_k(k_attn_tc<64, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
+      case 128: r = launch_k(k_attn_tc<128, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
+      default: r = launch_k(k_attn_tc<256, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
+    }
+    if (r != cudaSuccess) return r;
+    return launch_k(k_attn_combine<O16>, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
+  };
+  return a.o16 ? go(std::true_type()) : go(std::false_type());
 }
 
 }  // namespace ae

@@ -93,7 +93,8 @@ cudaError_t fast_setup(ae_ctx* c) {
   c->q_box_rows = hp % 64 == 0 ? 64 : (hp % 32 == 0 ? 32 : 16);
   if ((e = make_map(&c->map_qtile, c->qkv, maxM, d.qkvdim(), c->q_box_rows)) != cudaSuccess) return e;
   const size_t units = attn_part_units(c->max_batch, d.H, d.Hq, d.Hkv, c->max_rows, c->sm_count);
-  return make_attn_o_map(&c->map_attn_o, c->attn_o, units, d.dh);
+  if ((e = make_attn_o_map(&c->map_attn_o, c->attn_o, units, d.dh)) != cudaSuccess) return e;
+  return make_attn_o16_map(&c->map_attn_o16, c->attn_o, units, d.dh);
 }
 
 cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows) {
@@ -124,6 +125,10 @@ cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int d
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_attn_o16_map(CUtensorMap* map, float* part_o, size_t units, int dh) {
+  return make_map(map, part_o, (long)(units * 128), dh, 128);
 }
 
 cudaError_t fast_activation_maps(ae_ctx* c, int box_rows) {
@@ -233,8 +238,12 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.status = c->status_dev;
       at.pipe = c->attn_pipe ? 1 : 0;
       at.q_box = c->q_box_rows;
+      // bf16 partials may be chosen on the default path; the pipelined kernel
+      // and callers' own scratch keep fp32
+      const bool o16_ok = attn_scratch == nullptr && !c->attn_pipe;
       ck(launch_attn_tc(c->map_qtile, c->bind.map_pk, c->bind.map_pv,
-                        attn_scratch ? attn_scratch->omap : c->map_attn_o, at, o, sm, s, pdl));
+                        attn_scratch ? attn_scratch->omap : c->map_attn_o, o16_ok ? &c->map_attn_o16 : nullptr, at, o,
+                        sm, s, pdl));
       n += 2;
     }
 

@@ -112,6 +112,7 @@ struct ae_ctx {
   CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
   CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
   CUtensorMap map_attn_o;                       // attention O partials (fp32)
+  CUtensorMap map_attn_o16;                     // the same buffer as bf16 partials of O / l
   CUtensorMap map_qkv_act;                      // q|k|v activations, boxes 16 rows x 64
   CUtensorMap map_qtile;                        // the same, boxes q_box_rows rows x 64 (attention query tiles)
   int q_box_rows = 16;
@@ -256,8 +257,9 @@ struct AttnArgs {
   int max_units;          // cap on work units (0: none), for fixed-size scratch
   int pipe;               // use the pipelined eight-warp kernel when the plan allows it
   int q_box;              // rows of a query-tile TMA box (64, 32 or 16; divides the padded head length)
-  float* part_o;          // [units][128][dh]
+  float* part_o;          // [units][128][dh] fp32 O, or (o16) bf16 O / l
   float2* part_ml;        // [units][128]
+  int o16;                // partials stored as bf16 rows of O / l (omap: bf16 boxes of 128 rows x 64)
   int* status;
 };
 size_t attn_part_units(int max_batch, int H, int Hq, int Hkv, int max_rows, int sm_count);
@@ -268,13 +270,17 @@ cudaError_t attn_kernel_setup();
 // qmap: bf16 [maxM, (Hq + 2 Hkv) dh] view of the q|k|v activations, boxes a.q_box rows x 64.
 // kmap, vmap: bf16 [L * total_rows, Hkv dh] views of the bound prefix K / V, boxes 64 rows x 64.
 // omap: fp32 [units * 128, dh] view of part_o, boxes of 128 rows x 32 columns, 128-byte swizzle.
+// omap16: bf16 view of the same partials (make_attn_o16_map), or nullptr; used
+// when every CTA merges more than one chunk (fewer, longer partials).
 cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const CUtensorMap& omap, AttnArgs a, bf16* o, int sm_count,
+                           const CUtensorMap& omap, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl);
 cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows);
 // fp32 [d2][d1][d0] view with boxes {32, box1, 1}, 128-byte swizzle (split-K partials)
 cudaError_t make_f32_3d_map(CUtensorMap* map, const void* ptr, long d0, long d1, long d2, int box1);
 cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int dh);
+// bf16 [units * 128, dh] view of part_o, boxes of 128 rows x 64 columns, 128-byte swizzle
+cudaError_t make_attn_o16_map(CUtensorMap* map, float* part_o, size_t units, int dh);
 
 // ---- bf16 path driver (ae_fast.cu)
 bool fast_path_supported(const Dims& d, std::string* why);
