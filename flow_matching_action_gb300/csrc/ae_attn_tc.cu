@@ -999,9 +999,8 @@ cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, con
                            const CUtensorMap& omap_f32, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl) {
   attn_plan(a, sm_count);
-  // bf16 rows of O / l halve the partials' bytes; measured faster where each
-  // CTA covers several chunks, slower for many one-chunk partials (batch 1)
-  a.o16 = (omap16 != nullptr && a.chunks_per_cta > 1) ? 1 : 0;
+  // bf16 rows of O / l halve the partials' bytes (store and combine)
+  a.o16 = omap16 != nullptr ? 1 : 0;
   const CUtensorMap& omap = a.o16 ? *omap16 : omap_f32;
   const unsigned grid = (unsigned)(a.batch * a.Hkv * a.q_tiles * a.max_splits);
   cudaError_t e;

@@ -270,8 +270,8 @@ cudaError_t attn_kernel_setup();
 // qmap: bf16 [maxM, (Hq + 2 Hkv) dh] view of the q|k|v activations, boxes a.q_box rows x 64.
 // kmap, vmap: bf16 [L * total_rows, Hkv dh] views of the bound prefix K / V, boxes 64 rows x 64.
 // omap: fp32 [units * 128, dh] view of part_o, boxes of 128 rows x 32 columns, 128-byte swizzle.
-// omap16: bf16 view of the same partials (make_attn_o16_map), or nullptr; used
-// when every CTA merges more than one chunk (fewer, longer partials).
+// omap16: bf16 view of the same partials (make_attn_o16_map), or nullptr (fp32
+// partials through omap).
 cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& omap, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl);
