@@ -888,51 +888,76 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 }
 
 // Merge the chunk ranges of every query row in range order; write bf16
-// o[token][head * dh + d].  Block = one (head, token) of a request, dh threads.
+// o[token][head * dh + d].  One warp per (head, token) row, 8 rows per block;
+// lane l merges dims 8l.. (16-byte loads and stores), all ranges' loads issued
+// together, merged with an online rescale (deterministic order).
+constexpr int kCombineRows = 8;
+
 template <bool O16>
-__global__ void k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
+__global__ void __launch_bounds__(32 * kCombineRows) k_attn_combine(const AttnArgs a, bf16* __restrict__ o) {
   pdl_trigger();
   pdl_wait();
   const int G = a.Hq / a.Hkv;
   const int Hp = fold_rows_per_head(a.H);
-  const int g = blockIdx.x / (G * a.H), hr = blockIdx.x % (G * a.H), b = blockIdx.y;
-  const int hh = hr / a.H, tok = hr % a.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ri = blockIdx.x * kCombineRows + warp;  // row over (request, KV head, head in group, token)
+  if (ri >= a.batch * a.Hq * a.H) return;
+  const int per_b = a.Hq * a.H;
+  const int b = ri / per_b, hr0 = ri - b * per_b;
+  const int g = hr0 / (G * a.H), hr = hr0 - g * (G * a.H);
+  const int hh = hr / a.H, tok = hr - hh * a.H;
   const int r = hh * Hp + tok;  // folded row
   const int qt = r / 128, row = r % 128;
   const int n_chunks = (a.n_valid[b] + a.H + kChunk - 1) / kChunk;
   const int n_splits = (n_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
-  const int d = threadIdx.x;
   const size_t unit0 = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits;
-  // one pass: the loads of up to 16 ranges are issued together, then merged
-  // in range order with an online rescale (deterministic)
-  float m = -INFINITY, l = 0.f, acc = 0.f;
-  for (int s0 = 0; s0 < n_splits; s0 += 16) {
-    float2 ml[16];
-    float pv[16];
+  bf16* orow = o + (size_t)(b * a.H + tok) * (a.Hq * a.dh) + (g * G + hh) * a.dh;
+  for (int d0 = 8 * lane; d0 < a.dh; d0 += 256) {
+    float m = -INFINITY, l = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < n_splits; s0 += 8) {
+      float2 ml[8];
+      float pv[8][8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const bool in = s0 + j < n_splits;
-      ml[j] = in ? __ldcg(a.part_ml + (unit0 + s0 + j) * 128 + row) : make_float2(-INFINITY, 0.f);
-      const size_t at = ((unit0 + s0 + j) * 128 + row) * a.dh + d;
-      if constexpr (O16)  // rows of O / l: weight l back in
-        pv[j] = in ? __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(a.part_o) + at) << 16) *
-                         ml[j].y
-                   : 0.f;
-      else
-        pv[j] = in ? __ldcg(a.part_o + at) : 0.f;
-    }
+      for (int j = 0; j < 8; ++j) {
+        const bool in = s0 + j < n_splits;
+        const size_t rw = (unit0 + s0 + j) * 128 + row;
+        ml[j] = in ? __ldcg(a.part_ml + rw) : make_float2(-INFINITY, 0.f);
+        if constexpr (O16) {  // rows of O / l: weight l back in below
+          const uint4 q = in ? __ldcg(reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(a.part_o) +
+                                                                      rw * a.dh + d0))
+                             : make_uint4(0u, 0u, 0u, 0u);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (s0 + j >= n_splits) break;
-      const float mn = fmaxf(m, ml[j].x);
-      const float ra = ex2_fast(m - mn), rb = ex2_fast(ml[j].x - mn);
-      l = l * ra + ml[j].y * rb;
-      acc = acc * ra + pv[j] * rb;
-      m = mn;
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            pv[j][2 * i] = f.x;
+            pv[j][2 * i + 1] = f.y;
+          }
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(a.part_o + rw * a.dh + d0);
+          const float4 x0 = in ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 x1 = in ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+          pv[j][0] = x0.x; pv[j][1] = x0.y; pv[j][2] = x0.z; pv[j][3] = x0.w;
+          pv[j][4] = x1.x; pv[j][5] = x1.y; pv[j][6] = x1.z; pv[j][7] = x1.w;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j >= n_splits) break;
+        const float mn = fmaxf(m, ml[j].x);
+        const float ra = ex2_fast(m - mn), rb = ex2_fast(ml[j].x - mn);
+        const float wv = O16 ? ml[j].y * rb : rb;  // weight of this range's values
+        l = l * ra + ml[j].y * rb;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = acc[i] * ra + pv[j][i] * wv;
+        m = mn;
+      }
     }
+    const float il = 1.f / l;
+    *reinterpret_cast<uint4*>(orow + d0) =
+        make_uint4(pack_bf16x2(acc[0] * il, acc[1] * il), pack_bf16x2(acc[2] * il, acc[3] * il),
+                   pack_bf16x2(acc[4] * il, acc[5] * il), pack_bf16x2(acc[6] * il, acc[7] * il));
   }
-  const int h = g * G + hh;
-  o[(size_t)(b * a.H + tok) * (a.Hq * a.dh) + h * a.dh + d] = __float2bfloat16_rn(acc / l);
 }
 
 }  // namespace
@@ -995,6 +1020,10 @@ cudaError_t attn_kernel_setup() {
   return e;
 }
 
+static unsigned combine_blocks(const AttnArgs& a) {
+  return (unsigned)((a.batch * a.Hq * a.H + kCombineRows - 1) / kCombineRows);
+}
+
 cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& omap_f32, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl) {
@@ -1012,7 +1041,7 @@ cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, con
       default: e = launch_k(k_attn_pipe<256>, dim3(grid), dim3(kPipeThreads), ps, s, pdl, qmap, kmap, vmap, omap, a); break;
     }
     if (e != cudaSuccess) return e;
-    return launch_k(k_attn_combine<false>, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
+    return launch_k(k_attn_combine<false>, dim3(combine_blocks(a)), dim3(32 * kCombineRows), 0, s, pdl, a, o);
   }
   const size_t smem = attn_smem_bytes(a.dh);
   auto go = [&](auto o16_tag) {
@@ -1024,7 +1053,7 @@ cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, con
       default: r = launch_k(k_attn_tc<256, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
     }
     if (r != cudaSuccess) return r;
-    return launch_k(k_attn_combine<O16>, dim3(a.Hq * a.H, a.batch), dim3(a.dh), 0, s, pdl, a, o);
+    return launch_k(k_attn_combine<O16>, dim3(combine_blocks(a)), dim3(32 * kCombineRows), 0, s, pdl, a, o);
   };
   return a.o16 ? go(std::true_type()) : go(std::false_type());
 }
