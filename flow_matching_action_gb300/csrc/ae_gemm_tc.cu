@@ -535,6 +535,37 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         // unsplit: the accumulator is the sum; emit straight from TMEM, 4 tokens a step
         auto run = [&](auto mode_tag) {
           constexpr int MODE = decltype(mode_tag)::value;
+          if constexpr (MODE == kEQkvRope) {
+            // Long tiles of a rotated head: the tile's slice of the RoPE table
+            // (tokens x its 64 pairs, 512 bytes a token) is copied once into
+            // the drained pipeline buffers, every thread's 16-byte pieces in
+            // flight together, instead of one round trip per 16-token chunk.
+            const int hb0 = (n_tile * 128) / E.dh;
+            const bool stage = E.dh >= 128 && hb0 < E.n_rot_heads && nv >= 64 &&
+                               (size_t)TT * 512 <= (size_t)S * (kATileBytes + (size_t)btile);
+            if (stage) {
+              float2* cs_s = reinterpret_cast<float2*>(smem);
+              const int pair0 = (n_tile * 128 - hb0 * E.dh) >> 1;
+              for (int i = threadIdx.x - 64; i < nv * 32; i += kEpiThreads) {
+                const int t = i >> 5, c = i & 31;
+                cp_async16(cs_s + t * 64 + 2 * c, E.rope_cs + (size_t)(t0 + t) * E.half + pair0 + 2 * c, 16);
+              }
+              cp_async_commit();
+              cp_async_wait<0>();
+              named_bar<1>(kEpiThreads);
+              const int pl = ((n - hb0 * E.dh) >> 1) - pair0;  // this thread's pair within the slice
+#pragma unroll 1
+              for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+                float2 cur[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) cur[j] = cs_s[(c0 + j) * 64 + pl];
+                float v[16];
+                tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+                emit16<MODE>(E, n, q, lane, c0, t0 + c0, v, min(16, c_hi - c0), cf, gt, sc, cur);
+              }
+              return;
+            }
+          }
           if (c_hi - c_lo >= 32) {
             // long run: 16 tokens a step, next chunk's inputs one step ahead
             float2 nx[16];
