@@ -968,9 +968,30 @@ size_t attn_smem_bytes(int dh) { return 1024 + attn_smem_layout(dh).total; }
 void attn_plan(AttnArgs& a, int sm_count) {
   a.q_tiles = ((a.Hq / a.Hkv) * fold_rows_per_head(a.H) + 127) / 128;
   const int max_chunks = (a.plan_rows + a.H + kChunk - 1) / kChunk;
-  const long est = (long)a.batch * a.Hkv * a.q_tiles * max_chunks;
-  int cpc = (int)((est + 2L * sm_count - 1) / (2L * sm_count));
-  if (cpc < 1) cpc = 1;
+  int cpc = 1;
+  if (a.host_cu != nullptr) {
+    // Chunk range per CTA that minimizes the makespan of whole waves of one
+    // CTA per SM, a CTA costing its chunks plus about two chunks of prologue
+    // and partial store (fit to GB300 measurements at batch 16), over the
+    // bound requests' physical lengths; ties keep the shorter range.
+    long best = -1;
+    for (int c = 1; c <= max_chunks; ++c) {
+      long ctas = 0;
+      for (int b = 0; b < a.batch; ++b) {
+        const int ch = (a.host_cu[b + 1] - a.host_cu[b] + a.H + kChunk - 1) / kChunk;
+        ctas += (long)a.Hkv * a.q_tiles * ((ch + c - 1) / c);
+      }
+      const long cost = ((ctas + sm_count - 1) / sm_count) * (c + 2);
+      if (best < 0 || cost < best) {
+        best = cost;
+        cpc = c;
+      }
+    }
+  } else {
+    const long est = (long)a.batch * a.Hkv * a.q_tiles * max_chunks;
+    cpc = (int)((est + 2L * sm_count - 1) / (2L * sm_count));
+    if (cpc < 1) cpc = 1;
+  }
   a.chunks_per_cta = cpc;
   a.max_splits = (max_chunks + cpc - 1) / cpc;
   // a fixed-size scratch: fewer, longer chunk ranges until the units fit

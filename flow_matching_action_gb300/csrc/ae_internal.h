@@ -250,6 +250,7 @@ struct AttnArgs {
   const int* n_valid;     // [batch]
   int max_rows;           // row stride of valid_idx
   int plan_rows;          // longest physical prefix of the bound requests (work split bound)
+  const int* host_cu;     // host copy of the binding's cu_lens (batch + 1), for the work split; may be null
   int layer_row0;         // first row of this layer in the prefix K/V maps
   int batch, H, Hq, Hkv, dh;
   float scale;
