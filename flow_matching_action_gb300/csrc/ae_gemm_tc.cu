@@ -602,11 +602,11 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         // buffers, then send each rank its run of tokens with one bulk copy
         float* stg = reinterpret_cast<float*>(smem);
 #pragma unroll 1
-        for (int c0 = c_lo; c0 < c_hi; c0 += 4) {
-          float v[4];
-          tmem_ld4(tmem_d + trow + (uint32_t)c0, v);
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+          float v[16];
+          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) stg[(c0 + j) * 128 + f] = v[j];
+          for (int j = 0; j < 16; ++j) stg[(c0 + j) * 128 + f] = v[j];
         }
         fence_proxy_async_smem();
       }
