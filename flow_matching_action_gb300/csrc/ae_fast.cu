@@ -131,15 +131,17 @@ cudaError_t make_attn_o16_map(CUtensorMap* map, float* part_o, size_t units, int
   return make_map(map, part_o, (long)(units * 128), dh, 128);
 }
 
-cudaError_t fast_activation_maps(ae_ctx* c, int box_rows) {
-  if (c->act_box_rows == box_rows) return cudaSuccess;
+cudaError_t fast_activation_maps(ae_ctx* c, int box_rows, int box_rows_q) {
+  if (c->act_box_rows == box_rows && c->act_box_rows_q == box_rows_q) return cudaSuccess;
   const Dims& d = c->d;
   const long maxM = (long)c->max_batch * d.H;
   cudaError_t e;
   if ((e = make_map(&c->map_y, c->y, maxM, d.D, box_rows)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_oact, c->o, maxM, d.qdim(), box_rows)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_mact, c->m, maxM, d.F, box_rows)) != cudaSuccess) return e;
+  if ((e = make_map(&c->map_yq, c->y, maxM, d.D, box_rows_q)) != cudaSuccess) return e;
   c->act_box_rows = box_rows;
+  c->act_box_rows_q = box_rows_q;
   return cudaSuccess;
 }
 
@@ -151,12 +153,13 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const int nqkv = d.qkvdim(), qd = d.qdim();
   const float eps = (float)d.eps;
   const int sm = c->sm_count;
-  const GemmPlan pq = plan_gemm_cl(nqkv, D, M, sm, c->ks_cap[0]);
+  const GemmPlan pq = plan_gemm_cl(nqkv, D, M, sm, c->ks_cap[0], true);
   const GemmPlan po = plan_gemm_cl(D, qd, M, sm, c->ks_cap[1]);
   const GemmPlan pg = plan_gemm_cl(2 * F, D, M, sm, c->ks_cap[2]);
   const GemmPlan pd = plan_gemm_cl(D, F, M, sm, c->ks_cap[3]);
-  // the four GEMMs share one token tiling (it depends on M only)
-  *err = fast_activation_maps(c, pq.tok_tile);
+  // the O, gate/up and down GEMMs share one token tiling (it depends on M
+  // only); the QKV GEMM may use more, shorter tiles through its own operand map
+  *err = fast_activation_maps(c, pg.tok_tile, pq.tok_tile);
   if (*err != cudaSuccess) return 0;
   bf16* qkv = (bf16*)c->qkv;
   bf16* o = (bf16*)c->o;
@@ -210,7 +213,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.e_mode = kEQkvRope;
     a.fold = fold(l);
     a.out_bf16 = qkv;
-    ck(launch_tc_gemm(c->map_qkv, c->map_y, pq, a, s, pdl));
+    ck(launch_tc_gemm(c->map_qkv, c->map_yq, pq, a, s, pdl));
     ++n;
 
     // attention over [valid prefix || actions]
@@ -314,7 +317,7 @@ cudaError_t sample_persistent(ae_ctx* c, const TimeTable& t, int n_steps, float*
       const int ks = (pl[i].kb_total + P.stages - 1) / P.stages;
       pl[i] = plan_gemm(pl[i].N, pl[i].K, M, sm, ks < 2 ? 2 : ks, ks < 2 ? 2 : ks);
     }
-  cudaError_t e = fast_activation_maps(c, TT);
+  cudaError_t e = fast_activation_maps(c, TT, TT);
   if (e != cudaSuccess) return e;
   P.w[0] = c->map_qkv;
   P.w[1] = c->map_o;

@@ -878,11 +878,11 @@ size_t tc_gemm_smem_bytes(int stages, int tok_tile) {
 }
 
 // Token tiling and pipeline depth shared by both planners.
-static void plan_tiles(GemmPlan& p, int N, int K, int M) {
+static void plan_tiles(GemmPlan& p, int N, int K, int M, int tok_tiles = 0) {
   p.N = N;
   p.K = K;
   p.n_tiles = N / 128;
-  p.tok_tiles = (M + 255) / 256;
+  p.tok_tiles = tok_tiles > 0 ? tok_tiles : (M + 255) / 256;
   if (p.tok_tiles < 1) p.tok_tiles = 1;
   int tt = (M + p.tok_tiles - 1) / p.tok_tiles;
   tt = ((tt + 15) / 16) * 16;
@@ -958,9 +958,20 @@ int max_active_clusters(int ew, int ks, size_t smem) {
 }
 }  // namespace
 
-GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split) {
+GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split, bool retile) {
   GemmPlan p;
   plan_tiles(p, N, K, M);
+  // An unsplit GEMM that leaves SMs idle spends them on more, shorter token
+  // tiles (down to 64 tokens) instead.
+  if (retile && sm_count / (p.n_tiles * p.tok_tiles) <= 1) {
+    int best = p.tok_tiles;
+    for (int t = p.tok_tiles + 1; p.n_tiles * t <= sm_count; ++t) {
+      const int tt = (((M + t - 1) / t + 15) / 16) * 16;
+      if (tt < 64) break;
+      best = t;
+    }
+    if (best != p.tok_tiles) plan_tiles(p, N, K, M, best);
+  }
   const int ew = p.tok_tile > 64 ? 8 : 4;
   const int base = p.n_tiles * p.tok_tiles;
   int ks = sm_count / base;

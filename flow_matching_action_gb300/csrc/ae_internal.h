@@ -111,12 +111,13 @@ struct ae_ctx {
   int ks_cap[4] = {0, 0, 0, 0};  // split-K caps of the QKV, O, gate/up, down GEMMs (0 = none)
   CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
   CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
+  CUtensorMap map_yq;                           // the QKV GEMM's operand, boxes act_box_rows_q x 64
   CUtensorMap map_attn_o;                       // attention O partials (fp32)
   CUtensorMap map_attn_o16;                     // the same buffer as bf16 partials of O / l
   CUtensorMap map_qkv_act;                      // q|k|v activations, boxes 16 rows x 64
   CUtensorMap map_qtile;                        // the same, boxes q_box_rows rows x 64 (attention query tiles)
   int q_box_rows = 16;
-  int act_box_rows = 0;
+  int act_box_rows = 0, act_box_rows_q = 0;
   float* sumsq = nullptr;    // [D/128][M] sums of h^2 per 128-feature tile (adaRMS folded into GEMMs)
   float* part = nullptr;     // split-K partials (persistent kernel)
   size_t part_floats = 0;
@@ -229,7 +230,9 @@ size_t tc_gemm_smem_bytes(int stages, int tok_tile);
 GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split = 0);
 // Split-K plan of k_tc_gemm: the splits of a tile form one cluster (<= 16 CTAs),
 // no more splits than keep every cluster of the launch resident at once.
-GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split = 0);
+// retile: an unsplit plan that leaves SMs idle may use more, shorter token
+// tiles (the operand's TMA box must then follow the plan's tok_tile).
+GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split = 0, bool retile = false);
 cudaError_t gemm_kernel_setup();
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
                            TcGemmArgs a, cudaStream_t s, bool pdl);
@@ -286,7 +289,8 @@ cudaError_t make_attn_o16_map(CUtensorMap* map, float* part_o, size_t units, int
 // ---- bf16 path driver (ae_fast.cu)
 bool fast_path_supported(const Dims& d, std::string* why);
 cudaError_t fast_setup(ae_ctx* c);  // tensor maps and scratch, after the weights are packed
-cudaError_t fast_activation_maps(ae_ctx* c, int box_rows);  // one box = one token tile
+// one box = one token tile: box_rows for the gate/up, O and down GEMMs, box_rows_q for QKV
+cudaError_t fast_activation_maps(ae_ctx* c, int box_rows, int box_rows_q);
 size_t fast_part_floats(const Dims& d, int max_batch, int sm_count);
 // Attention split-KV partials supplied by the caller instead of the context's.
 struct AttnScratch {
