@@ -159,7 +159,11 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const GemmPlan pd = plan_gemm_cl(D, F, M, sm, c->ks_cap[3]);
   // the O, gate/up and down GEMMs share one token tiling (it depends on M
   // only); the QKV GEMM may use more, shorter tiles through its own operand map
-  *err = fast_activation_maps(c, pg.tok_tile, pq.tok_tile);
+  // A single token tile loads only the M valid rows (the MMA still reads the
+  // whole tile; the rows past M hold stale data and feed columns never emitted).
+  const int box_m = pg.tok_tiles == 1 ? (M < pg.tok_tile ? M : pg.tok_tile) : pg.tok_tile;
+  const int box_q = pq.tok_tiles == 1 ? (M < pq.tok_tile ? M : pq.tok_tile) : pq.tok_tile;
+  *err = fast_activation_maps(c, box_m, box_q);
   if (*err != cudaSuccess) return 0;
   bf16* qkv = (bf16*)c->qkv;
   bf16* o = (bf16*)c->o;
@@ -191,6 +195,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.rope_cs = c->rope_cs;
     a.dh = d.dh;
     a.n_rot_heads = d.Hq + d.Hkv;
+    a.act_rows = box_m;
     return a;
   };
 
@@ -211,6 +216,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     // adaRMS1 (folded) -> merged QKV -> RoPE
     TcGemmArgs a = base_args(l * nqkv, ln * nqkv);
     a.e_mode = kEQkvRope;
+    a.act_rows = box_q;
     a.fold = fold(l);
     a.out_bf16 = qkv;
     ck(launch_tc_gemm(c->map_qkv, c->map_yq, pq, a, s, pdl));

@@ -445,7 +445,8 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       // moments later, so it keeps the normal policy
       const uint64_t pol_w = a.tok_tiles > 1 ? policy_evict_normal() : policy_evict_first();
       const int row = a.w_row0 + n_tile * 128;
-      const uint32_t bytes = kATileBytes + (uint32_t)btile;
+      // the token box may hold only the valid rows of a single short tile
+      const uint32_t bytes = kATileBytes + (uint32_t)(a.act_rows > 0 ? a.act_rows : TT) * 128u;
       // Weights do not depend on the previous kernel: fill the first stages and
       // start pulling this slab of the next layer into L2 before waiting on it.
       const int pre = n_it < S ? n_it : S;

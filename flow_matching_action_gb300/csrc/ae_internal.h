@@ -203,6 +203,7 @@ struct TcGemmArgs {
   int tok_tile, n_tiles, tok_tiles, ksplit, kb_total, stages, tmem_cols;
   int tok_half;         // first token column of the second epilogue half (multiple of 16)
   int xbulk;            // split K: partials sent by bulk copies (1) or per-thread remote stores (0)
+  int act_rows;         // rows of the operand map's token box (0: tok_tile); a single short tile loads only its valid rows
   int e_mode;           // kEQkvRope, kEGeglu or kEResid
   // kEQkvRope / kEGeglu: the operand is bf16(h * (1 + scale)); adaRMS is folded in
   const float* ss_in;   // [n_ss][M] sums of h^2 per 128 features of the operand's rows
