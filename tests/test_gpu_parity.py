@@ -128,6 +128,17 @@ def test_pi05_batched_ragged_sampled_requests(pi05_runner):
         assert np.abs(got[b] - alone[0]).max() <= BF16_ACT_TOL
 
 
+def test_pi05_batch_of_three_masked_and_ragged(pi05_runner):
+    """A batch between 1 and 16: 150 action tokens make one 160-token GEMM tile
+    (eight epilogue warps), one request has a masked camera slot, and the
+    lengths leave split-K token runs that end in partial 4-token groups."""
+    wl = synth.build_workload("pi05_b3", synth.PI05, 3,
+                              [[("v", 300)], [("v", 128), ("m", 256), ("v", 77)], [("v", 1100)]], seed=7)
+    got = pi05_runner.run(wl)
+    assert np.isfinite(got).all()
+    assert np.abs(got - oracle_actions(wl, weights("pi05"))).max() <= BF16_ACT_TOL
+
+
 def test_pi05_f32_debug_path_matches_oracle():
     """The same Pi0.5 weights, upcast exactly to fp32, through the fp32 path."""
     wl = synth.pi05_two_camera(n_steps=2)
