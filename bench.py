@@ -321,8 +321,34 @@ def peaks():
 
 
 # ----------------------------------------------------------------------------- main
+def _code_tokens(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and whitespace runs collapsed:
+    what the compiler sees, so that editing a comment leaves the digest alone."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, copied whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest() -> str:
-    """SHA-256 over the CUDA sources and the C header (what the kernels are built from)."""
+    """SHA-256 over the code of the CUDA sources and the C header (what the
+    kernels are built from), comments and whitespace aside."""
     import glob
     import hashlib
     root = os.path.dirname(os.path.abspath(__file__))
@@ -330,8 +356,8 @@ def source_digest() -> str:
     files = sorted(glob.glob(os.path.join(root, "flow_matching_action_gb300", "csrc", "*")))
     for p in files + [os.path.join(root, "include", "ae.h")]:
         h.update(os.path.basename(p).encode())
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8", errors="replace") as f:
+            h.update(_code_tokens(f.read()).encode())
     return h.hexdigest()
 
 

@@ -22,9 +22,11 @@
 //   O += P V       tcgen05, M = 128, N = dh, K = 64 keys; O stays in TMEM
 // The exponent reference m is raised (and O, l rescaled in place) only when a
 // chunk's maximum exceeds it by more than 8, so P <= e^8 and most chunks skip
-// the rescale.  Each CTA stores its unnormalized O (TMA store) with (m, l); a
-// combine kernel merges the ranges of a row in range order (deterministic) and
-// writes the bf16 attention output o[token][head * dh + d].
+// the rescale.  Each CTA stores its partial (TMA store) with (m, l): bf16 rows
+// of O / l by default, fp32 O where the caller supplies its own scratch or the
+// pipelined kernel runs; a combine kernel merges the ranges of a row in range
+// order (deterministic) and writes the bf16 attention output
+// o[token][head * dh + d].
 #include <math.h>
 #include <string.h>
 
@@ -398,8 +400,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   __syncthreads();  // every chunk buffer is free: reuse K/V space to stage O
   if (!failed) {
-    // O rows -> 128-byte-swizzled staging boxes of 32 fp32 columns x 128 rows
-    // (the K/V buffers hold exactly 128 x dh floats), then TMA stores
+    // O rows -> 128-byte-swizzled staging boxes (the K/V buffers hold exactly
+    // 128 x dh floats), then TMA stores
     const int r = qt * 128 + row;
     const bool valid_row = r / Hp < G && r % Hp < a.H;
     const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;

@@ -11,11 +11,13 @@
 // Merged Q/K/V and gate/up weights follow sglang PR #34599, item 1.
 //
 // Split K without a reduce kernel: the K splits of one output tile are the
-// CTAs of one thread-block cluster.  Each stages its fp32 partial tile in its
-// own shared memory; after a cluster barrier every CTA sums a slice of the
-// tile's tokens over all the cluster's partials (distributed shared memory,
-// in rank order, so the result does not depend on timing) and runs the
-// epilogue on it:
+// CTAs of one thread-block cluster, and the tile's tokens are dealt to them in
+// runs of 4-token groups.  Each CTA sends every other CTA its partial of that
+// CTA's run through distributed shared memory (one bulk copy per run out of
+// the drained pipeline buffers, or, where the fp32 tile does not fit there,
+// per-thread remote stores); the owner sums the cluster's partials in rank
+// order (so the result does not depend on timing) and runs the epilogue on
+// its run:
 //   kEQkvRope   adaRMS folded in (below), RoPE (rotate_half pairs) on q and k,
 //               bf16 q|k|v store
 //   kEGeglu     adaRMS folded in, gelu_tanh(g) * u of the interleaved gate/up
