@@ -1,0 +1,32 @@
+"""Host-side pieces of bench.py that need no GPU: the digest that ties the
+committed DRAM-traffic counters to the CUDA sources they were taken on."""
+import json
+import os
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_code_tokens_drop_comments_and_keep_strings():
+    text = 'int a = 1; // note\n/* block\n comment */ const char* s = "//x /*y*/";\n  int   b;'
+    assert bench._code_tokens(text) == 'int a = 1; const char* s = "//x /*y*/"; int b;'
+
+
+def test_code_tokens_see_code_changes_but_not_comment_edits():
+    base = "__global__ void k(int* p) { p[0] = 1; } // writes one\n"
+    assert bench._code_tokens(base) == bench._code_tokens(base.replace("writes one", "stores 1"))
+    assert bench._code_tokens(base) != bench._code_tokens(base.replace("= 1", "= 2"))
+
+
+def test_traffic_record_is_used_only_for_its_own_sources():
+    """The committed counters count only while the CUDA code they were taken
+    on is unchanged; otherwise bench.py reports no traffic."""
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        rec = json.load(f)
+    assert rec["bytes_per_flow_step"]["pi05_b1"] > 622e6  # the weights stream once per flow step
+    got = bench.measured_traffic("pi05_b1")
+    if rec["source_sha256"] == bench.source_digest():
+        assert got == rec["bytes_per_flow_step"]["pi05_b1"]
+    else:
+        assert got is None
