@@ -1011,6 +1011,14 @@ GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split, bool ret
     if (ks == 1) break;
     if (p.smem <= 232448 && max_active_clusters(ew, ks, p.smem) >= base) break;
   }
+  // An unsplit GEMM with between one and two waves of tiles keeps two CTAs
+  // per SM (half the shared memory each, at most 256 TMEM columns each), so
+  // every tile is resident at once and one CTA's epilogue runs under the
+  // other's mainloop.
+  if (p.ksplit == 1 && base > sm_count && base <= 2 * sm_count && p.tmem_cols <= 256) {
+    while (p.stages > 2 && 1024 + gemm_smem_layout(p.stages, p.tok_tile, 1).total > 113 * 1024) --p.stages;
+    p.smem = 1024 + gemm_smem_layout(p.stages, p.tok_tile, 1).total;
+  }
   return p;
 }
 
