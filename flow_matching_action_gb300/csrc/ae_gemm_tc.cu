@@ -75,7 +75,8 @@ __device__ __forceinline__ void named_bar(int n) {
 }
 
 // Split-K: the tokens of a tile are dealt to the ranks of its cluster in runs
-// of whole 4-token groups; rank r emits tokens [run_lo(r), run_hi(r)).
+// of whole 4-token groups; rank r emits tokens [run_lo(r), run_lo(r + 1)),
+// the last run clipped to the tile's valid tokens.
 __host__ __device__ inline int run_lo(int r, int ng, int ks) { return 4 * (r * ng / ks); }
 // Tokens of the longest run: a rank's receive buffer holds the partials of its
 // run from each rank, token-major: recv[src][token][128 features].
@@ -208,10 +209,8 @@ __device__ __forceinline__ void emit4(const Epi& E, int n, int q, int lane, int 
   }
 }
 
-// The same for a 16-token chunk (more independent work per warp for long
-// token runs).  Per-token inputs of one 16-token chunk that the epilogue of MODE reads from
-// global memory (RoPE (cos, sin) of the thread's pair, or the residual h),
-// loaded one chunk ahead of use.
+// pre4 for a 16-token chunk (more independent work per warp on long token
+// runs), loaded one chunk ahead of use.
 template <int MODE>
 __device__ __forceinline__ void pre16(const Epi& E, int n, int tok0, int cnt, float2 (&aux)[16]) {
   if (MODE == kEQkvRope) {
