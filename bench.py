@@ -126,7 +126,7 @@ def _dev(x, dtype):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True):
+def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_reps=50):
     import torch
     from flow_matching_action_gb300 import ae
 
@@ -183,6 +183,18 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True):
         total_ms = t0.elapsed_time(t1)
         bind_ms = [starts[i].elapsed_time(mids[i]) for i in range(steps)]
         sample_ms = [mids[i].elapsed_time(ends[i]) for i in range(steps)]
+        # per-call statistics (median, p90) over at least stat_reps ae_sample calls
+        extra = max(0, stat_reps - steps)
+        if extra:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(extra)]
+            ex.bind_prefix(k, v, cu, mask)
+            for i in range(extra):
+                ev[i][0].record(stream)
+                ex.sample(noises[i % n_noise], wl.n_steps, out)
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            sample_ms = sample_ms + [a.elapsed_time(b) for a, b in ev]
 
         e2e = None
         if measure_e2e:
@@ -378,7 +390,7 @@ def measured_traffic(workload: str):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="pi05_b1")
@@ -401,14 +413,17 @@ def main():
             return
         for _ in range(args.warmup):
             pass  # the oracle has no warm-up state; its first run is timed like the rest
+        # one step = one flow step of the workload through the oracle (measured);
+        # a chunk is n_steps of them, so the chunks/s value divides by n_steps
         per = []
         for _ in range(args.steps):
             sec, _ = oracle_flow_step_seconds(wl, w, budget_s=0.0)
-            per.append(sec * wl.n_steps)
+            per.append(sec)
         ms = statistics.median(per) * 1e3
-        value = wl.batch / (ms / 1e3)
+        value = wl.batch / (ms * wl.n_steps / 1e3)
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "chunks/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "step": f"one flow step of {wl.name} through the oracle (a chunk = {wl.n_steps} flow steps)",
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": {"workload": describe(wl)},
                 "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": blas_threads(),
@@ -452,6 +467,7 @@ def main():
                    "parallelism": f"replicas x{dist_ctx.world}"},
         "us_per_flow_step": sample_ms * 1e3 / wl.n_steps,
         "sample_ms_median": sample_ms, "sample_ms_p90": float(np.percentile(res["sample_ms"], 90)),
+        "sample_calls_timed": len(res["sample_ms"]),
         "bind_ms_median": bind_ms,
         "roofline": {"kernel": "ae_sample (all its launches, one flow step = 1 unit)",
                      "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
@@ -469,15 +485,21 @@ def main():
     if args.batched:
         wl2 = make_workload(args.batched)
         b2, f2 = algorithmic(wl2.dims, wl2.n_valid)
-        r2 = run_gpu_arm(wl2, w, max(3, args.steps // 4), args.warmup, dist_ctx, measure_e2e=False)
+        reps2 = max(50, args.steps)
+        r2 = run_gpu_arm(wl2, w, reps2, args.warmup, dist_ctx, measure_e2e=False, stat_reps=reps2)
         s2 = statistics.median(r2["sample_ms"])
-        t2 = dist_ctx.max(r2["total_ms"]) / max(3, args.steps // 4)
+        t2 = dist_ctx.max(r2["total_ms"]) / reps2
         tflops = f2 * wl2.n_steps / (s2 / 1e3) / 1e12
         line["batched"] = {"workload": describe(wl2), "chunks_per_s": wl2.batch / (t2 / 1e3) * dist_ctx.world,
                            "ms_per_step": t2, "us_per_flow_step": s2 * 1e3 / wl2.n_steps,
+                           "sample_ms_median": s2, "sample_ms_p90": float(np.percentile(r2["sample_ms"], 90)),
+                           "sample_calls_timed": len(r2["sample_ms"]),
+                           "clocks": r2["clocks"],
                            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
                                         "unit": "TFLOP/s", "frac": tflops / tf_sust,
-                                        "peak_kind": f"{peak_kind} sustained cuBLAS bf16",
+                                        "peak_burst": tf_burst, "frac_of_burst": tflops / tf_burst,
+                                        "peak_kind": f"{peak_kind} sustained cuBLAS bf16 (frac); "
+                                                     f"{peak_kind} burst cuBLAS bf16 (frac_of_burst)",
                                         "algorithmic_flops_per_flow_step": f2,
                                         "traffic": measured_traffic(args.batched),
                                         "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"}}

@@ -67,6 +67,7 @@ _SIGNATURES = {
     "ae_last_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_size_t]),
     "ae_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ae_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ae_info)]),
+    "ae_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64]),
 }
 
 _lib = None
@@ -166,6 +167,12 @@ def ae_sample_noalloc(ctx, noise, n_steps: int, out_actions) -> None:
     """ae_sample without device-memory allocation (see include/ae.h): for callers
     that sample inside a stream capture or under a fixed HBM budget."""
     _check(lib().ae_sample_noalloc(ctx, _ptr(noise), n_steps, _ptr(out_actions)), ctx)
+
+
+def ae_selftest_wait_timeout(ctx, budget_cycles: int) -> None:
+    """Run one bounded device wait that nothing completes (see include/ae.h):
+    the context's sticky status becomes AE_ERR_DEVICE."""
+    _check(lib().ae_selftest_wait_timeout(ctx, int(budget_cycles)), ctx)
 
 
 def ae_set_debug_dump(ctx, hidden, capacity: int) -> None:

@@ -193,8 +193,6 @@ ae_status alloc_scratch(ae_ctx* c) {
   AE_TRY(alloc(c, &c->rope_cs, (size_t)c->max_batch * d.H * (d.dh / 2) * sizeof(float2)));
   if (c->fast) {
     AE_TRY(alloc(c, &c->sumsq, (size_t)(d.D / 128) * M * sizeof(float)));
-    c->part_floats = ae::fast_part_floats(d, c->max_batch, c->sm_count);
-    AE_TRY(alloc(c, &c->part, 2 * c->part_floats * sizeof(float)));
     const size_t units = ae::attn_part_units(c->max_batch, d.H, d.Hq, d.Hkv, c->max_rows, c->sm_count);
     AE_TRY(alloc(c, &c->attn_o, units * 128 * d.dh * sizeof(float)));
     AE_TRY(alloc(c, &c->attn_ml, units * 128 * sizeof(float2)));
@@ -373,31 +371,6 @@ ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
     const char* pd = getenv("AE_PDL");
     c->use_graph = !(g && g[0] == '0');
     c->pdl = !(pd && pd[0] == '0');
-    // AE_KS=q,o,g,d caps the split-K factor of each projection (0 = no cap)
-    if (const char* ks = getenv("AE_KS"))
-      sscanf(ks, "%d,%d,%d,%d", &c->ks_cap[0], &c->ks_cap[1], &c->ks_cap[2], &c->ks_cap[3]);
-    // AE_ATTN_PIPE=1: pipelined eight-warp attention kernel
-    const char* ap = getenv("AE_ATTN_PIPE");
-    c->attn_pipe = ap && ap[0] == '1';
-    // AE_PERSIST=1: the whole sample as one persistent cooperative kernel
-    const char* pe = getenv("AE_PERSIST");
-    if (st == AE_OK && pe && pe[0] == '1') {
-      int coop = 0, per_sm = 0;
-      const size_t worst = ae::persist_smem_bytes(256, c->d.dh, c->d.D, c->d.A, nullptr, nullptr, nullptr);
-      e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-      if (e == cudaSuccess && worst <= 232448) e = ae::persist_setup(worst, &per_sm);
-      if (e == cudaSuccess && coop && per_sm >= 1 && worst <= 232448) {
-        st = alloc(c, &c->grid_sync, 2 * 128);
-        if (st == AE_OK) {
-          e = cudaMemsetAsync(c->grid_sync, 0, 2 * 128, c->stream);
-          if (e != cudaSuccess) st = cuda_fail(c, e, "grid barrier words");
-        }
-        c->persist = st == AE_OK;
-        // AE_PERSIST_SPIN=<ns> barrier poll back-off, AE_PERSIST_L2PF=1 L2 weight prefetch
-        if (const char* v = getenv("AE_PERSIST_SPIN")) c->persist_spin_ns = atoi(v);
-        if (const char* v = getenv("AE_PERSIST_L2PF")) c->persist_l2_pf = atoi(v);
-      }
-    }
   }
   if (st == AE_OK) {
     e = cudaStreamSynchronize(c->stream);
@@ -503,11 +476,7 @@ ae_status ae_sample(ae_ctx* c, const float* noise, int n_steps, float* out) {
   AE_TRY(get_table(c, n_steps, &t));
   const size_t xbytes = (size_t)B * d.H * d.A * sizeof(float);
   int64_t n = 0;
-  if (c->fast && c->persist) {
-    if (out != noise) AE_CK(c, cudaMemcpyAsync(out, noise, xbytes, cudaMemcpyDeviceToDevice, c->stream));
-    AE_CK(c, ae::sample_persistent(c, *t, n_steps, out, c->stream));
-    n = 1;
-  } else if (c->fast && c->use_graph) {
+  if (c->fast && c->use_graph) {
     AE_TRY(sample_graph(c, *t, n_steps, noise, out, xbytes, &n));
   } else {
     if (out != noise) AE_CK(c, cudaMemcpyAsync(out, noise, xbytes, cudaMemcpyDeviceToDevice, c->stream));

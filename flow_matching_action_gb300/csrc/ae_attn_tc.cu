@@ -23,8 +23,8 @@
 // The exponent reference m is raised (and O, l rescaled in place) only when a
 // chunk's maximum exceeds it by more than 8, so P <= e^8 and most chunks skip
 // the rescale.  Each CTA stores its partial (TMA store) with (m, l): bf16 rows
-// of O / l by default, fp32 O where the caller supplies its own scratch or the
-// pipelined kernel runs; a combine kernel merges the ranges of a row in range
+// of O / l by default, fp32 O where the caller supplies its own scratch; a
+// combine kernel merges the ranges of a row in range
 // order (deterministic) and writes the bf16 attention output
 // o[token][head * dh + d].
 #include <math.h>
@@ -406,7 +406,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const bool valid_row = r / Hp < G && r % Hp < a.H;
     const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;
     uint8_t* stg = smem + L.k[0];
-#pragma unroll 1
     if constexpr (O16) {
       // bf16 rows of O / l (half the bytes of fp32 partials): boxes of 64 columns
       const float inv_l = 1.f / l;
@@ -455,437 +454,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, tcols);
-  }
-}
-
-// ---------------------------------------------------------------- pipelined variant
-// Same work unit and partial outputs as k_attn_tc, with warp roles:
-//   warps 0..7  softmax: warp w owns TMEM lanes (query rows) 32 (w % 4).. and
-//               the key half w / 4 of every 64-key chunk; the two threads of a
-//               row exchange their maxima (and, at the end, their sums)
-//   warp 8      issues the MMAs: S(c) = Q K(c)^T into TMEM buffer c % 2, then
-//               O += P(c-1) V(c-1) once the softmax has written P(c-1)
-//   warp 9      loads: K(c) once S(c-2) is done, V(c) once P V(c-2) is done
-// An MMA issue blocks its warp while the tensor cores work, so only warp 8
-// issues them; the softmax of chunk c then overlaps S(c+1) and P V(c-1).
-// Every hand-off is an mbarrier, each phase used once per chunk or per
-// buffer, so no wait can mistake a later phase for the one it wants.
-constexpr int kPipeThreads = 320;
-constexpr int kPipeSoftmaxThreads = 256;
-constexpr int kPipeMaxChunks = 8;  // chunks a unit may visit (codes kept in shared memory)
-
-struct PipeSmem {
-  uint32_t q, k[2], v[2], p, xmax, xsum, codes, crow, bars, total;
-};
-
-__host__ __device__ inline PipeSmem pipe_smem_layout(int dh) {
-  PipeSmem L;
-  const uint32_t kv = (uint32_t)dh * kChunk * 2;
-  L.q = 0;
-  L.k[0] = (uint32_t)dh * 128 * 2;
-  L.k[1] = L.k[0] + kv;
-  L.v[0] = L.k[1] + kv;
-  L.v[1] = L.v[0] + kv;
-  L.p = L.v[1] + kv;
-  L.xmax = L.p + 128 * kChunk * 2;                 // float [2][128]
-  L.xsum = L.xmax + 2 * 128 * 4;                   // float [2][128]
-  L.codes = L.xsum + 2 * 128 * 4;                  // int [kPipeMaxChunks][kChunk]
-  L.crow = L.codes + kPipeMaxChunks * kChunk * 4;  // int [kPipeMaxChunks]: first row of a TMA chunk, or -1
-  L.bars = L.crow + kPipeMaxChunks * 4;            // 14 mbarriers, TMEM base, abort flag
-  L.total = L.bars + 128;
-  return L;
-}
-
-template <int ID>
-__device__ __forceinline__ void pipe_bar(int n) {
-  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ void pipe_quarter_bar(int q) {  // softmax warps q and q + 4
-  switch (q) {
-    case 0: pipe_bar<1>(64); break;
-    case 1: pipe_bar<2>(64); break;
-    case 2: pipe_bar<3>(64); break;
-    default: pipe_bar<4>(64); break;
-  }
-}
-
-// All lanes of a warp wait for the phase; uniform result (bounded).  Between
-// polls the warp sleeps in hardware until the phase completes, so waiting
-// warps do not flood the shared-memory pipe the working warps need.
-__device__ __forceinline__ bool pipe_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 1000000u))) return true;
-    int give_up = 0;
-    if ((threadIdx.x & 31) == 0) {
-      give_up = *abort ? 1 : 0;
-      if (!give_up && clock64() - t0 > kWaitBudgetCycles) {
-        report(status, kDevTimeout);
-        *abort = 1;
-        give_up = 1;
-      }
-    }
-    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
-  }
-}
-
-// Loader warp: K (kv = 0) or V (kv = 1) of the unit's chunk `slot` into buffer
-// `buf`, completing `bar`.  A TMA chunk: lane 0 arms the barrier with the
-// byte count and issues the boxes.  A gathered chunk: every lane issues its
-// cp.async rows and an arrive that fires when they land; then lane 0 adds the
-// barrier's one expected arrival.
-template <int DH>
-__device__ __forceinline__ void pipe_load(const AttnArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
-                                          uint8_t* smem, const PipeSmem& L, uint64_t* bar, int b, int g, int slot,
-                                          int buf, int kv) {
-  constexpr int kdb = DH / 64;
-  const int lane = threadIdx.x & 31;
-  const int* crow = reinterpret_cast<const int*>(smem + L.crow);
-  uint8_t* dst = smem + (kv ? L.v[buf] : L.k[buf]);
-  const int r0 = crow[slot];
-  if (r0 >= 0) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar, (uint32_t)kdb * kChunk * 128);
-      for (int kb = 0; kb < kdb; ++kb)
-        tma_load_2d_nohint(dst + kb * kChunk * 128, kv ? vmap : kmap, bar, g * DH + kb * 64, a.layer_row0 + r0);
-    }
-    __syncwarp();
-    return;
-  }
-  constexpr int CPR = DH / 8;  // 16-byte pieces per row
-  const int* ix = reinterpret_cast<const int*>(smem + L.codes) + slot * kChunk;
-  const int kvdim = a.Hkv * DH, qkvdim = (a.Hq + 2 * a.Hkv) * DH;
-  for (int i = lane; i < kChunk * CPR; i += 32) {
-    const int j = i / CPR, ch = i - j * CPR;
-    const int code = ix[j];
-    const bf16* src = a.qkv;  // any valid address when zero-filling
-    uint32_t bytes = 0;
-    if (code >= 0) {
-      src = (kv ? a.pv : a.pk) + (size_t)code * kvdim + g * DH;
-      bytes = 16;
-    } else if (code != kSkip) {
-      src = a.qkv + (size_t)(b * a.H + (-1 - code)) * qkvdim + (a.Hq + (kv ? a.Hkv : 0) + g) * DH;
-      bytes = 16;
-    }
-    cp_async16(dst + (ch >> 3) * kChunk * 128 + sw128_offset(j, ch & 7), bytes ? src + ch * 8 : src, bytes);
-  }
-  cp_async_mbar_arrive(bar);
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-  __syncwarp();
-}
-
-template <int DH>
-__global__ void __launch_bounds__(kPipeThreads, 1)
-    k_attn_pipe(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap, const AttnArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // keeps the shared address space
-  constexpr int kdb = DH / 64;
-  constexpr uint32_t kTmemCols = DH + 2 * kChunk <= 256 ? 256 : 512;
-  const PipeSmem L = pipe_smem_layout(DH);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* bar_q = bars;          // query tile landed
-  uint64_t* bar_k = bars + 1;      // [2] K buffer filled
-  uint64_t* bar_v = bars + 3;      // [2] V buffer filled
-  uint64_t* bar_s = bars + 5;      // [2] S buffer computed (tcgen05.commit)
-  uint64_t* bar_sfree = bars + 7;  // [2] S buffer read by all softmax warps (one arrive per warp)
-  uint64_t* bar_vfree = bars + 9;  // [2] V buffer consumed by P V (tcgen05.commit)
-  uint64_t* bar_p = bars + 11;     // P written by all softmax warps (one arrive per warp)
-  uint64_t* bar_o = bars + 12;     // P V complete (tcgen05.commit)
-  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(bars + 14);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
-  float* xmax = reinterpret_cast<float*>(smem + L.xmax);
-  float* xsum = reinterpret_cast<float*>(smem + L.xsum);
-  int* codes = reinterpret_cast<int*>(smem + L.codes);
-  int* crow = reinterpret_cast<int*>(smem + L.crow);
-
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int u = blockIdx.x;
-  const int sp = u % a.max_splits;
-  u /= a.max_splits;
-  const int qt = u % a.q_tiles;
-  u /= a.q_tiles;
-  const int g = u % a.Hkv;
-  const int b = u / a.Hkv;
-  const int G = a.Hq / a.Hkv;
-  const int Hp = fold_rows_per_head(a.H);
-  const int n_pre = a.n_valid[b];
-  const int n_keys = n_pre + a.H;
-  const int n_chunks = (n_keys + kChunk - 1) / kChunk;
-  const int c_begin = sp * a.chunks_per_cta;
-  const int c_end = min(c_begin + a.chunks_per_cta, n_chunks);
-  if (c_begin >= c_end) {  // uniform for the CTA
-    pdl_wait();
-    return;
-  }
-  const int n_my = min(c_end - c_begin, kPipeMaxChunks);  // the launcher keeps chunks_per_cta within it
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_k[i], 1);
-      mbar_init(&bar_v[i], 1);
-      mbar_init(&bar_s[i], 1);
-      mbar_init(&bar_sfree[i], kPipeSoftmaxThreads / 32);
-      mbar_init(&bar_vfree[i], 1);
-    }
-    mbar_init(bar_p, kPipeSoftmaxThreads / 32);
-    mbar_init(bar_o, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-    prefetch_tensormap(&qmap);
-    prefetch_tensormap(&kmap);
-    prefetch_tensormap(&vmap);
-    prefetch_tensormap(&omap);
-  }
-  if (warp == 0) {
-    tmem_alloc(tmem_base_p, kTmemCols);
-    tmem_relinquish();
-  }
-  // every gather code of the unit (binding data only: may run before the
-  // preceding kernel has finished)
-  for (int i = threadIdx.x; i < n_my * kChunk; i += kPipeThreads) {
-    const int sl = i / kChunk, j = i - sl * kChunk;
-    const int key0 = (c_begin + sl) * kChunk, key = key0 + j;
-    const int nk = min(kChunk, n_keys - key0);
-    int code = kSkip;
-    if (j < nk) {
-      if (key < n_pre) {
-        const int prow = a.valid_idx[(size_t)b * a.max_rows + key];
-        if (prow >= 0 && prow < a.total_rows) code = prow;
-        else report(a.status, kDevBounds);
-      } else {
-        code = -1 - (key - n_pre);
-      }
-    }
-    codes[i] = code;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (threadIdx.x < n_my) {
-    const int* ix = codes + threadIdx.x * kChunk;
-    // codes increase strictly over a chunk's prefix keys: first and last decide
-    crow[threadIdx.x] = (ix[0] >= 0 && ix[kChunk - 1] >= 0 && ix[kChunk - 1] - ix[0] == kChunk - 1) ? ix[0] : -1;
-  }
-  __syncthreads();
-  const uint32_t tmem = *tmem_base_p;
-  const int n_pro = n_my < 2 ? n_my : 2;
-  if (warp == 9)  // prefix-only (TMA) chunks 0 and 1 may load before the preceding kernel ends
-    for (int sl = 0; sl < n_pro; ++sl)
-      if (crow[sl] >= 0) {
-        pipe_load<DH>(a, &kmap, &vmap, smem, L, &bar_k[sl], b, g, sl, sl, 0);
-        pipe_load<DH>(a, &kmap, &vmap, smem, L, &bar_v[sl], b, g, sl, sl, 1);
-      }
-  pdl_wait();
-
-  bool failed = false;
-  if (warp == 9) {
-    // ---------------- loader
-    for (int sl = 0; sl < n_pro; ++sl)
-      if (crow[sl] < 0) {
-        pipe_load<DH>(a, &kmap, &vmap, smem, L, &bar_k[sl], b, g, sl, sl, 0);
-        pipe_load<DH>(a, &kmap, &vmap, smem, L, &bar_v[sl], b, g, sl, sl, 1);
-      }
-    if (lane == 0) {  // the query tile: groups of a.q_box rows of the fold (never straddling heads)
-      const int QB = a.q_box, n_rg = 128 / QB;
-      int nbox = 0;
-      for (int rg = 0; rg < n_rg; ++rg)
-        if ((qt * 128 + rg * QB) / Hp < G) ++nbox;
-      mbar_arrive_expect_tx(bar_q, (uint32_t)nbox * kdb * QB * 128);
-      for (int rg = 0; rg < n_rg; ++rg) {
-        const int r0 = qt * 128 + rg * QB;
-        const int hh = r0 / Hp;
-        if (hh >= G) continue;
-        const int tok0 = r0 - hh * Hp;
-        const int col = (g * G + hh) * DH;
-        for (int kb = 0; kb < kdb; ++kb)
-          tma_load_2d_nohint(smem + L.q + kb * 128 * 128 + rg * QB * 128, &qmap, bar_q, col + kb * 64, b * a.H + tok0);
-      }
-    }
-    __syncwarp();
-    for (int c = 2; c < n_my && !failed; ++c) {
-      const int bf = c & 1;
-      const uint32_t prev = (uint32_t)((c - 2) >> 1) & 1u;  // phase of chunk c - 2 in buffer bf
-      if (!pipe_warp_wait(&bar_s[bf], prev, abort_flag, a.status)) failed = true;  // S(c-2) done: K free
-      if (!failed) pipe_load<DH>(a, &kmap, &vmap, smem, L, &bar_k[bf], b, g, c, bf, 0);
-      if (!failed && !pipe_warp_wait(&bar_vfree[bf], prev, abort_flag, a.status)) failed = true;  // V free
-      if (!failed) pipe_load<DH>(a, &kmap, &vmap, smem, L, &bar_v[bf], b, g, c, bf, 1);
-    }
-  } else if (warp == 8) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16(128, kChunk);
-    constexpr uint32_t idesc_o = idesc_bf16(128, DH, true);
-    if (!pipe_warp_wait(bar_q, 0, abort_flag, a.status)) failed = true;
-    auto pv = [&](int c) {  // O += P(c) V(c)
-      const int bf = c & 1;
-      bool ok = pipe_warp_wait(bar_p, (uint32_t)c & 1u, abort_flag, a.status);
-      ok = ok && pipe_warp_wait(&bar_v[bf], (uint32_t)(c >> 1) & 1u, abort_flag, a.status);
-      if (lane == 0) {
-        if (ok) {
-          fence_proxy_async_smem();  // P and gathered V rows (generic proxy) before the MMA reads them
-          tc_fence_after();
-          const uint64_t ad = sdesc_sw128(smem_u32(smem + L.p));
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = sdesc_sw128_mn(smem_u32(smem + L.v[bf] + k * 2048), kChunk * 128, 1024);
-            mma_bf16(tmem, ad + 2 * k, bd, idesc_o, (c > 0 || k > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(&bar_vfree[bf]);
-        mma_commit(bar_o);  // also when failed: the phases still complete
-      }
-      __syncwarp();
-      return ok;
-    };
-    for (int c = 0; c < n_my && !failed; ++c) {
-      const int bf = c & 1;
-      bool ok = pipe_warp_wait(&bar_k[bf], (uint32_t)(c >> 1) & 1u, abort_flag, a.status);
-      if (c >= 2) ok = ok && pipe_warp_wait(&bar_sfree[bf], (uint32_t)((c - 2) >> 1) & 1u, abort_flag, a.status);
-      if (lane == 0) {
-        if (ok) {
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t tm_s = tmem + DH + kChunk * bf;
-#pragma unroll
-          for (int kb = 0; kb < kdb; ++kb) {
-            const uint64_t ad = sdesc_sw128(smem_u32(smem + L.q + kb * 128 * 128));
-            const uint64_t bd = sdesc_sw128(smem_u32(smem + L.k[bf] + kb * kChunk * 128));
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_bf16(tm_s, ad + 2 * k, bd + 2 * k, idesc_s, (kb > 0 || k > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(&bar_s[bf]);
-      }
-      __syncwarp();
-      if (!ok) failed = true;
-      if (c >= 1 && !failed && !pv(c - 1)) failed = true;
-    }
-    if (!failed && !pv(n_my - 1)) failed = true;
-  } else {
-    // ---------------- softmax warps 0..7
-    const int q4 = warp & 3, ch = warp >> 2;
-    const int row = 32 * q4 + lane;
-    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    const float sl2 = a.scale * 1.4426950408889634f;
-    float m_ref = -INFINITY, l_part = 0.f;
-    for (int c = 0; c < n_my; ++c) {
-      const int bf = c & 1;
-      const int nk = min(kChunk, n_keys - (c_begin + c) * kChunk);
-      if (!pipe_warp_wait(&bar_s[bf], (uint32_t)(c >> 1) & 1u, abort_flag, a.status)) failed = true;
-      tc_fence_after();
-      float sv[32];
-      tmem_ld32(tmem + DH + kChunk * bf + 32 * ch + lane_off, sv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_sfree[bf]);  // this warp is done with S buffer bf
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        sv[j] *= sl2;
-        if (32 * ch + j < nk) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
-      }
-      const float lmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      xmax[ch * 128 + row] = lmax;
-      pipe_quarter_bar(q4);
-      const float cmax = fmaxf(lmax, xmax[(ch ^ 1) * 128 + row]);
-      pipe_quarter_bar(q4);  // both halves read the exchange before it is written again
-      float factor = 1.f;
-      if (c == 0) {
-        m_ref = cmax;
-      } else if (cmax > m_ref + kRescaleMargin * 1.4426950408889634f) {
-        factor = ex2_fast(m_ref - cmax);
-        m_ref = cmax;
-      }
-      // P V(c - 1) must be complete before O is rescaled or P is overwritten
-      if (c > 0 && !pipe_warp_wait(bar_o, (uint32_t)(c - 1) & 1u, abort_flag, a.status)) failed = true;
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, factor != 1.f)) {
-        l_part *= factor;
-#pragma unroll 1
-        for (int c0 = 0; c0 < DH / 2; c0 += 16) {
-          float v[16];
-          const uint32_t ta = tmem + lane_off + (uint32_t)(ch * (DH / 2) + c0);
-          tmem_ld16(ta, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] *= factor;
-          tmem_st16(ta, v);
-        }
-      }
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float p0 = (32 * ch + j < nk) ? ex2_fast(sv[j] - m_ref) : 0.f;
-        const float p1 = (32 * ch + j + 1 < nk) ? ex2_fast(sv[j + 1] - m_ref) : 0.f;
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        // the row sum uses the bf16-rounded weights, the values P V multiplies
-        const float2 pr = __bfloat1622float2(pb);
-        l_part += pr.x + pr.y;
-        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        *reinterpret_cast<uint4*>(smem + L.p + sw128_offset(row, 4 * ch + cc)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);  // this warp's part of P(c) (and of the O rescale) is written
-    }
-    if (!pipe_warp_wait(bar_o, (uint32_t)(n_my - 1) & 1u, abort_flag, a.status)) failed = true;
-    failed = failed || *abort_flag;
-    if (!failed) {
-      tc_fence_after();
-      // row sum = half 0 + half 1 (fixed order)
-      xsum[ch * 128 + row] = l_part;
-      pipe_quarter_bar(q4);
-      const float l = xsum[row] + xsum[128 + row];
-      const int r = qt * 128 + row;
-      const bool valid_row = r / Hp < G && r % Hp < a.H;
-      const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;
-      // O rows -> staging boxes of 32 fp32 columns x 128 rows in the (now idle) K/V space -> TMA stores
-      uint8_t* stg = smem + L.k[0];
-#pragma unroll 1
-      for (int c0 = 0; c0 < DH / 2; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem + lane_off + (uint32_t)(ch * (DH / 2) + c0), v);
-        const int col0 = ch * (DH / 2) + c0;
-        uint8_t* box = stg + (col0 >> 5) * (128 * 128);
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq)
-          *reinterpret_cast<float4*>(box + sw128_offset(row, qq)) =
-              make_float4(v[4 * qq], v[4 * qq + 1], v[4 * qq + 2], v[4 * qq + 3]);
-      }
-      if (valid_row && ch == 0) a.part_ml[unit * 128 + row] = make_float2(m_ref, l);
-      fence_proxy_async_smem();
-      pipe_bar<5>(kPipeSoftmaxThreads);
-      if (threadIdx.x == 0) {
-        for (int bx = 0; bx < DH / 32; ++bx) tma_store_2d(&omap, stg + bx * (128 * 128), bx * 32, (int)(unit * 128));
-        bulk_commit();
-        bulk_wait_read_all();
-      }
-      __syncwarp();
-    }
-  }
-  if (failed && lane == 0) {
-    // leave nothing in flight: every copy this CTA started, and the MMAs
-    volatile int fresh = 0;
-    if (warp == 9) {
-      mbar_wait(bar_q, 0, &fresh, a.status);
-    } else if (warp == 8) {
-      mma_commit(bar_o);
-    }
-  }
-  cp_async_wait<0>();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -1026,10 +594,6 @@ cudaError_t attn_attrs() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   }
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_pipe<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_attn_pipe<DH>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
@@ -1055,17 +619,6 @@ cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, con
   a.o16 = omap16 != nullptr ? 1 : 0;
   const CUtensorMap& omap = a.o16 ? *omap16 : omap_f32;
   const unsigned grid = (unsigned)(a.batch * a.Hkv * a.q_tiles * a.max_splits);
-  cudaError_t e;
-  if (a.pipe && a.chunks_per_cta <= kPipeMaxChunks) {
-    const size_t ps = 1024 + pipe_smem_layout(a.dh).total;
-    switch (a.dh) {
-      case 64: e = launch_k(k_attn_pipe<64>, dim3(grid), dim3(kPipeThreads), ps, s, pdl, qmap, kmap, vmap, omap, a); break;
-      case 128: e = launch_k(k_attn_pipe<128>, dim3(grid), dim3(kPipeThreads), ps, s, pdl, qmap, kmap, vmap, omap, a); break;
-      default: e = launch_k(k_attn_pipe<256>, dim3(grid), dim3(kPipeThreads), ps, s, pdl, qmap, kmap, vmap, omap, a); break;
-    }
-    if (e != cudaSuccess) return e;
-    return launch_k(k_attn_combine<false>, dim3(combine_blocks(a)), dim3(32 * kCombineRows), 0, s, pdl, a, o);
-  }
   const size_t smem = attn_smem_bytes(a.dh);
   auto go = [&](auto o16_tag) {
     constexpr bool O16 = decltype(o16_tag)::value;

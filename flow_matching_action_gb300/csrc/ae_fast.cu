@@ -69,16 +69,6 @@ bool fast_path_supported(const Dims& d, std::string* why) {
   return true;
 }
 
-size_t fast_part_floats(const Dims& d, int max_batch, int sm_count) {
-  // a split chosen to fill the GPU has ksplit * M <= sm_count * 256 / n_tiles, so
-  // ksplit * M * N <= sm_count * 256 * 128; the O and down projections always
-  // split at least 2 ways
-  const size_t maxM = (size_t)max_batch * d.H;
-  const size_t a = (size_t)sm_count * 256 * 128;
-  const size_t b = 2 * maxM * (size_t)d.D;
-  return a > b ? a : b;
-}
-
 cudaError_t fast_setup(ae_ctx* c) {
   const Dims& d = c->d;
   cudaError_t e;
@@ -153,10 +143,10 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const int nqkv = d.qkvdim(), qd = d.qdim();
   const float eps = (float)d.eps;
   const int sm = c->sm_count;
-  const GemmPlan pq = plan_gemm_cl(nqkv, D, M, sm, c->ks_cap[0], true);
-  const GemmPlan po = plan_gemm_cl(D, qd, M, sm, c->ks_cap[1]);
-  const GemmPlan pg = plan_gemm_cl(2 * F, D, M, sm, c->ks_cap[2]);
-  const GemmPlan pd = plan_gemm_cl(D, F, M, sm, c->ks_cap[3]);
+  const GemmPlan pq = plan_gemm_cl(nqkv, D, M, sm, 0, true);
+  const GemmPlan po = plan_gemm_cl(D, qd, M, sm);
+  const GemmPlan pg = plan_gemm_cl(2 * F, D, M, sm);
+  const GemmPlan pd = plan_gemm_cl(D, F, M, sm);
   // the O, gate/up and down GEMMs share one token tiling (it depends on M
   // only); the QKV GEMM may use more, shorter tiles through its own operand map
   // A single token tile loads only the M valid rows (the MMA still reads the
@@ -246,11 +236,9 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.part_ml = attn_scratch ? attn_scratch->part_ml : c->attn_ml;
       at.max_units = attn_scratch ? attn_scratch->max_units : 0;
       at.status = c->status_dev;
-      at.pipe = c->attn_pipe ? 1 : 0;
       at.q_box = c->q_box_rows;
-      // bf16 partials may be chosen on the default path; the pipelined kernel
-      // and callers' own scratch keep fp32
-      const bool o16_ok = attn_scratch == nullptr && !c->attn_pipe;
+      // bf16 partials on the default path; callers' own scratch keeps fp32
+      const bool o16_ok = attn_scratch == nullptr;
       ck(launch_attn_tc(c->map_qtile, c->bind.map_pk, c->bind.map_pv,
                         attn_scratch ? attn_scratch->omap : c->map_attn_o, o16_ok ? &c->map_attn_o16 : nullptr, at, o,
                         sm, s, pdl));
@@ -292,141 +280,6 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   ++n;
   ck(cudaGetLastError());
   return n;
-}
-
-cudaError_t sample_persistent(ae_ctx* c, const TimeTable& t, int n_steps, float* x, cudaStream_t s) {
-  const Dims& d = c->d;
-  const int B = c->bind.batch, M = B * d.H, D = d.D, F = d.F;
-  const int nqkv = d.qkvdim(), qd = d.qdim();
-  const int sm = c->sm_count;
-  // A split-K GEMM costs an extra phase and grid barrier for its reduction;
-  // the QKV and gate/up projections skip it once their tiles occupy 16 SMs.
-  auto cap = [&](int i, int N) {
-    if (c->ks_cap[i] > 0) return c->ks_cap[i];
-    const int tok_tiles = (M + 255) / 256;
-    return (N / 128) * (tok_tiles < 1 ? 1 : tok_tiles) >= 16 ? 1 : 0;
-  };
-  GemmPlan pl[4] = {plan_gemm(nqkv, D, M, sm, 1, cap(0, nqkv)), plan_gemm(D, qd, M, sm, 2, c->ks_cap[1]),
-                    plan_gemm(2 * F, D, M, sm, 1, cap(2, 2 * F)), plan_gemm(D, F, M, sm, 2, c->ks_cap[3])};
-  const int TT = pl[0].tok_tile;  // the four GEMMs share one token tiling (it depends on M only)
-  PersistParams P;
-  memset(&P, 0, sizeof(P));
-  const size_t smem = persist_smem_bytes(TT, d.dh, D, d.A, &P.data_bytes, &P.row_bytes, &P.stages);
-  if (smem > 232448) return cudaErrorInvalidConfiguration;
-  // With one token tile, the O and down projections split K only as far as
-  // needed for a CTA's weight tiles to fit the pipeline: the tiles are then
-  // all in shared memory before the phase starts (they are issued during the
-  // phase before), and the split-K sum that follows has fewer partials.
-  if (pl[0].tok_tiles == 1)
-    for (int i : {1, 3}) {
-      if (c->ks_cap[i] > 0) continue;
-      const int ks = (pl[i].kb_total + P.stages - 1) / P.stages;
-      pl[i] = plan_gemm(pl[i].N, pl[i].K, M, sm, ks < 2 ? 2 : ks, ks < 2 ? 2 : ks);
-    }
-  cudaError_t e = fast_activation_maps(c, TT, TT);
-  if (e != cudaSuccess) return e;
-  P.w[0] = c->map_qkv;
-  P.w[1] = c->map_o;
-  P.w[2] = c->map_gu;
-  P.w[3] = c->map_d;
-  P.wptr[0] = (const bf16*)c->w_qkv;
-  P.wptr[1] = (const bf16*)c->w_o;
-  P.wptr[2] = (const bf16*)c->w_gu;
-  P.wptr[3] = (const bf16*)c->w_d;
-  P.act[0] = c->map_y;
-  P.act[1] = c->map_oact;
-  P.act[2] = c->map_y;
-  P.act[3] = c->map_mact;
-  float* part0 = c->part;
-  float* part1 = c->part + c->part_floats;
-  const int rows_per_layer[4] = {nqkv, D, 2 * F, D};
-  const long out_rows = (long)c->max_batch * d.H;
-  for (int i = 0; i < 4; ++i) {
-    PersistGemm& g = P.g[i];
-    g.n_tiles = pl[i].n_tiles;
-    g.ksplit = pl[i].ksplit;
-    g.kb_total = pl[i].kb_total;
-    g.rows_per_layer = rows_per_layer[i];
-    g.e_mode = kEPartial;
-    g.tma_out = 1;
-    if (i == 0 && g.ksplit == 1) {
-      g.e_mode = kEQkvRope;
-      g.tma_out = d.dh >= 128 ? 1 : 0;
-      if (g.tma_out) e = make_bf16_map(&P.out[i], c->qkv, out_rows, nqkv, TT);
-    } else if (i == 2 && g.ksplit == 1) {
-      g.e_mode = kEGeglu;
-      e = make_bf16_map(&P.out[i], c->m, out_rows, F, TT);
-    } else {
-      e = make_f32_3d_map(&P.out[i], i == 3 ? part1 : part0, pl[i].N, M, g.ksplit, TT);
-    }
-    if (e != cudaSuccess) return e;
-  }
-  P.q16 = c->map_qkv_act;
-  P.pk = c->bind.map_pk;
-  P.pv = c->bind.map_pv;
-  P.attn_o = c->map_attn_o;
-  AttnArgs at = {};
-  at.plan_rows = c->bind.max_phys_rows;
-  at.batch = B;
-  at.H = d.H;
-  at.Hq = d.Hq;
-  at.Hkv = d.Hkv;
-  at.dh = d.dh;
-  attn_plan(at, sm);
-  P.L = d.L;
-  P.D = D;
-  P.F = F;
-  P.A = d.A;
-  P.H = d.H;
-  P.Hq = d.Hq;
-  P.Hkv = d.Hkv;
-  P.dh = d.dh;
-  P.qkvdim = nqkv;
-  P.n_rot_heads = d.Hq + d.Hkv;
-  P.M = M;
-  P.batch = B;
-  P.tok_tile = TT;
-  P.tok_tiles = pl[0].tok_tiles;
-  P.n_steps = n_steps;
-  P.eps = (float)d.eps;
-  P.delta = (float)(-1.0 / (double)n_steps);
-  P.scale = (float)(1.0 / sqrt((double)d.dh));
-  P.total_rows = c->bind.total_rows;
-  P.max_rows = c->max_rows;
-  P.q_tiles = at.q_tiles;
-  P.chunks_per_cta = at.chunks_per_cta;
-  P.max_splits = at.max_splits;
-  P.valid_idx = c->valid_idx;
-  P.n_valid = c->n_valid;
-  P.pk_ptr = (const bf16*)c->bind.pk;
-  P.pv_ptr = (const bf16*)c->bind.pv;
-  P.attn_o_ptr = c->attn_o;
-  P.attn_ml = c->attn_ml;
-  P.x = x;
-  P.h = c->h;
-  P.y = (bf16*)c->y;
-  P.qkv = (bf16*)c->qkv;
-  P.o = (bf16*)c->o;
-  P.m = (bf16*)c->m;
-  P.part0 = part0;
-  P.part1 = part1;
-  P.rope_cs = c->rope_cs;
-  P.mod = t.mod;
-  P.fin = t.fin;
-  P.w_in = (const bf16*)c->w_in;
-  P.b_in = (const bf16*)c->b_in;
-  P.w_out = (const bf16*)c->w_out;
-  P.b_out = (const bf16*)c->b_out;
-  P.dump = c->dump;
-  P.status = c->status_dev;
-  P.spin_ns = c->persist_spin_ns;
-  P.l2_pf = c->persist_l2_pf;
-  P.bar_count = c->grid_sync;
-  P.grid_abort = (int*)(c->grid_sync + 32);
-  // a barrier abandoned by an earlier failed launch must not leave a count behind
-  e = cudaMemsetAsync(c->grid_sync, 0, 2 * 128, s);
-  if (e != cudaSuccess) return e;
-  return launch_persistent(P, sm, smem, s);
 }
 
 }  // namespace ae

@@ -535,8 +535,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       tc_fence_after();
       if constexpr (XP == 0) {
         // unsplit: the accumulator is the sum; emit straight from TMEM, 4 tokens a step
-        auto run = [&](auto mode_tag) {
-          constexpr int MODE = decltype(mode_tag)::value;
+        auto run = [&]() {
           if constexpr (MODE == kEQkvRope) {
             // Long tiles of a rotated head: the tile's slice of the RoPE table
             // (tokens x its 64 pairs, 512 bytes a token) is copied once into
@@ -598,7 +597,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
             emit4<MODE>(E, n, q, lane, c0, t0 + c0, v, min(4, c_hi - c0), cf, gt, sc, cur);
           }
         };
-        run(std::integral_constant<int, MODE>());
+        run();
       } else if constexpr (XP == 1) {
         // split K: stage this partial token-major in the drained pipeline
         // buffers, then send each rank its run of tokens with one bulk copy
@@ -670,8 +669,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
     }
     if (warp >= 2 && go) {
       // sum this rank's tokens over the cluster's partials in rank order, emit them
-      auto run = [&](auto mode_tag) {
-        constexpr int MODE = decltype(mode_tag)::value;
+      auto run = [&]() {
         if (MODE != kEResid && p_hi - p_lo >= 16) {
           // long run: 16 tokens a step, four ranks' loads in flight
           float2 nx[16];
@@ -735,7 +733,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
           emit4<MODE>(E, n, q, lane, c0, t0 + e_lo + c0, v, cnt, cf, gt, sc, cur);
         }
       };
-      run(std::integral_constant<int, MODE>());
+      run();
     }
   }
   if (MODE == kEResid && warp >= 2) {
@@ -895,34 +893,6 @@ static void plan_tiles(GemmPlan& p, int N, int K, int M, int tok_tiles = 0) {
   int cols = 32;
   while (cols < tt) cols <<= 1;
   p.tmem_cols = cols;
-}
-
-static void plan_stages(GemmPlan& p) {
-  const int tt = p.tok_tile;
-  // as many stages as a CTA has K blocks, within the shared-memory budget
-  const int per_cta = (p.kb_total + p.ksplit - 1) / p.ksplit;
-  int stages = per_cta < 8 ? per_cta : 8;
-  if (stages < 2) stages = 2;
-  while (stages > 2 && tc_gemm_smem_bytes(stages, tt) > 200 * 1024) --stages;
-  // the epilogue stages its fp32 tile (tt x 128) in the drained pipeline buffers
-  while ((size_t)stages * (kATileBytes + (size_t)tt * 128) < (size_t)tt * 512 && stages < 8) ++stages;
-  p.stages = stages;
-  p.smem = tc_gemm_smem_bytes(stages, tt);
-  p.grid = p.n_tiles * p.tok_tiles * p.ksplit;
-}
-
-GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split) {
-  GemmPlan p;
-  plan_tiles(p, N, K, M);
-  const int base = p.n_tiles * p.tok_tiles;
-  int ks = sm_count / base;
-  if (max_split > 0 && ks > max_split) ks = max_split;
-  if (ks < min_split) ks = min_split;
-  if (ks < 1) ks = 1;
-  if (ks > p.kb_total) ks = p.kb_total;
-  p.ksplit = ks;
-  plan_stages(p);
-  return p;
 }
 
 namespace {

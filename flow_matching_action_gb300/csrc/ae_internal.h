@@ -108,7 +108,6 @@ struct ae_ctx {
   bool fast = false;
   bool pdl = false;        // chain kernels by programmatic dependent launch
   bool use_graph = false;  // capture and replay the launch sequence
-  int ks_cap[4] = {0, 0, 0, 0};  // split-K caps of the QKV, O, gate/up, down GEMMs (0 = none)
   CUtensorMap map_qkv, map_o, map_gu, map_d;   // weights, boxes 128 rows x 64
   CUtensorMap map_y, map_oact, map_mact;        // bf16 activations, boxes act_box_rows x 64
   CUtensorMap map_yq;                           // the QKV GEMM's operand, boxes act_box_rows_q x 64
@@ -119,8 +118,6 @@ struct ae_ctx {
   int q_box_rows = 16;
   int act_box_rows = 0, act_box_rows_q = 0;
   float* sumsq = nullptr;    // [D/128][M] sums of h^2 per 128-feature tile (adaRMS folded into GEMMs)
-  float* part = nullptr;     // split-K partials (persistent kernel)
-  size_t part_floats = 0;
   float* attn_o = nullptr;   // attention partials
   float2* attn_ml = nullptr;
   float* x = nullptr;        // [M, A] flow state while a captured graph runs
@@ -140,12 +137,6 @@ struct ae_ctx {
              pk == o.pk && pv == o.pv && total_rows == o.total_rows && dump == o.dump;
     }
   } graph_key;
-
-  // Persistent path: the whole sample as one cooperative kernel (ae_persist.cu).
-  bool persist = false;
-  unsigned* grid_sync = nullptr;  // barrier arrival count and abort word (separate 128-byte lines)
-  int persist_spin_ns = 100, persist_l2_pf = 0;
-  bool attn_pipe = false;  // pipelined attention kernel
 
   int64_t launches_sample = 0, launches_bind = 0, device_bytes = 0;
   std::vector<void*> allocations;
@@ -227,8 +218,6 @@ struct GemmPlan {
   size_t smem;
 };
 size_t tc_gemm_smem_bytes(int stages, int tok_tile);
-// Split-K plan of the persistent kernel (partials through global memory).
-GemmPlan plan_gemm(int N, int K, int M, int sm_count, int min_split, int max_split = 0);
 // Split-K plan of k_tc_gemm: the splits of a tile form one cluster (<= 16 CTAs),
 // no more splits than keep every cluster of the launch resident at once.
 // retile: an unsplit plan that leaves SMs idle may use more, shorter token
@@ -260,7 +249,6 @@ struct AttnArgs {
   float scale;
   int q_tiles, chunks_per_cta, max_splits;  // set by the planner
   int max_units;          // cap on work units (0: none), for fixed-size scratch
-  int pipe;               // use the pipelined eight-warp kernel when the plan allows it
   int q_box;              // rows of a query-tile TMA box (64, 32 or 16; divides the padded head length)
   float* part_o;          // [units][128][dh] fp32 O, or (o16) bf16 O / l
   float2* part_ml;        // [units][128]
@@ -292,7 +280,6 @@ bool fast_path_supported(const Dims& d, std::string* why);
 cudaError_t fast_setup(ae_ctx* c);  // tensor maps and scratch, after the weights are packed
 // one box = one token tile: box_rows for the gate/up, O and down GEMMs, box_rows_q for QKV
 cudaError_t fast_activation_maps(ae_ctx* c, int box_rows, int box_rows_q);
-size_t fast_part_floats(const Dims& d, int max_batch, int sm_count);
 // Attention split-KV partials supplied by the caller instead of the context's.
 struct AttnScratch {
   float* part_o;
@@ -305,65 +292,5 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
 // The cached time table of n_steps, or nullptr (never allocates).
 const TimeTable* find_time_table(const ae_ctx* c, int n_steps);
 void attn_plan(AttnArgs& a, int sm_count);
-
-// ---- persistent kernel (ae_persist.cu)
-struct PersistGemm {
-  int n_tiles, ksplit, kb_total;
-  int rows_per_layer;   // rows of one layer's matrix in the stacked weight
-  int e_mode;           // EMode
-  int tma_out;          // kEQkvRope: output by TMA store (head_dim >= 128)
-};
-// Everything one launch needs, passed by value (__grid_constant__).  GEMM
-// index 0..3 = merged QKV, O, merged gate/up, down.
-struct PersistParams {
-  CUtensorMap w[4];     // stacked weights, boxes 128 rows x 64
-  CUtensorMap act[4];   // bf16 activation operands, boxes tok_tile rows x 64
-  CUtensorMap out[4];   // epilogue outputs (bf16 boxes or fp32 split-K partial boxes)
-  CUtensorMap q16;      // q|k|v activations, boxes 16 rows x 64
-  CUtensorMap pk, pv;   // bound prefix K / V, boxes 64 rows x 64 (used when >= 64 rows)
-  CUtensorMap attn_o;   // attention O partials, boxes 128 rows x 32 fp32
-  PersistGemm g[4];
-  const bf16* wptr[4];  // the same stacked weights as w[], for L2 prefetches
-  int L, D, F, A, H, Hq, Hkv, dh, qkvdim, n_rot_heads;
-  int M, batch, tok_tile, tok_tiles, n_steps;
-  float eps, delta, scale;
-  long total_rows;
-  int max_rows, q_tiles, chunks_per_cta, max_splits;
-  uint32_t data_bytes, row_bytes;   // shared-memory layout
-  int stages;                       // GEMM pipeline stages
-  int spin_ns;                      // grid-barrier poll back-off
-  int l2_pf;                        // pull later GEMMs' weights into L2 during row phases
-  const int* valid_idx;
-  const int* n_valid;
-  const bf16* pk_ptr;
-  const bf16* pv_ptr;
-  float* attn_o_ptr;
-  float2* attn_ml;
-  float* x;
-  float* h;
-  bf16* y;
-  bf16* qkv;
-  bf16* o;
-  bf16* m;
-  float* part0;
-  float* part1;
-  const float2* rope_cs;
-  const float* mod;
-  const float* fin;
-  const bf16* w_in;
-  const bf16* b_in;
-  const bf16* w_out;
-  const bf16* b_out;
-  float* dump;
-  int* status;
-  unsigned* bar_count;  // grid-barrier arrivals, zero at launch
-  int* grid_abort;
-};
-size_t persist_smem_bytes(int tok_tile, int dh, int D, int A, uint32_t* data_bytes, uint32_t* row_bytes,
-                          int* stages);
-cudaError_t persist_setup(size_t smem, int* blocks_per_sm);
-cudaError_t launch_persistent(const PersistParams& P, int grid, size_t smem, cudaStream_t s);
-// One ae_sample of n_steps on the persistent path, the flow state in place in x.
-cudaError_t sample_persistent(ae_ctx* c, const TimeTable& t, int n_steps, float* x, cudaStream_t s);
 
 }  // namespace ae

@@ -22,26 +22,51 @@ constexpr size_t kScratchFloats = (size_t)4 << 20;
 static __device__ __align__(256) float g_attn_scratch[kScratchFloats];
 
 // Device address of g_attn_scratch per device.  In host code the symbol's name
-// is only a host-side stand-in, so the address is looked up once per device,
-// with that device current, and passed to the kernels as a plain pointer.
+// is only a host-side stand-in, so the address is looked up with that device
+// current and passed to the kernels as a plain pointer.  It is cached per
+// device together with the CUDA context it was looked up in: after
+// cudaDeviceReset the device gets a new primary context, in which the module
+// (and the array) is loaded again, so a lookup from another context is redone.
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 float* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (CtxGetCurrentFn)p;
+  }
+  return fn;
+}
 
 cudaError_t scratch_address(int device, float** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (g_scratch_addr[device] == nullptr) {
-    int cur = -1;
-    cudaError_t e = cudaGetDevice(&cur);
-    if (e != cudaSuccess) return e;
-    if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return e;
+  if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+  CUcontext ctx = nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr || get(&ctx) != CUDA_SUCCESS) e = cudaErrorNotSupported;
+  if (e == cudaSuccess && (g_scratch_addr[device] == nullptr || g_scratch_ctx[device] != ctx)) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_attn_scratch);
-    if (cur != device) cudaSetDevice(cur);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[device] = static_cast<float*>(p);
+    if (e == cudaSuccess) {
+      g_scratch_addr[device] = static_cast<float*>(p);
+      g_scratch_ctx[device] = ctx;
+    }
   }
+  if (cur != device) cudaSetDevice(cur);
+  if (e != cudaSuccess) return e;
   *out = g_scratch_addr[device];
   return cudaSuccess;
 }

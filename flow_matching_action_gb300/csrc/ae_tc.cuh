@@ -14,7 +14,9 @@
 namespace ae {
 namespace tc {
 
-// ~1 s at 2 GHz; no correct wait in this library comes near it.
+// Default budget of a bounded wait: ~1 s at 2 GHz; no correct wait in this
+// library comes near it.  ae_selftest_wait_timeout runs the same wait with a
+// caller-chosen budget.
 constexpr long long kWaitBudgetCycles = 2000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -83,13 +85,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 
 // Bounded wait for the phase of `parity` to complete, sleeping between polls.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                int* status) {
+                                                int* status, long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       report(status, kDevTimeout);
       *abort = 1;
       return false;
@@ -98,16 +100,16 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
 }
 
 // Bounded wait for the phase of `parity` to complete.  Returns false (after
-// reporting kDevTimeout and raising *abort) if the budget runs out or another
-// role of the CTA already aborted.
+// reporting kDevTimeout and raising *abort) if `budget` SM cycles pass first
+// or another role of the CTA already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+                                          int* status, long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       report(status, kDevTimeout);
       *abort = 1;
       return false;

@@ -208,6 +208,22 @@ AE_API ae_status ae_sample_noalloc(ae_ctx* ctx, const float* noise, int n_steps,
                                    float* out_actions);
 
 /*
+ * Self-test of device-side failure detection (the pages have no counterpart;
+ * it checks this library's own error path).  The tensor-core kernels bound
+ * every wait on an mbarrier by a cycle budget (about one second); a wait that
+ * runs out records a timeout in the context's sticky device status and the
+ * kernel returns instead of hanging.  This call enqueues one small kernel that
+ * runs that same bounded wait on an mbarrier nothing ever completes, with a
+ * budget of `budget_cycles` SM clock cycles, and with no copy, MMA or TMEM
+ * allocation in flight.  After it, ae_synchronize, ae_last_error and every
+ * later ae_sample of this context report AE_ERR_DEVICE; the status is not
+ * cleared (create a new context to continue).  The GPU and other contexts are
+ * not affected.
+ * Errors: AE_ERR_INVALID_ARG (NULL ctx, budget_cycles < 0), AE_ERR_CUDA.
+ */
+AE_API ae_status ae_selftest_wait_timeout(ae_ctx* ctx, int64_t budget_cycles);
+
+/*
  * Optional per-layer hidden-state dump for parity checks.  When set, every
  * ae_sample writes the fp32 residual stream entering layer l (l = 0..L-1) and
  * leaving the last layer (l = L) of every step s to
