@@ -3,12 +3,33 @@ the oracle on the same inputs, and cache what is expensive to rebuild."""
 from __future__ import annotations
 
 import functools
+import os
 
 import numpy as np
 
 from flow_matching_action_gb300 import synth
 
 MAX_ROWS = 2048
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+GOLDEN_SEEDS = (0, 1, 2, 3, 4)
+
+
+@functools.lru_cache(maxsize=4)
+def golden(name: str) -> np.ndarray:
+    """A stored oracle output (written by tests/golden/make_golden.py from the oracle alone)."""
+    return np.loadtxt(os.path.join(GOLDEN, name))
+
+
+def golden_pad2048(seed: int) -> np.ndarray:
+    """Oracle actions [1, 50, 32] of the 2048-padded Pi0.5 workload of `seed`."""
+    g = golden("pi05_pad2048_actions.txt.gz").reshape(len(GOLDEN_SEEDS), 1, 50, 32)
+    return g[GOLDEN_SEEDS.index(seed)]
+
+
+def golden_b16(seed: int) -> np.ndarray:
+    """Oracle actions [16, 50, 32] of the batch-16 ragged Pi0.5 workload of `seed`."""
+    g = golden("pi05_b16_ragged_actions.txt.gz").reshape(len(GOLDEN_SEEDS), 16, 50, 32)
+    return g[GOLDEN_SEEDS.index(seed)]
 
 
 @functools.lru_cache(maxsize=4)

@@ -12,7 +12,7 @@ import pytest
 
 from flow_matching_action_gb300 import synth
 
-from .helpers import GpuRunner, oracle_actions, rel_l2, weights
+from .helpers import GOLDEN_SEEDS, GpuRunner, golden_b16, golden_pad2048, oracle_actions, rel_l2, weights
 
 pytestmark = pytest.mark.gpu
 
@@ -103,27 +103,52 @@ def test_pi05_masked_slot_equals_two_camera_bitwise(pi05_runner, pi05_two_camera
     np.testing.assert_array_equal(masked, base)
 
 
-@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("seed", GOLDEN_SEEDS)
 def test_pi05_padded_equals_unpadded_bitwise(pi05_runner, seed):
+    """The 2048-padded workload (1621..1634 valid rows, NaN pads) equals its
+    unpadded run bitwise and the oracle's stored actions within 1e-2."""
     padded = pi05_runner.run(synth.pi05_padded(seed, padded=True))
     unpadded = pi05_runner.run(synth.pi05_padded(seed, padded=False))
     assert np.isfinite(padded).all()
     np.testing.assert_array_equal(padded, unpadded)
-    if seed == 0:
-        ref = oracle_actions(synth.pi05_padded(seed, padded=False), weights("pi05"))
-        assert np.abs(padded - ref).max() <= BF16_ACT_TOL
+    err = np.abs(padded - golden_pad2048(seed)).max()
+    assert err <= BF16_ACT_TOL, err
 
 
-def test_pi05_batched_ragged_sampled_requests(pi05_runner):
-    wl = synth.pi05_batched(0)
+def test_pi05_padded_per_layer_hidden(pi05_runner):
+    """Per-layer residual stream of the 2048-padded workload against the oracle's."""
+    wl = synth.pi05_padded(0, padded=True)
+    got, dump = pi05_runner.run(wl, dump=True)
+    ref, ref_dump = oracle_actions(synth.pi05_padded(0, padded=False), weights("pi05"), dump=True)
+    assert np.abs(got - ref).max() <= BF16_ACT_TOL
+    hid = rel_l2(dump, ref_dump, axis=(2, 3, 4))
+    assert hid.max() <= BF16_HID_TOL, hid.max()
+
+
+@pytest.mark.parametrize("seed", GOLDEN_SEEDS)
+def test_pi05_batched_ragged_every_request(pi05_runner, seed):
+    """Batch of 16 ragged prefixes (600..2048 valid rows): every request against
+    the oracle's stored actions."""
+    wl = synth.pi05_batched(seed)
     got = pi05_runner.run(wl)
     assert np.isfinite(got).all()
+    err = np.abs(got - golden_b16(seed)).max(axis=(1, 2))
+    assert err.max() <= BF16_ACT_TOL, err
+
+
+def test_pi05_batched_per_layer_hidden_and_alone(pi05_runner):
+    """Per-layer residual stream of the shortest and the longest request of the
+    batch of 16 against the oracle run on that request alone, and each equal
+    (within tolerance) to the library's own batch-1 run of the request."""
+    wl = synth.pi05_batched(0)
+    got, dump = pi05_runner.run(wl, dump=True)
     lens = wl.n_valid
-    # the oracle, one request at a time, on the shortest and the longest request
     for b in (int(np.argmin(lens)), int(np.argmax(lens))):
         single = synth.pi05_request(0, b, lens[b])
-        ref = oracle_actions(single, weights("pi05"))
+        ref, ref_dump = oracle_actions(single, weights("pi05"), dump=True)
         assert np.abs(got[b] - ref[0]).max() <= BF16_ACT_TOL
+        hid = rel_l2(dump[:, :, b:b + 1], ref_dump, axis=(2, 3, 4))
+        assert hid.max() <= BF16_HID_TOL, (b, hid.max())
         alone = pi05_runner.run(single)
         assert np.abs(got[b] - alone[0]).max() <= BF16_ACT_TOL
 

@@ -15,7 +15,7 @@ import pytest
 
 from flow_matching_action_gb300 import synth
 
-from .helpers import GpuRunner, weights
+from .helpers import GpuRunner, golden_b16, oracle_actions, weights
 
 pytestmark = pytest.mark.gpu
 
@@ -59,10 +59,46 @@ def test_noalloc_matches_sample_tiny_bf16():
 def test_noalloc_matches_sample_pi05_two_camera():
     wl = synth.pi05_two_camera()
     ref, outs, free = _run_pair(synth.PI05, weights("pi05"), wl, max_rows=712)
+    oracle = oracle_actions(wl, weights("pi05"))
     for out in outs[:2]:
         assert np.isfinite(out).all()
         assert np.abs(out - ref).max() <= BF16_ACT_TOL
+        assert np.abs(out - oracle).max() <= BF16_ACT_TOL
     assert free[1] == free[2]
+
+
+def test_noalloc_pi05_batch_of_16():
+    """At batch 16 the fixed scratch holds fewer attention work units than
+    ae_sample would use, so the planner gives each CTA a longer range of key
+    chunks; the result must still match ae_sample and the oracle."""
+    wl = synth.pi05_batched(0)
+    ref, outs, free = _run_pair(synth.PI05, weights("pi05"), wl, max_rows=2048)
+    oracle = golden_b16(0)
+    for out in outs[:2]:
+        assert np.isfinite(out).all()
+        assert np.abs(out - ref).max() <= BF16_ACT_TOL
+        assert np.abs(out - oracle).max() <= BF16_ACT_TOL
+    assert free[1] == free[2]
+
+
+def test_noalloc_rejects_a_batch_beyond_the_fixed_scratch():
+    """32 requests of 4 query tiles each need 128 attention work units; the
+    16 MiB array holds 127 at head_dim 256."""
+    import torch
+    from flow_matching_action_gb300 import ae
+    wl = synth.build_workload("b32", synth.PI05, 1, [[("v", 8)]] * 32, seed=2)
+    r = GpuRunner(synth.PI05, weights("pi05"), max_batch=32, max_rows=8)
+    try:
+        k, v, mask, noise = r.upload(wl)
+        r.expert.bind_prefix(k, v, [int(c) for c in wl.cu_lens], mask)
+        out = torch.empty_like(noise)
+        ae.ae_sample(r.expert.ctx, noise, 1, out)  # builds the table; allowed to allocate
+        with pytest.raises(ae.AEError) as e:
+            ae.ae_sample_noalloc(r.expert.ctx, noise, 1, out)
+        assert e.value.status == -2
+        r.expert.synchronize()
+    finally:
+        r.close()
 
 
 def test_noalloc_rejects_unprepared_steps_and_fp32():
