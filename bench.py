@@ -397,6 +397,7 @@ def main():
     ap.add_argument("--batched", default="pi05_b16", help="second workload reported beside ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--reps", type=int, default=50, help="minimum ae_sample calls in the per-call statistics")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
@@ -446,7 +447,8 @@ def main():
     dist_ctx.barrier()
     ae_build.build()
 
-    res = run_gpu_arm(wl, w, args.steps, args.warmup, dist_ctx, measure_e2e=not args.no_e2e)
+    res = run_gpu_arm(wl, w, args.steps, args.warmup, dist_ctx, measure_e2e=not args.no_e2e,
+                      stat_reps=args.reps)
     total_ms = dist_ctx.max(res["total_ms"])
     ms_per_step = total_ms / args.steps
     chunks = wl.batch * args.steps * dist_ctx.world
@@ -485,7 +487,7 @@ def main():
     if args.batched:
         wl2 = make_workload(args.batched)
         b2, f2 = algorithmic(wl2.dims, wl2.n_valid)
-        reps2 = max(50, args.steps)
+        reps2 = max(args.reps, args.steps)
         r2 = run_gpu_arm(wl2, w, reps2, args.warmup, dist_ctx, measure_e2e=False, stat_reps=reps2)
         s2 = statistics.median(r2["sample_ms"])
         t2 = dist_ctx.max(r2["total_ms"]) / reps2

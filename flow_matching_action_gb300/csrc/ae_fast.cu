@@ -234,7 +234,10 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.scale = (float)(1.0 / sqrt((double)d.dh));
       at.part_o = attn_scratch ? attn_scratch->part_o : c->attn_o;
       at.part_ml = attn_scratch ? attn_scratch->part_ml : c->attn_ml;
-      at.max_units = attn_scratch ? attn_scratch->max_units : 0;
+      // the grid's work units index the partial buffers: keep them within
+      // what those buffers hold (library scratch or the caller's)
+      at.max_units = attn_scratch ? attn_scratch->max_units
+                                  : (int)attn_part_units(c->max_batch, d.H, d.Hq, d.Hkv, c->max_rows, sm);
       at.status = c->status_dev;
       at.q_box = c->q_box_rows;
       // bf16 partials on the default path; callers' own scratch keeps fp32

@@ -164,6 +164,21 @@ def test_pi05_batch_of_three_masked_and_ragged(pi05_runner):
     assert np.abs(got - oracle_actions(wl, weights("pi05"))).max() <= BF16_ACT_TOL
 
 
+def test_pi05_batched_long_request_then_short_ones(pi05_runner):
+    """One 2048-row request, then fifteen of 600 rows.  The attention work
+    split that minimizes the wave makespan here would index more partial
+    units than the partial buffers hold; the planner must lengthen the chunk
+    ranges instead.  The long and the last short request against the oracle
+    (two Euler steps)."""
+    lay = [[("v", 2048)]] + [[("v", 600)] for _ in range(15)]
+    wl = synth.build_workload("pi05_long_then_short", synth.PI05, 2, lay, seed=3)
+    got = pi05_runner.run(wl)
+    assert np.isfinite(got).all()
+    for b in (0, 15):
+        ref = oracle_actions(synth.pi05_request(3, b, wl.n_valid[b], n_steps=2), weights("pi05"))
+        assert np.abs(got[b] - ref[0]).max() <= BF16_ACT_TOL, b
+
+
 def test_pi05_f32_debug_path_matches_oracle():
     """The same Pi0.5 weights, upcast exactly to fp32, through the fp32 path."""
     wl = synth.pi05_two_camera(n_steps=2)
@@ -176,6 +191,28 @@ def test_pi05_f32_debug_path_matches_oracle():
     ref, ref_dump = oracle_actions(wl, w, dump=True)
     assert np.abs(got - ref).max() <= F32_TOL
     assert rel_l2(dump, ref_dump, axis=(2, 3, 4)).max() <= F32_TOL
+
+
+def test_debug_launch_switches_change_nothing(monkeypatch):
+    """AE_GRAPH=0 (kernels launched one by one instead of one graph replay) and
+    AE_PDL=0 (no programmatic dependent launch) are debugging aids read at
+    ae_create: the same kernels run and the actions are bitwise the same."""
+    wl = synth.pi05_masked_slot(n_steps=2)
+    w = weights("pi05")
+    outs = []
+    for env in ({}, {"AE_GRAPH": "0"}, {"AE_GRAPH": "0", "AE_PDL": "0"}):
+        for k in ("AE_GRAPH", "AE_PDL"):
+            monkeypatch.delenv(k, raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        r = GpuRunner(synth.PI05, w, max_batch=1, max_rows=1024)
+        try:
+            outs.append(r.run(wl))
+        finally:
+            r.close()
+    assert np.isfinite(outs[0]).all()
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0])
 
 
 # ------------------------------------------------------------------ bf16 path, small shapes and edges
