@@ -108,15 +108,39 @@ def make_workload(name: str, seed: int = 0):
         return synth.pi05_padded(seed, N_FLOW_STEPS, True)
     if name == "tiny":
         return synth.tiny(seed)
+    if name == "pi05_shared16":
+        return shared_samples(synth.pi05_two_camera(seed, N_FLOW_STEPS), 16, seed)
     raise ValueError(name)
 
 
+def shared_samples(wl, n_samples, seed):
+    """n_samples action samples of the one request of `wl` over its prefix:
+    the prefix is laid out once per sample here only so that the oracle and
+    the flop count see n_samples requests; the GPU arm binds one copy with
+    ae_bind_prefix_shared.  Each sample has its own noise."""
+    import dataclasses
+    from flow_matching_action_gb300 import synth
+    rows = wl.n_rows[0]
+    noise = np.stack([synth.request_noise(wl.dims, seed + 100, s) for s in range(n_samples)])
+    many = dataclasses.replace(
+        wl, name=f"pi05_shared{n_samples}_{rows}", layouts=[list(wl.layouts[0]) for _ in range(n_samples)],
+        prefix_k=np.concatenate([wl.prefix_k] * n_samples, axis=1),
+        prefix_v=np.concatenate([wl.prefix_v] * n_samples, axis=1),
+        mask=np.concatenate([wl.mask] * n_samples), cu_lens=np.arange(n_samples + 1, dtype=np.int32) * rows,
+        noise=noise)
+    many.shared_rows = rows
+    return many
+
+
 def describe(wl) -> str:
+    shared = getattr(wl, "shared_rows", None)
+    prefix = (f"{wl.batch} samples over one shared prefix of {shared} rows ({min(wl.n_valid)} valid)"
+              if shared is not None else
+              f"batch {wl.batch}, valid prefix rows {min(wl.n_valid)}..{max(wl.n_valid)} "
+              f"(physical {sum(wl.n_rows)})")
     return (f"{wl.name}: Pi0.5-shaped action expert L={wl.dims.layers} D={wl.dims.width} "
             f"F={wl.dims.mlp} Hq={wl.dims.n_q_heads} Hkv={wl.dims.n_kv_heads} dh={wl.dims.head_dim}, "
-            f"batch {wl.batch}, valid prefix rows {min(wl.n_valid)}..{max(wl.n_valid)} "
-            f"(physical {sum(wl.n_rows)}), horizon {wl.dims.horizon} x {wl.dims.action_dim}, "
-            f"{wl.n_steps} Euler steps")
+            f"{prefix}, horizon {wl.dims.horizon} x {wl.dims.action_dim}, {wl.n_steps} Euler steps")
 
 
 def _dev(x, dtype):
@@ -137,9 +161,11 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_
     ex = ae.ActionExpert(wl.dims, dev_w, max(wl.batch, 1), max(max(wl.n_rows), 1),
                          stream=stream.cuda_stream)
     del dev_w
-    k = _dev(wl.prefix_k, dtype)
-    v = _dev(wl.prefix_v, dtype)
-    mask = torch.from_numpy(wl.mask).cuda()
+    shared = getattr(wl, "shared_rows", None)
+    rows = shared if shared is not None else None
+    k = _dev(wl.prefix_k[:, :rows], dtype)
+    v = _dev(wl.prefix_v[:, :rows], dtype)
+    mask = torch.from_numpy(wl.mask[:rows]).cuda()
     cu = [int(c) for c in wl.cu_lens]
     rng = np.random.default_rng(123)
     n_noise = 4
@@ -147,8 +173,14 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_
               for _ in range(n_noise)]
     out = torch.empty_like(noises[0])
 
+    def bind():
+        if shared is not None:
+            ex.bind_prefix_shared(wl.batch, k, v, shared, mask)
+        else:
+            ex.bind_prefix(k, v, cu, mask)
+
     def one_step(i):
-        ex.bind_prefix(k, v, cu, mask)
+        bind()
         ex.sample(noises[i % n_noise], wl.n_steps, out)
 
     with torch.cuda.stream(stream):
@@ -172,7 +204,7 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_
         t0.record(stream)
         for i in range(steps):
             starts[i].record(stream)
-            ex.bind_prefix(k, v, cu, mask)
+            bind()
             mids[i].record(stream)
             ex.sample(noises[i % n_noise], wl.n_steps, out)
             ends[i].record(stream)
@@ -188,7 +220,7 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_
         if extra:
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(extra)]
-            ex.bind_prefix(k, v, cu, mask)
+            bind()
             for i in range(extra):
                 ev[i][0].record(stream)
                 ex.sample(noises[i % n_noise], wl.n_steps, out)
@@ -387,6 +419,30 @@ def measured_traffic(workload: str):
     return rec.get("bytes_per_flow_step", {}).get(workload)
 
 
+def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind):
+    """A workload reported beside the headline one, against the bf16 tensor roofline."""
+    wl2 = make_workload(name)
+    b2, f2 = algorithmic(wl2.dims, wl2.n_valid)
+    reps2 = max(args.reps, args.steps)
+    r2 = run_gpu_arm(wl2, w, reps2, args.warmup, dist_ctx, measure_e2e=False, stat_reps=reps2)
+    s2 = statistics.median(r2["sample_ms"])
+    t2 = dist_ctx.max(r2["total_ms"]) / reps2
+    tflops = f2 * wl2.n_steps / (s2 / 1e3) / 1e12
+    return {"workload": describe(wl2), "chunks_per_s": wl2.batch / (t2 / 1e3) * dist_ctx.world,
+            "ms_per_step": t2, "us_per_flow_step": s2 * 1e3 / wl2.n_steps,
+            "sample_ms_median": s2, "sample_ms_p90": float(np.percentile(r2["sample_ms"], 90)),
+            "sample_calls_timed": len(r2["sample_ms"]),
+            "clocks": r2["clocks"],
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
+                         "unit": "TFLOP/s", "frac": tflops / tf_sust,
+                         "peak_burst": tf_burst, "frac_of_burst": tflops / tf_burst,
+                         "peak_kind": f"{peak_kind} sustained cuBLAS bf16 (frac); "
+                                      f"{peak_kind} burst cuBLAS bf16 (frac_of_burst)",
+                         "algorithmic_flops_per_flow_step": f2,
+                         "traffic": measured_traffic(name),
+                         "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,6 +451,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="pi05_b1")
     ap.add_argument("--batched", default="pi05_b16", help="second workload reported beside ('' = none)")
+    ap.add_argument("--shared", default="pi05_shared16",
+                    help="many samples over one shared prefix, reported beside ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--reps", type=int, default=50, help="minimum ae_sample calls in the per-call statistics")
@@ -484,27 +542,9 @@ def main():
         e = res["e2e"]
         line["e2e"] = {"value": chunks / (e["ms"] / 1e3), "unit": "chunks/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
-    if args.batched:
-        wl2 = make_workload(args.batched)
-        b2, f2 = algorithmic(wl2.dims, wl2.n_valid)
-        reps2 = max(args.reps, args.steps)
-        r2 = run_gpu_arm(wl2, w, reps2, args.warmup, dist_ctx, measure_e2e=False, stat_reps=reps2)
-        s2 = statistics.median(r2["sample_ms"])
-        t2 = dist_ctx.max(r2["total_ms"]) / reps2
-        tflops = f2 * wl2.n_steps / (s2 / 1e3) / 1e12
-        line["batched"] = {"workload": describe(wl2), "chunks_per_s": wl2.batch / (t2 / 1e3) * dist_ctx.world,
-                           "ms_per_step": t2, "us_per_flow_step": s2 * 1e3 / wl2.n_steps,
-                           "sample_ms_median": s2, "sample_ms_p90": float(np.percentile(r2["sample_ms"], 90)),
-                           "sample_calls_timed": len(r2["sample_ms"]),
-                           "clocks": r2["clocks"],
-                           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
-                                        "unit": "TFLOP/s", "frac": tflops / tf_sust,
-                                        "peak_burst": tf_burst, "frac_of_burst": tflops / tf_burst,
-                                        "peak_kind": f"{peak_kind} sustained cuBLAS bf16 (frac); "
-                                                     f"{peak_kind} burst cuBLAS bf16 (frac_of_burst)",
-                                        "algorithmic_flops_per_flow_step": f2,
-                                        "traffic": measured_traffic(args.batched),
-                                        "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"}}
+    for key, name in (("batched", args.batched), ("shared_prefix", args.shared)):
+        if name:
+            line[key] = side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind)
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, w)
     if dist_ctx.rank == 0:

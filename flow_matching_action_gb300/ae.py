@@ -60,6 +60,8 @@ _SIGNATURES = {
     "ae_set_stream": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "ae_bind_prefix": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    "ae_bind_prefix_shared": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int32, ctypes.c_void_p]),
     "ae_sample": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "ae_sample_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "ae_set_debug_dump": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
@@ -159,6 +161,11 @@ def ae_bind_prefix(ctx, batch: int, prefix_k, prefix_v, cu_lens: Sequence[int], 
     _check(lib().ae_bind_prefix(ctx, batch, _ptr(prefix_k), _ptr(prefix_v), cu, _ptr(prefix_mask)), ctx)
 
 
+def ae_bind_prefix_shared(ctx, n_samples: int, prefix_k, prefix_v, n_rows: int, prefix_mask=None) -> None:
+    _check(lib().ae_bind_prefix_shared(ctx, n_samples, _ptr(prefix_k), _ptr(prefix_v), int(n_rows),
+                                       _ptr(prefix_mask)), ctx)
+
+
 def ae_sample(ctx, noise, n_steps: int, out_actions) -> None:
     _check(lib().ae_sample(ctx, _ptr(noise), n_steps, _ptr(out_actions)), ctx)
 
@@ -210,6 +217,11 @@ class ActionExpert:
     def bind_prefix(self, prefix_k, prefix_v, cu_lens, prefix_mask=None):
         batch = len(cu_lens) - 1
         ae_bind_prefix(self.ctx, batch, prefix_k, prefix_v, cu_lens, prefix_mask)
+        self._bound = (prefix_k, prefix_v, prefix_mask)
+
+    def bind_prefix_shared(self, n_samples: int, prefix_k, prefix_v, n_rows: int, prefix_mask=None):
+        """One request's prefix bound for n_samples samples of the same observation."""
+        ae_bind_prefix_shared(self.ctx, n_samples, prefix_k, prefix_v, n_rows, prefix_mask)
         self._bound = (prefix_k, prefix_v, prefix_mask)
 
     def sample(self, noise, n_steps: int, out=None):

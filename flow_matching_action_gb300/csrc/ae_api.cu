@@ -256,6 +256,7 @@ ae_status sample_graph(ae_ctx* c, const TimeTable& t, int n_steps, const float* 
   key.pv = c->bind.pv;
   key.total_rows = c->bind.total_rows;
   key.dump = c->dump;
+  key.lens = c->bind.lens;
   if (c->graph_exec == nullptr || !(key == c->graph_key)) {
     if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
     c->graph_exec = nullptr;
@@ -297,6 +298,58 @@ const TimeTable* find_time_table(const ae_ctx* c, int n_steps) {
   return nullptr;
 }
 }  // namespace ae
+
+namespace {
+
+// Bind `batch` requests whose physical row ranges are [lo[b], hi[b]) of prefix
+// K / V with `total` rows per layer (ranges checked by the caller).
+ae_status bind_ranges(ae_ctx* c, int batch, const void* prefix_k, const void* prefix_v, const int* lo,
+                      const int* hi, int64_t total, const uint8_t* prefix_mask) {
+  if (total > 0 && (prefix_k == nullptr || prefix_v == nullptr))
+    return set_msg(c, AE_ERR_INVALID_ARG, "prefix_k / prefix_v is NULL");
+  ae::BindArgs a;
+  memset(&a, 0, sizeof(a));
+  a.batch = batch;
+  for (int b = 0; b < batch; ++b) {
+    a.lo[b] = lo[b];
+    a.hi[b] = hi[b];
+  }
+  a.max_rows = c->max_rows;
+  a.mask = prefix_mask;
+  a.valid_idx = c->valid_idx;
+  a.n_valid = c->n_valid;
+  a.rope_cs = c->rope_cs;
+  a.H = c->d.H;
+  a.half_dh = c->d.dh / 2;
+  a.theta = c->d.theta;
+  a.status = c->status_dev;
+  if (c->fast && total >= 64) {
+    // TMA views of the borrowed prefix K / V (host-side descriptors, no copy);
+    // only chunks of 64 contiguous valid rows use them
+    const long rows = (long)c->d.L * total;
+    cudaError_t e = ae::make_bf16_map(&c->bind.map_pk, prefix_k, rows, c->d.kvdim(), 64);
+    if (e == cudaSuccess) e = ae::make_bf16_map(&c->bind.map_pv, prefix_v, rows, c->d.kvdim(), 64);
+    if (e != cudaSuccess)
+      return set_msg(c, AE_ERR_INVALID_ARG,
+                     "prefix_k / prefix_v cannot be described for TMA (16-byte alignment needed)");
+  }
+  c->launches_bind = ae::launch_bind(a, c->stream);
+  AE_CK(c, cudaGetLastError());
+  c->bind.batch = batch;
+  c->bind.pk = prefix_k;
+  c->bind.pv = prefix_v;
+  c->bind.total_rows = total;
+  c->bind.lens.resize(batch);
+  int longest = 0;
+  for (int b = 0; b < batch; ++b) {
+    c->bind.lens[b] = hi[b] - lo[b];
+    longest = c->bind.lens[b] > longest ? c->bind.lens[b] : longest;
+  }
+  c->bind.max_phys_rows = longest;
+  return AE_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -405,9 +458,7 @@ ae_status ae_bind_prefix(ae_ctx* c, int batch, const void* prefix_k, const void*
   if (batch < 0 || batch > c->max_batch)
     return set_msg(c, AE_ERR_SHAPE, "batch %d outside 0..%d", batch, c->max_batch);
   if (batch > 0 && cu_lens == nullptr) return set_msg(c, AE_ERR_INVALID_ARG, "cu_lens is NULL");
-  ae::BindArgs a;
-  memset(&a, 0, sizeof(a));
-  a.batch = batch;
+  int lo[AE_MAX_BATCH], hi[AE_MAX_BATCH];
   if (batch > 0) {
     if (cu_lens[0] != 0) return set_msg(c, AE_ERR_SHAPE, "cu_lens[0] must be 0");
     for (int b = 0; b < batch; ++b) {
@@ -416,42 +467,26 @@ ae_status ae_bind_prefix(ae_ctx* c, int batch, const void* prefix_k, const void*
       if (len > c->max_rows)
         return set_msg(c, AE_ERR_SHAPE, "request %d has %lld prefix rows > max_prefix_rows %d", b,
                        (long long)len, c->max_rows);
+      lo[b] = cu_lens[b];
+      hi[b] = cu_lens[b + 1];
     }
   }
-  const int64_t total = batch > 0 ? cu_lens[batch] : 0;
-  if (total > 0 && (prefix_k == nullptr || prefix_v == nullptr))
-    return set_msg(c, AE_ERR_INVALID_ARG, "prefix_k / prefix_v is NULL");
-  for (int b = 0; b <= batch; ++b) a.cu[b] = batch > 0 ? cu_lens[b] : 0;
-  a.max_rows = c->max_rows;
-  a.mask = prefix_mask;
-  a.valid_idx = c->valid_idx;
-  a.n_valid = c->n_valid;
-  a.rope_cs = c->rope_cs;
-  a.H = c->d.H;
-  a.half_dh = c->d.dh / 2;
-  a.theta = c->d.theta;
-  a.status = c->status_dev;
-  if (c->fast && total >= 64) {
-    // TMA views of the borrowed prefix K / V (host-side descriptors, no copy);
-    // only chunks of 64 contiguous valid rows use them
-    const long rows = (long)c->d.L * total;
-    cudaError_t e = ae::make_bf16_map(&c->bind.map_pk, prefix_k, rows, c->d.kvdim(), 64);
-    if (e == cudaSuccess) e = ae::make_bf16_map(&c->bind.map_pv, prefix_v, rows, c->d.kvdim(), 64);
-    if (e != cudaSuccess)
-      return set_msg(c, AE_ERR_INVALID_ARG,
-                     "prefix_k / prefix_v cannot be described for TMA (16-byte alignment needed)");
+  return bind_ranges(c, batch, prefix_k, prefix_v, lo, hi, batch > 0 ? cu_lens[batch] : 0, prefix_mask);
+}
+
+ae_status ae_bind_prefix_shared(ae_ctx* c, int n_samples, const void* prefix_k, const void* prefix_v,
+                                int32_t n_rows, const uint8_t* prefix_mask) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  if (n_samples < 0 || n_samples > c->max_batch)
+    return set_msg(c, AE_ERR_SHAPE, "n_samples %d outside 0..%d", n_samples, c->max_batch);
+  if (n_rows < 0 || n_rows > c->max_rows)
+    return set_msg(c, AE_ERR_SHAPE, "n_rows %d outside 0..max_prefix_rows %d", n_rows, c->max_rows);
+  int lo[AE_MAX_BATCH], hi[AE_MAX_BATCH];
+  for (int b = 0; b < n_samples; ++b) {
+    lo[b] = 0;
+    hi[b] = n_rows;
   }
-  c->launches_bind = ae::launch_bind(a, c->stream);
-  AE_CK(c, cudaGetLastError());
-  c->bind.batch = batch;
-  c->bind.pk = prefix_k;
-  c->bind.pv = prefix_v;
-  c->bind.total_rows = total;
-  c->bind.cu.assign(a.cu, a.cu + batch + 1);
-  int longest = 0;
-  for (int b = 0; b < batch; ++b) longest = a.cu[b + 1] - a.cu[b] > longest ? a.cu[b + 1] - a.cu[b] : longest;
-  c->bind.max_phys_rows = longest;
-  return AE_OK;
+  return bind_ranges(c, n_samples, prefix_k, prefix_v, lo, hi, n_samples > 0 ? n_rows : 0, prefix_mask);
 }
 
 ae_status ae_sample(ae_ctx* c, const float* noise, int n_steps, float* out) {

@@ -539,7 +539,7 @@ void attn_plan(AttnArgs& a, int sm_count) {
   a.q_tiles = ((a.Hq / a.Hkv) * fold_rows_per_head(a.H) + 127) / 128;
   const int max_chunks = (a.plan_rows + a.H + kChunk - 1) / kChunk;
   int cpc = 1;
-  if (a.host_cu != nullptr) {
+  if (a.host_lens != nullptr) {
     // Chunk range per CTA that minimizes the makespan of whole waves of one
     // CTA per SM, a CTA costing its chunks plus about two chunks of prologue
     // and partial store (fit to GB300 measurements at batch 16), over the
@@ -548,7 +548,7 @@ void attn_plan(AttnArgs& a, int sm_count) {
     for (int c = 1; c <= max_chunks; ++c) {
       long ctas = 0;
       for (int b = 0; b < a.batch; ++b) {
-        const int ch = (a.host_cu[b + 1] - a.host_cu[b] + a.H + kChunk - 1) / kChunk;
+        const int ch = (a.host_lens[b] + a.H + kChunk - 1) / kChunk;
         ctas += (long)a.Hkv * a.q_tiles * ((ch + c - 1) / c);
       }
       const long cost = ((ctas + sm_count - 1) / sm_count) * (c + 2);

@@ -225,7 +225,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.n_valid = c->n_valid;
       at.max_rows = c->max_rows;
       at.plan_rows = c->bind.max_phys_rows;
-      at.host_cu = c->bind.cu.data();
+      at.host_lens = c->bind.lens.data();
       at.batch = B;
       at.H = d.H;
       at.Hq = d.Hq;

@@ -50,7 +50,7 @@ struct BindState {
   int64_t total_rows = 0;               // rows per layer of pk / pv
   int max_phys_rows = 0;                // longest request of the binding
   CUtensorMap map_pk, map_pv;           // bf16 path: TMA views of pk / pv, boxes 64 rows x 64
-  std::vector<int> cu;                  // host copy of cu_lens
+  std::vector<int> lens;                // physical rows of every request
 };
 
 }  // namespace ae
@@ -132,9 +132,10 @@ struct ae_ctx {
     const void *pk = nullptr, *pv = nullptr;
     int64_t total_rows = 0;
     const float* dump = nullptr;
+    std::vector<int> lens;  // the attention work split depends on every request's length
     bool operator==(const GraphKey& o) const {
       return batch == o.batch && n_steps == o.n_steps && max_phys_rows == o.max_phys_rows &&
-             pk == o.pk && pv == o.pv && total_rows == o.total_rows && dump == o.dump;
+             pk == o.pk && pv == o.pv && total_rows == o.total_rows && dump == o.dump && lens == o.lens;
     }
   } graph_key;
 
@@ -163,11 +164,12 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Parameters of the bind kernel; cu_lens travel by value with the launch.
+// Parameters of the bind kernel; every request's physical row range travels
+// by value with the launch (ranges may coincide: samples sharing one prefix).
 struct BindArgs {
   int batch;
   int max_rows;
-  int cu[AE_MAX_BATCH + 1];
+  int lo[AE_MAX_BATCH], hi[AE_MAX_BATCH];  // request b owns physical rows [lo[b], hi[b])
   const uint8_t* mask;
   int* valid_idx;
   int* n_valid;
@@ -243,7 +245,7 @@ struct AttnArgs {
   const int* n_valid;     // [batch]
   int max_rows;           // row stride of valid_idx
   int plan_rows;          // longest physical prefix of the bound requests (work split bound)
-  const int* host_cu;     // host copy of the binding's cu_lens (batch + 1), for the work split; may be null
+  const int* host_lens;   // host copy of every request's physical row count, for the work split; may be null
   int layer_row0;         // first row of this layer in the prefix K/V maps
   int batch, H, Hq, Hkv, dh;
   float scale;

@@ -48,7 +48,7 @@ __device__ float block_sum(float v) {
 // action token i of request b sits at position n_b + i.
 __global__ void k_bind(BindArgs a) {
   const int b = blockIdx.x;
-  const int r0 = a.cu[b], r1 = a.cu[b + 1];
+  const int r0 = a.lo[b], r1 = a.hi[b];
   __shared__ int warp_cnt[32];
   __shared__ int s_base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;

@@ -166,6 +166,24 @@ AE_API ae_status ae_bind_prefix(ae_ctx* ctx, int batch, const void* prefix_k,
                          const uint8_t* prefix_mask);
 
 /*
+ * Bind ONE request's VLM prefix KV for n_samples action samples of the same
+ * observation (OxyGen, "Cross-task KV Sharing": the prefill's KV is a shared
+ * resource that every consumer reads in place).  Every sample attends to the
+ * same prefix rows; each has its own noise and actions in ae_sample
+ * ([n_samples][horizon][action_dim]).  The result equals ae_bind_prefix of
+ * n_samples copies of the prefix, without the copies: the K/V stay in one
+ * place and are read by all samples' attention work.
+ *   prefix_k, prefix_v  device T [layers][n_rows][Hkv*dh], K already rotated
+ *   n_rows              physical rows per layer, 0..max_prefix_rows
+ *   prefix_mask         device uint8 [n_rows] (1 = valid) or NULL
+ * Lifetime rules, positions and errors as for ae_bind_prefix (n_samples plays
+ * the part of batch: AE_ERR_SHAPE above max_batch).
+ */
+AE_API ae_status ae_bind_prefix_shared(ae_ctx* ctx, int n_samples, const void* prefix_k,
+                                const void* prefix_v, int32_t n_rows,
+                                const uint8_t* prefix_mask);
+
+/*
  * Run n_steps Euler steps of delta = -1/n_steps from t = 1 for every bound
  * request (MolmoBot Part 2), the velocity of step k taken at t = 1 - k/n_steps.
  *   noise        device fp32 [batch][horizon][action_dim], the state at t = 1

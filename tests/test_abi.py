@@ -77,6 +77,7 @@ def test_create_rejects_null_weights_and_bad_batch(lib):
 def test_calls_on_null_context_are_rejected(lib):
     assert lib.ae_sample(None, None, 1, None) == -1
     assert lib.ae_bind_prefix(None, 0, None, None, None, None) == -1
+    assert lib.ae_bind_prefix_shared(None, 1, None, None, 10, None) == -1
     assert lib.ae_synchronize(None) == -1
     lib.ae_destroy(None)  # ignored
 
