@@ -16,6 +16,8 @@ No dataset is read; every tensor is N(0, sigma) from a counter-seeded
 * stream ``[seed, 1]``       prefix lengths (only where a workload draws them)
 * stream ``[seed, 2, b]``    valid prefix K then V rows of request ``b``
 * stream ``[seed, 3, b]``    initial noise of request ``b``
+* stream ``[seed, 4]``       context K/V projection weights (cross-attention form)
+* stream ``[seed, 5, b]``    valid context hidden-state rows of request ``b``
 
 Because request ``b`` owns its own streams, request ``b`` of a batch is the
 same as a batch-1 workload built from the same ``(seed, b)``.
@@ -47,6 +49,7 @@ class ExpertDims:
     rope_theta: float = 10000.0
     time_min_period: float = 4e-3
     time_max_period: float = 4.0
+    ctx_dim: int = 0    # C, width of the VLM hidden states projected into K/V (0: none)
 
     @property
     def q_dim(self) -> int:
@@ -152,6 +155,39 @@ def make_weights(d: ExpertDims, seed: int = 0) -> Dict[str, object]:
     return w
 
 
+def make_context_weights(d: ExpertDims, seed: int = 0) -> Dict[str, List[np.ndarray]]:
+    """Per-layer context projections w_ck, w_cv [Hkv*dh, C], N(0, 0.02), from
+    their own stream (the expert's other weights are unchanged by them)."""
+    rng = np.random.default_rng([seed, 4])
+    w: Dict[str, List[np.ndarray]] = {"w_ck": [], "w_cv": []}
+    for _ in range(d.layers):
+        w["w_ck"].append(_store(d, _normal(rng, (d.kv_dim, d.ctx_dim), WEIGHT_STD)))
+        w["w_cv"].append(_store(d, _normal(rng, (d.kv_dim, d.ctx_dim), WEIGHT_STD)))
+    return w
+
+
+def build_context_workload(name: str, d: ExpertDims, n_steps: int, layouts, seed: int = 0,
+                           fill=np.nan) -> "Workload":
+    """As build_workload, but every request's prefix arrives as per-layer VLM
+    hidden states ``context`` [L, total_rows, C] (N(0, 1) valid rows from
+    stream [seed, 5, b], ``fill`` elsewhere) instead of pre-projected K/V."""
+    wl = build_workload(name, d, n_steps, layouts, seed, fill)
+    total = int(sum(wl.n_rows))
+    ctx = np.full((d.layers, total, d.ctx_dim), fill, dtype=np.float32)
+    for b, lay in enumerate(wl.layouts):
+        rng = np.random.default_rng([seed, 5, b])
+        rows = _store(d, _normal(rng, (d.layers, wl.n_valid[b], d.ctx_dim)))
+        phys, used = int(wl.cu_lens[b]), 0
+        for kind, n in lay:
+            if kind == "v":
+                ctx[:, phys:phys + n] = rows[:, used:used + n]
+                used += n
+            phys += n
+    wl.context = ctx
+    wl.prefix_k = wl.prefix_v = None
+    return wl
+
+
 # A request's prefix layout is a list of segments ("v", n) for n valid rows or
 # ("m", n) for n masked / padded rows.  Valid rows are consumed in order, so two
 # layouts with the same total of valid rows hold the same valid K/V.
@@ -171,6 +207,7 @@ class Workload:
     mask: np.ndarray = None           # [total_rows] uint8, 1 = valid
     cu_lens: np.ndarray = None        # [batch + 1] int32 physical row offsets
     noise: np.ndarray = None          # [batch, horizon, action_dim] float32
+    context: np.ndarray = None        # [layers, total_rows, ctx_dim] hidden states (context workloads)
 
     @property
     def batch(self) -> int:
@@ -285,3 +322,22 @@ def pi05_request(seed: int, b: int, n_valid: int, n_steps: int = 10) -> Workload
     wl.prefix_k[:], wl.prefix_v[:] = k, v
     wl.noise = request_noise(PI05, seed, b)[None]
     return wl
+
+
+# Context (cross-attention) workloads: the same expert with C = 2048-wide VLM
+# hidden states (a Gemma-2B-sized VLM, as in Pi0.5) projected into the prefix
+# K/V at bind time; the tiny case uses C = 128.
+TINY_CTX = dataclasses.replace(TINY, ctx_dim=128)
+PI05_CTX = dataclasses.replace(PI05, ctx_dim=2048)
+
+
+def tiny_context(seed: int = 0, kind: str = "plain") -> Workload:
+    lay = {"plain": [("v", 48)], "masked": [("v", 16), ("m", 16), ("v", 32)],
+           "padded": [("v", 48), ("m", 16)]}[kind]
+    return build_context_workload(f"tiny_ctx_{kind}", TINY_CTX, 2, [lay], seed)
+
+
+def pi05_context(seed: int = 0, n_steps: int = 10, padded: bool = False) -> Workload:
+    """The two-camera 712-row prefix as 2048-wide hidden states (optionally padded to 968 rows)."""
+    lay = [("v", 512), ("m", 256), ("v", 200)] if padded else [("v", 712)]
+    return build_context_workload("pi05_ctx_712" + ("_masked" if padded else ""), PI05_CTX, n_steps, [lay], seed)

@@ -27,6 +27,10 @@ Sources (page title, section):
 * [sglang] sglang PR #34599 summary, implementation items 1-2 (merged Q/K/V and
   gate/up projections; mask, positions and sinusoidal time scaling computed once
   per request instead of once per step).
+* [MolmoBot] Part 2 also describes the cross-attention form of the prefix: the
+  VLM hands over per-layer hidden states of its context, and the action expert
+  projects them into K/V; the fix computes that projection once per query and
+  reuses it for every flow step (``project_request``, ``sample(context=...)``).
 
 Parity status of each function is listed in ``PINS``: every function has a
 test that pins it to something other than itself, except the end-to-end action
@@ -48,6 +52,8 @@ PINS = {
     "gelu_tanh": "tests/test_oracle_pins.py: torch gelu(approximate='tanh')",
     "attention": "tests/test_oracle_pins.py: brute-force joint prefix-LM attention via torch SDPA",
     "expert_layer": "tests/test_oracle_pins.py: identity modulation equals a standard pre-norm block",
+    "project_request": "tests/test_oracle_pins.py: torch F.linear + complex-rotation RoPE, identity "
+                       "weights reduce to rope(), masked rows skipped, projected once == recomputed",
     "sample": "tests/test_oracle_pins.py: zero velocity, constant velocity closed form, pad/mask "
               "invariance (bitwise), hoisted == recomputed (bitwise), batch independence; "
               "end-to-end values: parity unpinned (no page prints an expected action)",
@@ -218,6 +224,39 @@ def bind_request(prefix_k, prefix_v, mask, row0: int, row1: int):
     return prefix_k[:, idx, :], prefix_v[:, idx, :], int(idx.size)
 
 
+def project_request(dims, hidden, w_ck, w_cv, mask, row0: int, row1: int):
+    """Cross-attention K/V of one request's VLM context ([MolmoBot] Part 2).
+
+    hidden: [L, total_rows, C] per-layer hidden states of the packed context
+    (rows outside the request's valid set may hold anything, NaN included);
+    w_ck, w_cv: per layer [Hkv*dh, C].  For layer l and the request's valid
+    rows in order (the same valid set and order as ``bind_request``):
+        K = RoPE(hidden W_ck^T) at positions 0..n-1,   V = hidden W_cv^T.
+    Readings: no bias (Gemma style); the projected K is rotated at the row's
+    position among the request's valid rows, which is the convention the
+    joint attention of this path already assumes for a pre-projected prefix
+    (prefix keys rotated at their positions, action token i at n + i), so a
+    projected context is used exactly like a bound prefix.  Returns
+    (K [L, n, Hkv*dh], V [L, n, Hkv*dh], n).
+    """
+    if mask is None:
+        idx = np.arange(row0, row1)
+    else:
+        idx = row0 + np.nonzero(np.asarray(mask[row0:row1]))[0]
+    n = int(idx.size)
+    hkv, dh = dims.n_kv_heads, dims.head_dim
+    L = len(w_ck)
+    ks = np.empty((L, n, hkv * dh))
+    vs = np.empty((L, n, hkv * dh))
+    pos = np.arange(n, dtype=np.float64)
+    for l in range(L):
+        x = _f64(hidden[l, idx, :])                                   # [n, C]
+        k = (x @ _f64(w_ck[l]).T).reshape(n, hkv, dh).transpose(1, 0, 2)
+        ks[l] = rope(k, pos, dims.rope_theta).transpose(1, 0, 2).reshape(n, hkv * dh)
+        vs[l] = x @ _f64(w_cv[l]).T
+    return ks, vs, n
+
+
 def step_times(n_steps: int) -> List[float]:
     """Euler schedule: n_steps steps of delta = -1/n_steps from t = 1.
 
@@ -229,7 +268,7 @@ def step_times(n_steps: int) -> List[float]:
 
 
 def sample(dims, w: Dict, prefix_k, prefix_v, cu_lens, mask, noise, n_steps: int,
-           hoist: bool = True, dump: Optional[np.ndarray] = None) -> np.ndarray:
+           hoist: bool = True, dump: Optional[np.ndarray] = None, context=None) -> np.ndarray:
     """Integrate the action chunk of every request from ``noise`` for ``n_steps`` Euler steps.
 
     prefix_k, prefix_v: [L, total_rows, Hkv*dh]; cu_lens: [B+1] physical row
@@ -244,6 +283,11 @@ def sample(dims, w: Dict, prefix_k, prefix_v, cu_lens, mask, noise, n_steps: int
     the residual stream entering each layer and leaving the last one.
     Requests are processed one at a time: request b's result does not depend
     on the others.
+
+    ``context=(hidden, w_ck, w_cv)`` replaces prefix_k / prefix_v by the
+    cross-attention K/V projected from the per-layer hidden states
+    (``project_request``): once per request when hoisted, as [MolmoBot] Part 2
+    does, or again in every step and layer when not.
     """
     B = len(cu_lens) - 1
     x_all = _f64(noise).copy()
@@ -257,10 +301,17 @@ def sample(dims, w: Dict, prefix_k, prefix_v, cu_lens, mask, noise, n_steps: int
         return time_mlp(e, w["w_t1"], w["b_t1"], w["w_t2"], w["b_t2"])
 
     hoisted_c = [cond(t) for t in times] if hoist else None
+
+    def bind(r0, r1):
+        if context is not None:
+            hidden, w_ck, w_cv = context
+            return project_request(dims, hidden, w_ck, w_cv, mask, r0, r1)
+        return bind_request(prefix_k, prefix_v, mask, r0, r1)
+
     for b in range(B):
         r0, r1 = int(cu_lens[b]), int(cu_lens[b + 1])
         if hoist:
-            kp, vp, n = bind_request(prefix_k, prefix_v, mask, r0, r1)
+            kp, vp, n = bind(r0, r1)
             positions = n + np.arange(H, dtype=np.float64)
         x = x_all[b]
         for s, t in enumerate(times):
@@ -270,7 +321,7 @@ def sample(dims, w: Dict, prefix_k, prefix_v, cu_lens, mask, noise, n_steps: int
                 if dump is not None:
                     dump[s, l, b] = h
                 if not hoist:
-                    kp, vp, n = bind_request(prefix_k, prefix_v, mask, r0, r1)
+                    kp, vp, n = bind(r0, r1)
                     positions = n + np.arange(H, dtype=np.float64)
                     c = cond(t)
                 m1 = modulation(c, w["w_mod1"][l], w["b_mod1"][l], 3)

@@ -353,3 +353,69 @@ def test_golden_tiny_regression():
     path = os.path.join(os.path.dirname(__file__), "golden", "tiny_actions.txt")
     ref = np.loadtxt(path).reshape(1, synth.TINY.horizon, synth.TINY.action_dim)
     np.testing.assert_allclose(_run(synth.tiny()), ref, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- context projection
+def _ctx_run(wl, w, wc, hoist=True):
+    return O.sample(wl.dims, w, None, None, wl.cu_lens, wl.mask, wl.noise, wl.n_steps, hoist=hoist,
+                    context=(wl.context, wc["w_ck"], wc["w_cv"]))
+
+
+def test_project_request_matches_torch_linear_and_complex_rotation():
+    d = synth.TINY_CTX
+    wl = synth.tiny_context(1, "masked")
+    wc = synth.make_context_weights(d, 1)
+    ks, vs, n = O.project_request(d, wl.context, wc["w_ck"], wc["w_cv"], wl.mask, 0, wl.n_rows[0])
+    idx = np.nonzero(wl.mask)[0]
+    assert n == idx.size == 48
+    half = d.head_dim // 2
+    freq = 1.0 / d.rope_theta ** (np.arange(0, d.head_dim, 2) / d.head_dim)
+    for l in range(d.layers):
+        x = T(wl.context[l, idx])
+        k = F.linear(x, T(wc["w_ck"][l])).numpy()
+        v = F.linear(x, T(wc["w_cv"][l])).numpy()
+        z = k[:, :half] + 1j * k[:, half:]
+        zr = z * np.exp(1j * np.arange(n)[:, None] * freq[None, :])
+        np.testing.assert_allclose(ks[l], np.concatenate([zr.real, zr.imag], -1), rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(vs[l], v, rtol=1e-12, atol=1e-12)
+
+
+def test_project_request_identity_weights_reduce_to_rope():
+    import dataclasses
+    d = dataclasses.replace(synth.TINY_CTX, ctx_dim=synth.TINY.kv_dim)
+    rng = np.random.default_rng(5)
+    hidden = rng.standard_normal((d.layers, 10, d.ctx_dim))
+    eye = [np.eye(d.kv_dim)] * d.layers
+    ks, vs, n = O.project_request(d, hidden, eye, eye, None, 0, 10)
+    np.testing.assert_array_equal(vs, hidden)
+    for l in range(d.layers):
+        np.testing.assert_allclose(ks[l], O.rope(hidden[l], np.arange(10.0), d.rope_theta), rtol=1e-13)
+
+
+def test_context_projected_once_equals_recomputed_bitwise():
+    d = synth.TINY_CTX
+    wl = synth.tiny_context(2, "masked")
+    w, wc = synth.make_weights(d, 2), synth.make_context_weights(d, 2)
+    np.testing.assert_array_equal(_ctx_run(wl, w, wc, hoist=True), _ctx_run(wl, w, wc, hoist=False))
+
+
+def test_context_masked_and_padded_rows_are_skipped_bitwise():
+    d = synth.TINY_CTX
+    w, wc = synth.make_weights(d, 0), synth.make_context_weights(d, 0)
+    outs = {k: _ctx_run(synth.tiny_context(0, k), w, wc) for k in ("plain", "masked", "padded")}
+    assert np.isfinite(outs["masked"]).all()      # NaN hidden rows never projected
+    np.testing.assert_array_equal(outs["masked"], outs["plain"])
+    np.testing.assert_array_equal(outs["padded"], outs["plain"])
+
+
+def test_context_equals_its_projection_bound_as_prefix_bitwise():
+    d = synth.TINY_CTX
+    wl = synth.tiny_context(3, "padded")
+    w, wc = synth.make_weights(d, 3), synth.make_context_weights(d, 3)
+    ks, vs, n = O.project_request(d, wl.context, wc["w_ck"], wc["w_cv"], wl.mask, 0, wl.n_rows[0])
+    pk = np.full((d.layers, wl.n_rows[0], d.kv_dim), np.nan)
+    pv = pk.copy()
+    idx = np.nonzero(wl.mask)[0]
+    pk[:, idx], pv[:, idx] = ks, vs
+    ref = O.sample(d, w, pk, pv, wl.cu_lens, wl.mask, wl.noise, wl.n_steps)
+    np.testing.assert_array_equal(_ctx_run(wl, w, wc), ref)
