@@ -35,16 +35,17 @@ class ae_config(ctypes.Structure):
                 ("action_dim", ctypes.c_int), ("horizon", ctypes.c_int),
                 ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double),
                 ("time_min_period", ctypes.c_double), ("time_max_period", ctypes.c_double),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("ctx_dim", ctypes.c_int)]
 
 
 _GLOBAL = ("w_in", "b_in", "w_t1", "b_t1", "w_t2", "b_t2", "w_mod_f", "b_mod_f", "w_out", "b_out")
 _LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "w_mod1", "b_mod1", "w_mod2", "b_mod2")
+_CONTEXT = ("w_ck", "w_cv")  # per layer, only with ctx_dim > 0
 
 
 class ae_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _GLOBAL] + \
-               [(n, ctypes.POINTER(ctypes.c_void_p)) for n in _LAYER]
+               [(n, ctypes.POINTER(ctypes.c_void_p)) for n in _LAYER + _CONTEXT]
 
 
 class ae_info(ctypes.Structure):
@@ -62,6 +63,8 @@ _SIGNATURES = {
                                       ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
     "ae_bind_prefix_shared": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_int32, ctypes.c_void_p]),
+    "ae_bind_context": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                       ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
     "ae_sample": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "ae_sample_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "ae_set_debug_dump": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
@@ -119,7 +122,7 @@ def make_config(dims, dtype: Optional[str] = None) -> ae_config:
     return ae_config(dims.layers, dims.width, dims.mlp, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
                      dims.action_dim, dims.horizon, dims.rms_eps, dims.rope_theta,
                      dims.time_min_period, dims.time_max_period,
-                     AE_DTYPE_BF16 if dt == "bf16" else AE_DTYPE_F32)
+                     AE_DTYPE_BF16 if dt == "bf16" else AE_DTYPE_F32, getattr(dims, "ctx_dim", 0))
 
 
 def make_weights(w: Dict) -> ae_weights:
@@ -131,7 +134,9 @@ def make_weights(w: Dict) -> ae_weights:
     keep = []
     for n in _GLOBAL:
         setattr(s, n, _ptr(w[n]))
-    for n in _LAYER:
+    for n in _LAYER + _CONTEXT:
+        if n not in w:  # context projections are optional
+            continue
         arr = (ctypes.c_void_p * len(w[n]))(*[_ptr(t) for t in w[n]])
         keep.append(arr)
         setattr(s, n, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
@@ -164,6 +169,11 @@ def ae_bind_prefix(ctx, batch: int, prefix_k, prefix_v, cu_lens: Sequence[int], 
 def ae_bind_prefix_shared(ctx, n_samples: int, prefix_k, prefix_v, n_rows: int, prefix_mask=None) -> None:
     _check(lib().ae_bind_prefix_shared(ctx, n_samples, _ptr(prefix_k), _ptr(prefix_v), int(n_rows),
                                        _ptr(prefix_mask)), ctx)
+
+
+def ae_bind_context(ctx, batch: int, hidden, cu_lens: Sequence[int], prefix_mask=None) -> None:
+    cu = (ctypes.c_int32 * (len(cu_lens)))(*[int(v) for v in cu_lens]) if cu_lens is not None else None
+    _check(lib().ae_bind_context(ctx, batch, _ptr(hidden), cu, _ptr(prefix_mask)), ctx)
 
 
 def ae_sample(ctx, noise, n_steps: int, out_actions) -> None:
@@ -218,6 +228,11 @@ class ActionExpert:
         batch = len(cu_lens) - 1
         ae_bind_prefix(self.ctx, batch, prefix_k, prefix_v, cu_lens, prefix_mask)
         self._bound = (prefix_k, prefix_v, prefix_mask)
+
+    def bind_context(self, hidden, cu_lens, prefix_mask=None):
+        """Per-layer VLM hidden states projected into K/V once, then bound."""
+        ae_bind_context(self.ctx, len(cu_lens) - 1, hidden, cu_lens, prefix_mask)
+        self._bound = (None, None, prefix_mask)
 
     def bind_prefix_shared(self, n_samples: int, prefix_k, prefix_v, n_rows: int, prefix_mask=None):
         """One request's prefix bound for n_samples samples of the same observation."""

@@ -73,6 +73,8 @@ ae_status check_config(const ae_config* cfg) {
   if (!(cfg->rms_eps > 0.0) || !(cfg->rope_theta > 0.0) || !(cfg->time_min_period > 0.0) ||
       !(cfg->time_max_period > 0.0))
     return set_msg(nullptr, AE_ERR_INVALID_ARG, "eps, rope_theta and time periods must be > 0");
+  if (cfg->ctx_dim < 0 || cfg->ctx_dim % 8 != 0)
+    return set_msg(nullptr, AE_ERR_SHAPE, "ctx_dim must be 0 or a positive multiple of 8");
   return AE_OK;
 }
 
@@ -89,6 +91,13 @@ ae_status check_weights(const ae_config* cfg, const ae_weights* w) {
       if (arr[l] == nullptr)
         return set_msg(nullptr, AE_ERR_INVALID_ARG, "per-layer weight pointer of layer %d is NULL", l);
   }
+  if (cfg->ctx_dim > 0)
+    for (const void* const* arr : {w->w_ck, w->w_cv}) {
+      if (arr == nullptr) return set_msg(nullptr, AE_ERR_INVALID_ARG, "w_ck / w_cv is NULL while ctx_dim > 0");
+      for (int l = 0; l < cfg->layers; ++l)
+        if (arr[l] == nullptr)
+          return set_msg(nullptr, AE_ERR_INVALID_ARG, "w_ck / w_cv pointer of layer %d is NULL", l);
+    }
   return AE_OK;
 }
 
@@ -174,6 +183,31 @@ ae_status pack_weights(ae_ctx* c, const ae_weights* w) {
     AE_TRY(put(c, bmod + (l * 2 + 0) * 3 * D * es, w->b_mod1[l], 3 * D * es));
     AE_TRY(put(c, bmod + (l * 2 + 1) * 3 * D * es, w->b_mod2[l], 3 * D * es));
   }
+  if (d.C > 0) {
+    // context projections, per layer [K rows | V rows] of [2 Hkv dh, C]; on the
+    // tensor-core path every head's rows as rotation pairs (as for Q/K/V above)
+    const size_t C = d.C, crow = C * es, kvd = d.kvdim();
+    c->ctx_tc = c->fast && kvd % 128 == 0 && C % 64 == 0;
+    AE_TRY(alloc(c, &c->w_ctx, L * 2 * kvd * crow));
+    for (size_t l = 0; l < L; ++l) {
+      char* dst0 = (char*)c->w_ctx + l * 2 * kvd * crow;
+      const void* srcs[2] = {w->w_ck[l], w->w_cv[l]};
+      for (int part = 0; part < 2; ++part) {
+        char* dst = dst0 + part * kvd * crow;
+        if (!c->ctx_tc) {
+          AE_TRY(put(c, dst, srcs[part], kvd * crow));
+          continue;
+        }
+        for (size_t h = 0; h < (size_t)d.Hkv; ++h) {
+          const char* src = (const char*)srcs[part] + h * dh * crow;
+          char* hd = dst + h * dh * crow;
+          AE_CK(c, cudaMemcpy2DAsync(hd, 2 * crow, src, crow, crow, dh / 2, cudaMemcpyDefault, c->stream));
+          AE_CK(c, cudaMemcpy2DAsync(hd + crow, 2 * crow, src + dh / 2 * crow, crow, crow, dh / 2,
+                                     cudaMemcpyDefault, c->stream));
+        }
+      }
+    }
+  }
   return AE_OK;
 }
 
@@ -197,6 +231,14 @@ ae_status alloc_scratch(ae_ctx* c) {
     AE_TRY(alloc(c, &c->attn_o, units * 128 * d.dh * sizeof(float)));
     AE_TRY(alloc(c, &c->attn_ml, units * 128 * sizeof(float2)));
     AE_TRY(alloc(c, &c->x, M * d.A * sizeof(float)));
+  }
+  if (d.C > 0) {
+    // projected context K / V of up to max_batch requests of max_rows rows
+    const size_t rows = (size_t)c->max_batch * (c->max_rows > 0 ? c->max_rows : 1);
+    AE_TRY(alloc(c, &c->ctx_k, (size_t)d.L * rows * d.kvdim() * es));
+    AE_TRY(alloc(c, &c->ctx_v, (size_t)d.L * rows * d.kvdim() * es));
+    if (c->ctx_tc) AE_TRY(alloc(c, &c->ctx_rope, rows * (d.dh / 2) * sizeof(float2)));
+    else AE_TRY(alloc(c, &c->ctx_tmp, rows * 2 * d.kvdim() * sizeof(float)));
   }
   return AE_OK;
 }
@@ -393,7 +435,7 @@ ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
   ae_ctx* c = new ae_ctx();
   c->d = Dims{cfg->layers, cfg->width, cfg->mlp, cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim,
               cfg->action_dim, cfg->horizon, cfg->rms_eps, cfg->rope_theta,
-              cfg->time_min_period, cfg->time_max_period, cfg->dtype};
+              cfg->time_min_period, cfg->time_max_period, cfg->dtype, cfg->ctx_dim};
   c->max_batch = max_batch;
   c->max_rows = max_prefix_rows;
   c->stream = (cudaStream_t)stream;
@@ -487,6 +529,53 @@ ae_status ae_bind_prefix_shared(ae_ctx* c, int n_samples, const void* prefix_k, 
     hi[b] = n_rows;
   }
   return bind_ranges(c, n_samples, prefix_k, prefix_v, lo, hi, n_samples > 0 ? n_rows : 0, prefix_mask);
+}
+
+ae_status ae_bind_context(ae_ctx* c, int batch, const void* hidden, const int32_t* cu_lens,
+                          const uint8_t* prefix_mask) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  const Dims& d = c->d;
+  if (d.C <= 0) return set_msg(c, AE_ERR_UNSUPPORTED, "the context was created with ctx_dim 0");
+  if (batch < 0 || batch > c->max_batch)
+    return set_msg(c, AE_ERR_SHAPE, "batch %d outside 0..%d", batch, c->max_batch);
+  if (batch > 0 && cu_lens == nullptr) return set_msg(c, AE_ERR_INVALID_ARG, "cu_lens is NULL");
+  int lo[AE_MAX_BATCH], hi[AE_MAX_BATCH];
+  if (batch > 0) {
+    if (cu_lens[0] != 0) return set_msg(c, AE_ERR_SHAPE, "cu_lens[0] must be 0");
+    for (int b = 0; b < batch; ++b) {
+      const int64_t len = (int64_t)cu_lens[b + 1] - cu_lens[b];
+      if (len < 0) return set_msg(c, AE_ERR_SHAPE, "cu_lens decreases at request %d", b);
+      if (len > c->max_rows)
+        return set_msg(c, AE_ERR_SHAPE, "request %d has %lld rows > max_prefix_rows %d", b, (long long)len,
+                       c->max_rows);
+      lo[b] = cu_lens[b];
+      hi[b] = cu_lens[b + 1];
+    }
+  }
+  const int64_t total = batch > 0 ? cu_lens[batch] : 0;
+  if (total > 0 && hidden == nullptr) return set_msg(c, AE_ERR_INVALID_ARG, "hidden is NULL");
+  // the projected K / V live in the library's buffers, laid out for this
+  // binding ([L][total][Hkv dh]), and are bound like a caller's prefix
+  AE_TRY(bind_ranges(c, batch, c->ctx_k, c->ctx_v, lo, hi, total, prefix_mask));
+  if (total == 0) return AE_OK;
+  int64_t n = 0;
+  const size_t es = elem_size(d.dtype);
+  if (c->ctx_tc) {
+    n += ae::launch_ctx_rope(c->valid_idx, c->n_valid, batch, c->max_rows, d.dh / 2, d.theta, c->ctx_rope,
+                             c->stream);
+    cudaError_t e = cudaSuccess;
+    n += ae::launch_ctx_project_tc(c, hidden, total, c->stream, &e);
+    if (e != cudaSuccess) return cuda_fail(c, e, "context projection");
+  } else {
+    const size_t kv_layer = (size_t)total * d.kvdim() * es;
+    for (int l = 0; l < d.L; ++l)
+      n += ae::launch_ctx_project_simt(c, (const char*)hidden + (size_t)l * total * d.C * es, total,
+                                       (const char*)c->w_ctx + (size_t)l * 2 * d.kvdim() * d.C * es,
+                                       (char*)c->ctx_k + l * kv_layer, (char*)c->ctx_v + l * kv_layer, c->stream);
+  }
+  AE_CK(c, cudaGetLastError());
+  c->launches_bind += n;
+  return AE_OK;
 }
 
 ae_status ae_sample(ae_ctx* c, const float* noise, int n_steps, float* out) {

@@ -82,6 +82,8 @@ cudaError_t fast_setup(ae_ctx* c) {
   const int hp = (d.H + 15) & ~15;
   c->q_box_rows = hp % 64 == 0 ? 64 : (hp % 32 == 0 ? 32 : 16);
   if ((e = make_map(&c->map_qtile, c->qkv, maxM, d.qkvdim(), c->q_box_rows)) != cudaSuccess) return e;
+  if (c->ctx_tc && (e = make_map(&c->map_wctx, c->w_ctx, (long)d.L * 2 * d.kvdim(), d.C, 128)) != cudaSuccess)
+    return e;
   const size_t units = attn_part_units(c->max_batch, d.H, d.Hq, d.Hkv, c->max_rows, c->sm_count);
   if ((e = make_attn_o_map(&c->map_attn_o, c->attn_o, units, d.dh)) != cudaSuccess) return e;
   return make_attn_o16_map(&c->map_attn_o16, c->attn_o, units, d.dh);
@@ -282,6 +284,53 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   ck(launch_final_bf16(c, t, step, x, s, pdl));
   ++n;
   ck(cudaGetLastError());
+  return n;
+}
+
+// Context projection on the tensor cores (ae_bind_context, MolmoBot PR,
+// Part 2): per layer, K = hidden W_ck^T with RoPE at the rows' positions and
+// V = hidden W_cv^T, as two GEMMs whose epilogue is the QKV epilogue without
+// adaRMS (no norm, no shift): every physical row of the stacked hidden states
+// [L * rows, C] is a token; masked rows yield values nothing reads.  The
+// K split is fixed (kCtxSplit), not chosen from the row count: the projection
+// of a valid row then sums in the same order however many masked or padded
+// rows the binding has, so padded and unpadded contexts agree bitwise.
+constexpr int kCtxSplit = 4;
+
+int launch_ctx_project_tc(ae_ctx* c, const void* hidden, int64_t rows, cudaStream_t s, cudaError_t* err) {
+  const Dims& d = c->d;
+  const int kvd = d.kvdim(), M = (int)rows;
+  const GemmPlan p = plan_gemm_cl(kvd, d.C, M, c->sm_count, 0, false, kCtxSplit);
+  const int box = p.tok_tiles == 1 ? (M < p.tok_tile ? M : p.tok_tile) : p.tok_tile;
+  CUtensorMap amap;
+  *err = make_map(&amap, hidden, (long)d.L * M, d.C, box);
+  if (*err != cudaSuccess) return 0;
+  int n = 0;
+  for (int l = 0; l < d.L; ++l)
+    for (int part = 0; part < 2; ++part) {
+      TcGemmArgs a = {};
+      a.M = M;
+      a.status = c->status_dev;
+      a.w_row0 = (l * 2 + part) * kvd;
+      a.w_next_row0 = -1;
+      a.n_ss = 0;  // a plain projection: no adaRMS factor
+      a.norm_dim = 1;
+      a.eps = 1.f;
+      a.fold = nullptr;
+      a.rope_cs = c->ctx_rope;
+      a.dh = d.dh;
+      a.n_rot_heads = part == 0 ? d.Hkv : 0;
+      a.act_rows = box;
+      a.act_row0 = l * M;
+      a.e_mode = kEQkvRope;
+      a.out_bf16 = (bf16*)(part == 0 ? c->ctx_k : c->ctx_v) + (size_t)l * M * kvd;
+      const cudaError_t e = launch_tc_gemm(c->map_wctx, amap, p, a, s, false);
+      if (e != cudaSuccess) {
+        *err = e;
+        return n;
+      }
+      ++n;
+    }
   return n;
 }
 

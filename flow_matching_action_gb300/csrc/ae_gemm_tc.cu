@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
           tma_prefetch_l2_2d(&wmap, (kb_begin + it) * 64, a.w_next_row0 + n_tile * 128);
       pdl_wait();
       for (int it = 0; it < pre; ++it)
-        tma_load_2d_nohint(smB + (size_t)it * btile, &amap, &full[it], kcol(it), t0);
+        tma_load_2d_nohint(smB + (size_t)it * btile, &amap, &full[it], kcol(it), a.act_row0 + t0);
       int it = pre;
       for (; it < n_it; ++it) {
         const int s = it % S;
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         const int kc = kcol(it);
         mbar_arrive_expect_tx(&full[s], bytes);
         tma_load_2d(smA + (size_t)s * kATileBytes, &wmap, &full[s], kc, row, pol_w);
-        tma_load_2d_nohint(smB + (size_t)s * btile, &amap, &full[s], kc, t0);
+        tma_load_2d_nohint(smB + (size_t)s * btile, &amap, &full[s], kc, a.act_row0 + t0);
       }
       // drain: no copy may still be in flight when the CTA exits
       for (int j = it - S > 0 ? it - S : 0; j < it; ++j)
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       gt = E.gate[n];
       if (E.scale_next != nullptr) sc = E.scale_next[n];
     } else {
-      cf = E.fold[n];
+      cf = E.fold != nullptr ? E.fold[n] : 0.f;
     }
     pdl_wait();
     // reciprocal RMS of the emitted tokens, while the mainloop runs
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         const int tok = t0 + e_lo + i;
         float ss = 0.f;
         for (int j = 0; j < E.n_ss; ++j) ss += E.ss_in[(size_t)j * E.M + tok];
-        rn_s[i] = 1.0f / sqrtf(ss / (float)E.norm_dim + E.eps);
+        rn_s[i] = E.n_ss > 0 ? 1.0f / sqrtf(ss / (float)E.norm_dim + E.eps) : 1.f;  // n_ss 0: no norm
       }
     // the first two groups' per-token inputs, issued before the accumulator is ready
     {
@@ -930,9 +930,11 @@ int max_active_clusters(int ew, int ks, size_t smem) {
 }
 }  // namespace
 
-GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split, bool retile) {
+GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split, bool retile, int exact_split) {
   GemmPlan p;
-  plan_tiles(p, N, K, M);
+  // a fixed split keeps the token tiles at 128 so that the split-K receive
+  // buffer (the fp32 tile) fits beside the pipeline whatever M is
+  plan_tiles(p, N, K, M, exact_split > 0 ? (M + 127) / 128 : 0);
   // An unsplit GEMM that leaves SMs idle spends them on more, shorter token
   // tiles (down to 64 tokens) instead.
   if (retile && sm_count / (p.n_tiles * p.tok_tiles) <= 1) {
@@ -946,7 +948,7 @@ GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split, bool ret
   }
   const int ew = p.tok_tile > 64 ? 8 : 4;
   const int base = p.n_tiles * p.tok_tiles;
-  int ks = sm_count / base;
+  int ks = exact_split > 0 ? exact_split : sm_count / base;
   if (max_split > 0 && ks > max_split) ks = max_split;
   if (ks > kMaxCluster) ks = kMaxCluster;
   if (ks > p.kb_total) ks = p.kb_total;
@@ -977,7 +979,7 @@ GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split, bool ret
     p.stages = stages;
     p.smem = 1024 + gemm_smem_layout(stages, p.tok_tile, ks).total;
     p.grid = base * ks;
-    if (ks == 1) break;
+    if (ks == 1 || exact_split > 0) break;
     if (p.smem <= 232448 && max_active_clusters(ew, ks, p.smem) >= base) break;
   }
   // An unsplit GEMM with between one and two waves of tiles keeps two CTAs

@@ -27,6 +27,7 @@ struct Dims {
   int L, D, F, Hq, Hkv, dh, A, H;
   double eps, theta, tmin, tmax;
   int dtype;
+  int C;  // width of the VLM hidden states projected by ae_bind_context (0: none)
   int qdim() const { return Hq * dh; }
   int kvdim() const { return Hkv * dh; }
   int qkvdim() const { return (Hq + 2 * Hkv) * dh; }
@@ -78,6 +79,15 @@ struct ae_ctx {
   void* w_d = nullptr;    // [L][D, F]
   void* w_mod = nullptr;  // [L][2][3D, D]
   void* b_mod = nullptr;  // [L][2][3D]
+  // Context projection (ctx_dim > 0): per layer [K rows | V rows] of [2 Hkv dh, C];
+  // rows of every head as rotation pairs when ctx_tc (the tensor-core path).
+  void* w_ctx = nullptr;
+  bool ctx_tc = false;        // context projection on the tensor cores
+  void* ctx_k = nullptr;      // [L][rows][Hkv dh] T: projected K of the bound context
+  void* ctx_v = nullptr;      // [L][rows][Hkv dh] T
+  float2* ctx_rope = nullptr; // [max_batch * max_rows][dh/2] (cos, sin) at each valid row's position
+  float* ctx_tmp = nullptr;   // [max_batch * max_rows][2 Hkv dh] fp32 (SIMT projection)
+  CUtensorMap map_wctx;       // w_ctx, boxes 128 rows x 64
 
   // Scratch, sized for max_batch * H rows.
   float* h = nullptr;        // [M, D]    residual stream
@@ -197,12 +207,13 @@ struct TcGemmArgs {
   int tok_half;         // first token column of the second epilogue half (multiple of 16)
   int xbulk;            // split K: partials sent by bulk copies (1) or per-thread remote stores (0)
   int act_rows;         // rows of the operand map's token box (0: tok_tile); a single short tile loads only its valid rows
+  int act_row0;         // row of the operand map where token 0 sits (a layer of a stacked operand)
   int e_mode;           // kEQkvRope, kEGeglu or kEResid
   // kEQkvRope / kEGeglu: the operand is bf16(h * (1 + scale)); adaRMS is folded in
   const float* ss_in;   // [n_ss][M] sums of h^2 per 128 features of the operand's rows
-  int n_ss, norm_dim;   // D / 128, D
+  int n_ss, norm_dim;   // D / 128, D; n_ss == 0: no norm (a plain projection)
   float eps;
-  const float* fold;    // [N] shift W^T of this layer and flow step
+  const float* fold;    // [N] shift W^T of this layer and flow step (nullptr: none)
   bf16* out_bf16;       // kEQkvRope: [M][N]; kEGeglu: [M][N/2]
   const float2* rope_cs;
   int dh, n_rot_heads;
@@ -224,7 +235,10 @@ size_t tc_gemm_smem_bytes(int stages, int tok_tile);
 // no more splits than keep every cluster of the launch resident at once.
 // retile: an unsplit plan that leaves SMs idle may use more, shorter token
 // tiles (the operand's TMA box must then follow the plan's tok_tile).
-GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split = 0, bool retile = false);
+// exact_split > 0: exactly that many K splits whatever M is (the sum order over
+// K, and so the rounding of every output, then does not depend on M).
+GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split = 0, bool retile = false,
+                      int exact_split = 0);
 cudaError_t gemm_kernel_setup();
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
                            TcGemmArgs a, cudaStream_t s, bool pdl);
@@ -276,6 +290,17 @@ cudaError_t make_f32_3d_map(CUtensorMap* map, const void* ptr, long d0, long d1,
 cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int dh);
 // bf16 [units * 128, dh] view of part_o, boxes of 128 rows x 64 columns, 128-byte swizzle
 cudaError_t make_attn_o16_map(CUtensorMap* map, float* part_o, size_t units, int dh);
+
+// ---- context projection (ae_bind_context)
+// ctx_rope[valid row of request b at position i] = (cos, sin)(i theta^(-2j/dh)).
+int launch_ctx_rope(const int* valid_idx, const int* n_valid, int batch, int max_rows, int half_dh, double theta,
+                    float2* ctx_rope, cudaStream_t s);
+// SIMT projection of one layer: [K | V] = hidden W_ctx^T for all rows, then the
+// valid rows rotated (K) and stored as T into k_out / v_out [rows][Hkv dh].
+int launch_ctx_project_simt(const ae_ctx* c, const void* hidden_l, int64_t rows, const void* w_l, void* k_out,
+                            void* v_out, cudaStream_t s);
+// Tensor-core projection of every layer (bf16, Hkv dh % 128 == 0): two GEMMs a layer.
+int launch_ctx_project_tc(ae_ctx* c, const void* hidden, int64_t rows, cudaStream_t s, cudaError_t* err);
 
 // ---- bf16 path driver (ae_fast.cu)
 bool fast_path_supported(const Dims& d, std::string* why);

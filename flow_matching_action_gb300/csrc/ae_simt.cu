@@ -481,7 +481,85 @@ int step_simt(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s)
   return n + 1;
 }
 
+// ---------------------------------------------------------------- context projection
+// (cos, sin) at every valid context row's position among its request's valid
+// rows, for the projected K (MolmoBot PR, Part 2: the context K/V are
+// projected once per query; positions as for a bound prefix, LoongForge
+// section 1: masked rows do not advance them).
+__global__ void k_ctx_rope(const int* __restrict__ valid_idx, const int* __restrict__ n_valid, int max_rows,
+                           int half_dh, double theta, float2* __restrict__ cs) {
+  const int b = blockIdx.y;
+  const int n = n_valid[b];
+  const int dh = 2 * half_dh;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n * half_dh; e += gridDim.x * blockDim.x) {
+    const int i = e / half_dh, j = e - i * half_dh;
+    const int row = valid_idx[(size_t)b * max_rows + i];
+    const double inv_freq = pow(theta, -2.0 * (double)j / (double)dh);
+    double sn, cn;
+    sincos((double)i * inv_freq, &sn, &cn);
+    cs[(size_t)row * half_dh + j] = make_float2((float)cn, (float)sn);
+  }
+}
+
+// SIMT projection, second half: every valid row of request blockIdx.y, its K
+// head pairs (j, j + dh/2) rotated at the row's position, K and V stored as T.
+template <typename T>
+__global__ void k_ctx_split(const float* __restrict__ kv, int hkv, int dh, const int* __restrict__ valid_idx,
+                            const int* __restrict__ n_valid, int max_rows, double theta, T* __restrict__ k_out,
+                            T* __restrict__ v_out) {
+  const int b = blockIdx.y;
+  const int n = n_valid[b];
+  const int half = dh / 2, kvd = hkv * dh;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n * hkv * half; e += gridDim.x * blockDim.x) {
+    const int i = e / (hkv * half), r = e - i * (hkv * half);
+    const int h = r / half, j = r - h * half;
+    const size_t row = (size_t)valid_idx[(size_t)b * max_rows + i];
+    const float* src = kv + row * 2 * kvd + h * dh;
+    const double inv_freq = pow(theta, -2.0 * (double)j / (double)dh);
+    double sn, cn;
+    sincos((double)i * inv_freq, &sn, &cn);
+    const float c = (float)cn, sv = (float)sn;
+    const float x1 = src[j], x2 = src[j + half];
+    T* ko = k_out + row * kvd + h * dh;
+    T* vo = v_out + row * kvd + h * dh;
+    ko[j] = from_f<T>(x1 * c - x2 * sv);
+    ko[j + half] = from_f<T>(x2 * c + x1 * sv);
+    vo[j] = from_f<T>(src[kvd + j]);
+    vo[j + half] = from_f<T>(src[kvd + j + half]);
+  }
+}
+
+template <typename T>
+int ctx_project_simt(const ae_ctx* c, const void* hidden_l, int64_t rows, const void* w_l, void* k_out, void* v_out,
+                     cudaStream_t s) {
+  const Dims& d = c->d;
+  const int kvd = d.kvdim();
+  gemm((int)rows, 2 * kvd, d.C, (const T*)hidden_l, (long)d.C, (const T*)w_l, (long)d.C,
+       EpiStore{c->ctx_tmp, 2 * kvd}, s);
+  const int B = c->bind.batch;
+  const int per_b = c->max_rows * d.Hkv * (d.dh / 2);
+  dim3 grid((unsigned)((per_b + 255) / 256 < 1 ? 1 : (per_b + 255) / 256), (unsigned)B);
+  k_ctx_split<T><<<grid, 256, 0, s>>>(c->ctx_tmp, d.Hkv, d.dh, c->valid_idx, c->n_valid, c->max_rows, d.theta,
+                                       (T*)k_out, (T*)v_out);
+  return 2;
+}
+
 }  // namespace
+
+int launch_ctx_rope(const int* valid_idx, const int* n_valid, int batch, int max_rows, int half_dh, double theta,
+                    float2* ctx_rope, cudaStream_t s) {
+  if (batch <= 0) return 0;
+  const int per_b = max_rows * half_dh;
+  dim3 grid((unsigned)((per_b + 255) / 256 < 1 ? 1 : (per_b + 255) / 256), (unsigned)batch);
+  k_ctx_rope<<<grid, 256, 0, s>>>(valid_idx, n_valid, max_rows, half_dh, theta, ctx_rope);
+  return 1;
+}
+
+int launch_ctx_project_simt(const ae_ctx* c, const void* hidden_l, int64_t rows, const void* w_l, void* k_out,
+                            void* v_out, cudaStream_t s) {
+  return c->d.dtype == AE_DTYPE_BF16 ? ctx_project_simt<bf16>(c, hidden_l, rows, w_l, k_out, v_out, s)
+                                     : ctx_project_simt<float>(c, hidden_l, rows, w_l, k_out, v_out, s);
+}
 
 int launch_bind(const BindArgs& a, cudaStream_t s) {
   if (a.batch <= 0) return 0;

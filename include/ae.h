@@ -94,6 +94,9 @@ typedef struct {
   double time_min_period; /* double: the smallest period's angle reaches ~1.6e3 rad */
   double time_max_period;
   int dtype;       /* ae_dtype: storage type T of weights and prefix K/V */
+  int ctx_dim;     /* C, width of the per-layer VLM hidden states that
+                      ae_bind_context projects into K/V; 0 = no context
+                      projection (w_ck / w_cv are then ignored) */
 } ae_config;
 
 /*
@@ -110,6 +113,8 @@ typedef struct {
  *                                       the attention / MLP sublayer
  *   w_mod_f [2D, D], b_mod_f [2D]       final adaRMS (scale, shift)
  *   w_out [A, D], b_out [A]             action output projection
+ *   w_ck, w_cv [Hkv*dh, C]              context K / V projections (ae_bind_context);
+ *                                       required when ctx_dim > 0, else may be NULL
  */
 typedef struct {
   const void *w_in, *b_in;
@@ -119,6 +124,7 @@ typedef struct {
   const void *const *wq, *const *wk, *const *wv, *const *wo;
   const void *const *wg, *const *wu, *const *wd;
   const void *const *w_mod1, *const *b_mod1, *const *w_mod2, *const *b_mod2;
+  const void *const *w_ck, *const *w_cv;
 } ae_weights;
 
 /*
@@ -182,6 +188,27 @@ AE_API ae_status ae_bind_prefix(ae_ctx* ctx, int batch, const void* prefix_k,
 AE_API ae_status ae_bind_prefix_shared(ae_ctx* ctx, int n_samples, const void* prefix_k,
                                 const void* prefix_v, int32_t n_rows,
                                 const uint8_t* prefix_mask);
+
+/*
+ * Bind `batch` requests whose prefix arrives as per-layer VLM hidden states
+ * (the cross-attention form of MolmoBot PR Part 2: "compute the cross-attention
+ * K/V once per query and reuse them across every step").  The library
+ * projects every valid row once, here, into its own K/V buffers:
+ *   K = RoPE(hidden W_ck^T) at the row's position among its request's valid
+ *   rows (0 .. n_b - 1),  V = hidden W_cv^T,
+ * and binds them exactly as ae_bind_prefix binds a pre-projected prefix;
+ * every later ae_sample reuses them.  hidden is only read during this call's
+ * work on the stream: it may be freed or changed once that work is done.
+ *   hidden       device T, packed varlen [layers][total_rows][ctx_dim],
+ *                total_rows = cu_lens[batch]
+ *   cu_lens      HOST int32 [batch + 1], as in ae_bind_prefix
+ *   prefix_mask  device uint8 [total_rows] (1 = valid) or NULL; masked rows
+ *                are never read (they may hold NaN) and do not advance positions
+ * Errors: AE_ERR_UNSUPPORTED (context created with ctx_dim == 0), and those
+ * of ae_bind_prefix.
+ */
+AE_API ae_status ae_bind_context(ae_ctx* ctx, int batch, const void* hidden, const int32_t* cu_lens,
+                          const uint8_t* prefix_mask);
 
 /*
  * Run n_steps Euler steps of delta = -1/n_steps from t = 1 for every bound
