@@ -110,6 +110,8 @@ def make_workload(name: str, seed: int = 0):
         return synth.tiny(seed)
     if name == "pi05_shared16":
         return shared_samples(synth.pi05_two_camera(seed, N_FLOW_STEPS), 16, seed)
+    if name == "pi05_context":
+        return synth.pi05_context(seed, N_FLOW_STEPS)
     raise ValueError(name)
 
 
@@ -133,6 +135,12 @@ def shared_samples(wl, n_samples, seed):
 
 
 def describe(wl) -> str:
+    if wl.context is not None:
+        return (f"{wl.name}: Pi0.5-shaped action expert L={wl.dims.layers} D={wl.dims.width} "
+                f"F={wl.dims.mlp} Hq={wl.dims.n_q_heads} Hkv={wl.dims.n_kv_heads} dh={wl.dims.head_dim}, "
+                f"batch {wl.batch}, prefix as {wl.dims.ctx_dim}-wide per-layer hidden states of "
+                f"{min(wl.n_valid)}..{max(wl.n_valid)} valid rows projected into K/V at every bind, "
+                f"horizon {wl.dims.horizon} x {wl.dims.action_dim}, {wl.n_steps} Euler steps")
     shared = getattr(wl, "shared_rows", None)
     prefix = (f"{wl.batch} samples over one shared prefix of {shared} rows ({min(wl.n_valid)} valid)"
               if shared is not None else
@@ -163,8 +171,13 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_
     del dev_w
     shared = getattr(wl, "shared_rows", None)
     rows = shared if shared is not None else None
-    k = _dev(wl.prefix_k[:, :rows], dtype)
-    v = _dev(wl.prefix_v[:, :rows], dtype)
+    context = wl.context is not None
+    if context:  # per-layer VLM hidden states, projected into K/V by every bind
+        k = _dev(wl.context, dtype)
+        v = None
+    else:
+        k = _dev(wl.prefix_k[:, :rows], dtype)
+        v = _dev(wl.prefix_v[:, :rows], dtype)
     mask = torch.from_numpy(wl.mask[:rows]).cuda()
     cu = [int(c) for c in wl.cu_lens]
     rng = np.random.default_rng(123)
@@ -174,7 +187,9 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_
     out = torch.empty_like(noises[0])
 
     def bind():
-        if shared is not None:
+        if context:
+            ex.bind_context(k, cu, mask)
+        elif shared is not None:
             ex.bind_prefix_shared(wl.batch, k, v, shared, mask)
         else:
             ex.bind_prefix(k, v, cu, mask)
@@ -419,28 +434,44 @@ def measured_traffic(workload: str):
     return rec.get("bytes_per_flow_step", {}).get(workload)
 
 
-def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind):
-    """A workload reported beside the headline one, against the bf16 tensor roofline."""
+def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm):
+    """A workload reported beside the headline one: against the HBM roofline at
+    batch 1 (weight streaming), else against the bf16 tensor roofline."""
     wl2 = make_workload(name)
     b2, f2 = algorithmic(wl2.dims, wl2.n_valid)
     reps2 = max(args.reps, args.steps)
+    if wl2.dims.ctx_dim > 0:
+        from flow_matching_action_gb300 import synth
+        w = {**w, **synth.make_context_weights(wl2.dims, 0)}
     r2 = run_gpu_arm(wl2, w, reps2, args.warmup, dist_ctx, measure_e2e=False, stat_reps=reps2)
     s2 = statistics.median(r2["sample_ms"])
     t2 = dist_ctx.max(r2["total_ms"]) / reps2
     tflops = f2 * wl2.n_steps / (s2 / 1e3) / 1e12
-    return {"workload": describe(wl2), "chunks_per_s": wl2.batch / (t2 / 1e3) * dist_ctx.world,
+    extra = {}
+    if wl2.dims.ctx_dim > 0:
+        # the bind projects every valid row of every layer: 2 GEMMs [n, C] x [C, Hkv dh] a layer
+        d2 = wl2.dims
+        pf = 2.0 * 2 * d2.layers * sum(wl2.n_valid) * d2.ctx_dim * d2.kv_dim
+        bm = statistics.median(r2["bind_ms"])
+        extra["context_projection"] = {"bind_ms_median": bm, "flops_per_bind": pf,
+                                       "achieved_tflops": pf / (bm / 1e3) / 1e12,
+                                       "frac_of_burst_bf16": pf / (bm / 1e3) / 1e12 / tf_burst}
+    return {**extra, "workload": describe(wl2), "chunks_per_s": wl2.batch / (t2 / 1e3) * dist_ctx.world,
             "ms_per_step": t2, "us_per_flow_step": s2 * 1e3 / wl2.n_steps,
             "sample_ms_median": s2, "sample_ms_p90": float(np.percentile(r2["sample_ms"], 90)),
             "sample_calls_timed": len(r2["sample_ms"]),
             "clocks": r2["clocks"],
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
+            "roofline": ({"bound": "hbm", "achieved": b2 * wl2.n_steps / (s2 / 1e3) / 1e9, "peak": hbm,
+                          "unit": "GB/s", "frac": b2 * wl2.n_steps / (s2 / 1e3) / 1e9 / hbm,
+                          "algorithmic_bytes_per_flow_step": b2} if wl2.batch == 1 else
+                         {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
                          "unit": "TFLOP/s", "frac": tflops / tf_sust,
                          "peak_burst": tf_burst, "frac_of_burst": tflops / tf_burst,
                          "peak_kind": f"{peak_kind} sustained cuBLAS bf16 (frac); "
                                       f"{peak_kind} burst cuBLAS bf16 (frac_of_burst)",
                          "algorithmic_flops_per_flow_step": f2,
                          "traffic": measured_traffic(name),
-                         "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"}}
+                         "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"})}
 
 
 def main():
@@ -453,6 +484,8 @@ def main():
     ap.add_argument("--batched", default="pi05_b16", help="second workload reported beside ('' = none)")
     ap.add_argument("--shared", default="pi05_shared16",
                     help="many samples over one shared prefix, reported beside ('' = none)")
+    ap.add_argument("--context", default="pi05_context",
+                    help="prefix as per-layer VLM hidden states projected at bind, reported beside ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--reps", type=int, default=50, help="minimum ae_sample calls in the per-call statistics")
@@ -542,9 +575,9 @@ def main():
         e = res["e2e"]
         line["e2e"] = {"value": chunks / (e["ms"] / 1e3), "unit": "chunks/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
-    for key, name in (("batched", args.batched), ("shared_prefix", args.shared)):
+    for key, name in (("batched", args.batched), ("shared_prefix", args.shared), ("context", args.context)):
         if name:
-            line[key] = side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind)
+            line[key] = side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm)
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, w)
     if dist_ctx.rank == 0:

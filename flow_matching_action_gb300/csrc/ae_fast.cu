@@ -306,31 +306,34 @@ int launch_ctx_project_tc(ae_ctx* c, const void* hidden, int64_t rows, cudaStrea
   *err = make_map(&amap, hidden, (long)d.L * M, d.C, box);
   if (*err != cudaSuccess) return 0;
   int n = 0;
-  for (int l = 0; l < d.L; ++l)
-    for (int part = 0; part < 2; ++part) {
-      TcGemmArgs a = {};
-      a.M = M;
-      a.status = c->status_dev;
-      a.w_row0 = (l * 2 + part) * kvd;
-      a.w_next_row0 = -1;
-      a.n_ss = 0;  // a plain projection: no adaRMS factor
-      a.norm_dim = 1;
-      a.eps = 1.f;
-      a.fold = nullptr;
-      a.rope_cs = c->ctx_rope;
-      a.dh = d.dh;
-      a.n_rot_heads = part == 0 ? d.Hkv : 0;
-      a.act_rows = box;
-      a.act_row0 = l * M;
-      a.e_mode = kEQkvRope;
-      a.out_bf16 = (bf16*)(part == 0 ? c->ctx_k : c->ctx_v) + (size_t)l * M * kvd;
-      const cudaError_t e = launch_tc_gemm(c->map_wctx, amap, p, a, s, false);
-      if (e != cudaSuccess) {
-        *err = e;
-        return n;
-      }
-      ++n;
+  for (int part = 0; part < 2; ++part) {  // every layer's K in one launch, then every V
+    TcGemmArgs a = {};
+    a.M = M;
+    a.status = c->status_dev;
+    a.w_row0 = part * kvd;
+    a.w_next_row0 = -1;
+    a.n_ss = 0;  // a plain projection: no adaRMS factor
+    a.norm_dim = 1;
+    a.eps = 1.f;
+    a.fold = nullptr;
+    a.rope_cs = c->ctx_rope;
+    a.dh = d.dh;
+    a.n_rot_heads = part == 0 ? d.Hkv : 0;
+    a.act_rows = box;
+    a.act_row0 = 0;
+    a.e_mode = kEQkvRope;
+    a.out_bf16 = (bf16*)(part == 0 ? c->ctx_k : c->ctx_v);
+    a.z_count = d.L;
+    a.z_w_rows = 2 * kvd;
+    a.z_act_rows = M;
+    a.z_out = (long)M * kvd;
+    const cudaError_t e = launch_tc_gemm(c->map_wctx, amap, p, a, s, false);
+    if (e != cudaSuccess) {
+      *err = e;
+      return n;
     }
+    ++n;
+  }
   return n;
 }
 

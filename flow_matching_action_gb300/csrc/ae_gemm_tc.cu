@@ -414,7 +414,10 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   E.eps = a.eps;
   E.ss_in = a.ss_in;
   E.fold = a.fold;
-  E.out = a.out_bf16;
+  // gridDim.y > 1: independent GEMMs of the same shape, z-th one offset in the
+  // stacked weight, the stacked operand and the output (layers of a stack)
+  const int z = blockIdx.y;
+  E.out = a.out_bf16 + (size_t)z * a.z_out;
   E.rope_cs = a.rope_cs;
   E.h = a.h;
   E.gate = a.gate;
@@ -445,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       // evict it first; with several token tiles the other tiles' CTAs read it
       // moments later, so it keeps the normal policy
       const uint64_t pol_w = a.tok_tiles > 1 ? policy_evict_normal() : policy_evict_first();
-      const int row = a.w_row0 + n_tile * 128;
+      const int row = a.w_row0 + z * a.z_w_rows + n_tile * 128;
       // the token box may hold only the valid rows of a single short tile
       const uint32_t bytes = kATileBytes + (uint32_t)(a.act_rows > 0 ? a.act_rows : TT) * 128u;
       // Weights do not depend on the previous kernel: fill the first stages and
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
           tma_prefetch_l2_2d(&wmap, (kb_begin + it) * 64, a.w_next_row0 + n_tile * 128);
       pdl_wait();
       for (int it = 0; it < pre; ++it)
-        tma_load_2d_nohint(smB + (size_t)it * btile, &amap, &full[it], kcol(it), a.act_row0 + t0);
+        tma_load_2d_nohint(smB + (size_t)it * btile, &amap, &full[it], kcol(it), a.act_row0 + z * a.z_act_rows + t0);
       int it = pre;
       for (; it < n_it; ++it) {
         const int s = it % S;
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         const int kc = kcol(it);
         mbar_arrive_expect_tx(&full[s], bytes);
         tma_load_2d(smA + (size_t)s * kATileBytes, &wmap, &full[s], kc, row, pol_w);
-        tma_load_2d_nohint(smB + (size_t)s * btile, &amap, &full[s], kc, a.act_row0 + t0);
+        tma_load_2d_nohint(smB + (size_t)s * btile, &amap, &full[s], kc, a.act_row0 + z * a.z_act_rows + t0);
       }
       // drain: no copy may still be in flight when the CTA exits
       for (int j = it - S > 0 ? it - S : 0; j < it; ++j)
@@ -1047,7 +1050,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, con
   a.xbulk = p.xbulk;
   const int ew = p.tok_tile > 64 ? 8 : 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.gridDim = dim3((unsigned)p.grid, (unsigned)(a.z_count > 1 ? a.z_count : 1));
   cfg.blockDim = dim3((unsigned)kThreadsFor(ew));
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;

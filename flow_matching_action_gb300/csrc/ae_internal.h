@@ -208,6 +208,11 @@ struct TcGemmArgs {
   int xbulk;            // split K: partials sent by bulk copies (1) or per-thread remote stores (0)
   int act_rows;         // rows of the operand map's token box (0: tok_tile); a single short tile loads only its valid rows
   int act_row0;         // row of the operand map where token 0 sits (a layer of a stacked operand)
+  // z_count > 1 runs that many GEMMs of this shape in one launch (gridDim.y):
+  // the z-th reads weight rows + z * z_w_rows, operand rows + z * z_act_rows
+  // and writes out_bf16 + z * z_out (kEQkvRope only)
+  int z_count, z_w_rows, z_act_rows;
+  long z_out;
   int e_mode;           // kEQkvRope, kEGeglu or kEResid
   // kEQkvRope / kEGeglu: the operand is bf16(h * (1 + scale)); adaRMS is folded in
   const float* ss_in;   // [n_ss][M] sums of h^2 per 128 features of the operand's rows
