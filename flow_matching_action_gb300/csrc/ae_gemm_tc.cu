@@ -619,11 +619,12 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       cluster_wait();  // every rank of the cluster has started and initialised its barrier
       if constexpr (XP == 1) {
         named_bar<1>(kEpiThreads);
-        if (go && threadIdx.x == 64) {
+        // one lane per destination rank issues that rank's copy
+        if (go && warp == 2) {
           const uint32_t stg_u = smem_u32(smem);
           const uint32_t dst0 = smem_u32(smem + L.recv) + (uint32_t)(ks * slice) * 512u;
           const uint32_t bar_u = smem_u32(recv_bar);
-          for (int r = 0; r < ksn; ++r) {
+          for (int r = lane; r < ksn; r += 32) {
             const int lo = run_lo(r, ng, ksn), hi = min(run_lo(r + 1, ng, ksn), nv);
             if (hi <= lo) continue;
             bulk_to_peer(mapa(dst0, (uint32_t)r), stg_u + (uint32_t)lo * 512u, (uint32_t)(hi - lo) * 512u,
@@ -748,7 +749,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
             (red_s[i] + red_s[TT + i]) + (red_s[2 * TT + i] + red_s[3 * TT + i]);
   }
   // the bulk copies out of the staging must have read it before the CTA exits
-  if (XP == 1 && threadIdx.x == 64) bulk_wait_read_all();
+  if (XP == 1 && warp == 2) bulk_wait_read_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
