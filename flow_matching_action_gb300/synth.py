@@ -18,6 +18,8 @@ No dataset is read; every tensor is N(0, sigma) from a counter-seeded
 * stream ``[seed, 3, b]``    initial noise of request ``b``
 * stream ``[seed, 4]``       context K/V projection weights (cross-attention form)
 * stream ``[seed, 5, b]``    valid context hidden-state rows of request ``b``
+* stream ``[seed, 6]``       synthetic VLM weights (prefill)
+* stream ``[seed, 7, b]``    prefix token embeddings of request ``b`` (prefill)
 
 Because request ``b`` owns its own streams, request ``b`` of a batch is the
 same as a batch-1 workload built from the same ``(seed, b)``.
@@ -341,3 +343,44 @@ def pi05_context(seed: int = 0, n_steps: int = 10, padded: bool = False) -> Work
     """The two-camera 712-row prefix as 2048-wide hidden states (optionally padded to 968 rows)."""
     lay = [("v", 512), ("m", 256), ("v", 200)] if padded else [("v", 712)]
     return build_context_workload("pi05_ctx_712" + ("_masked" if padded else ""), PI05_CTX, n_steps, [lay], seed)
+
+
+# Synthetic VLM for the prefill that produces the prefix KV: a Gemma-style
+# decoder with the expert's layer; ``horizon`` is the number of prefix tokens a
+# request carries.  TINY_VLM is the oracle-sized case; PI05_VLM_2L has the
+# widths of Pi0.5's 2B VLM (D 2048, F 16384, 8 query heads, one KV head) over
+# the two-camera 712-token prefix, with 2 layers so that the oracle stays fast.
+TINY_VLM = ExpertDims(layers=2, width=256, mlp=1024, n_q_heads=4, n_kv_heads=1,
+                      head_dim=64, horizon=48, action_dim=8, dtype="f32")
+PI05_VLM_2L = ExpertDims(layers=2, width=2048, mlp=16384, n_q_heads=8, n_kv_heads=1,
+                         head_dim=256, horizon=712, action_dim=32, dtype="bf16")
+
+
+def make_vlm_weights(d: ExpertDims, seed: int = 0, norm_std: float = 0.1) -> Dict[str, object]:
+    """Weights of a synthetic VLM in the expert's weight layout: its layers'
+    projections N(0, 0.02); its RMSNorm weights w N(0, norm_std) stored as the
+    biases (w, 0, 1) of modulation Linears whose weights are zero; the time
+    MLP and action projections (unused by a prefill) N(0, 0.02)."""
+    rng = np.random.default_rng([seed, 6])
+    D = d.width
+    w: Dict[str, object] = {}
+    for name, shape in global_weight_shapes(d):
+        w[name] = _store(d, _normal(rng, shape, WEIGHT_STD))
+    for name in LAYER_WEIGHTS:
+        w[name] = []
+    for _ in range(d.layers):
+        for name, shape in layer_weight_shapes(d):
+            if name in ("w_mod1", "w_mod2"):
+                w[name].append(np.zeros(shape, dtype=np.float32))
+            elif name in ("b_mod1", "b_mod2"):
+                norm = _store(d, _normal(rng, (D,), norm_std))
+                w[name].append(np.concatenate([norm, np.zeros(D, np.float32), np.ones(D, np.float32)]))
+            else:
+                w[name].append(_store(d, _normal(rng, shape, WEIGHT_STD)))
+    return w
+
+
+def prefix_embeddings(d: ExpertDims, seed: int, batch: int) -> np.ndarray:
+    """[batch * n, D] token embeddings, N(0, 1), request b from stream [seed, 7, b]."""
+    return np.concatenate([_store(d, _normal(np.random.default_rng([seed, 7, b]), (d.horizon, d.width)))
+                           for b in range(batch)]) if batch else np.zeros((0, d.width), np.float32)

@@ -31,6 +31,9 @@ Sources (page title, section):
   VLM hands over per-layer hidden states of its context, and the action expert
   projects them into K/V; the fix computes that projection once per query and
   reuses it for every flow step (``project_request``, ``sample(context=...)``).
+* [OxyGen] "Unified KV Cache Management for VLA Inference under Multi-Task
+  Parallelism": the VLM prefill of a frame's observation and instruction
+  produces the KV cache KV[t] that the action expert reads (``prefill_request``).
 
 Parity status of each function is listed in ``PINS``: every function has a
 test that pins it to something other than itself, except the end-to-end action
@@ -54,6 +57,8 @@ PINS = {
     "expert_layer": "tests/test_oracle_pins.py: identity modulation equals a standard pre-norm block",
     "project_request": "tests/test_oracle_pins.py: torch F.linear + complex-rotation RoPE, identity "
                        "weights reduce to rope(), masked rows skipped, projected once == recomputed",
+    "prefill_request": "tests/test_oracle_pins.py: one layer against torch rms_norm/linear and the "
+                       "complex-rotation RoPE; layer-0 K/V per token, deeper K/V see every token",
     "sample": "tests/test_oracle_pins.py: zero velocity, constant velocity closed form, pad/mask "
               "invariance (bitwise), hoisted == recomputed (bitwise), batch independence; "
               "end-to-end values: parity unpinned (no page prints an expected action)",
@@ -255,6 +260,39 @@ def project_request(dims, hidden, w_ck, w_cv, mask, row0: int, row1: int):
         ks[l] = rope(k, pos, dims.rope_theta).transpose(1, 0, 2).reshape(n, hkv * dh)
         vs[l] = x @ _f64(w_cv[l]).T
     return ks, vs, n
+
+
+def prefill_request(dims, w: Dict, emb: np.ndarray):
+    """Per-layer K and V of a VLM prefill over one request's prefix tokens.
+
+    [OxyGen] (the VLM prefill of the observation produces KV[t]) and
+    [MolmoBot] Part 2 (the VLM backbone runs once per query) put this step
+    before the path.  Readings: the VLM is a Gemma-style decoder with the same
+    layer as the action expert ([LoongForge] section 2) under constant
+    conditioning: its RMSNorm is x * rsqrt(mean(x^2) + eps) * (1 + w_norm)
+    and its residuals are plain, i.e. adaRMS with (scale, shift, gate) =
+    (w_norm, 0, 1), stored as the biases of modulation Linears whose weights
+    are zero; the prefix tokens attend to each other bidirectionally (the
+    prefix half of [LoongForge] section 3's prefix-LM mask) at positions
+    0..n-1, and K is stored after RoPE (the prefix convention of this path).
+    emb: [n, D] token embeddings.  Returns (K [L, n, Hkv*dh], V [L, n, Hkv*dh]).
+    """
+    n, D = emb.shape
+    L, hkv, dh = dims.layers, dims.n_kv_heads, dims.head_dim
+    zero_c = np.zeros(D)
+    pos = np.arange(n, dtype=np.float64)
+    empty = np.zeros((0, hkv * dh))
+    ks = np.empty((L, n, hkv * dh))
+    vs = np.empty((L, n, hkv * dh))
+    h = _f64(emb)
+    for l in range(L):
+        m1 = modulation(zero_c, w["w_mod1"][l], w["b_mod1"][l], 3)
+        m2 = modulation(zero_c, w["w_mod2"][l], w["b_mod2"][l], 3)
+        trace: Dict = {}
+        h = expert_layer(h, m1, m2, w, l, empty, empty, pos, dims, trace=trace)
+        ks[l] = trace["k"].transpose(1, 0, 2).reshape(n, hkv * dh)
+        vs[l] = trace["v"].transpose(1, 0, 2).reshape(n, hkv * dh)
+    return ks, vs
 
 
 def step_times(n_steps: int) -> List[float]:

@@ -419,3 +419,35 @@ def test_context_equals_its_projection_bound_as_prefix_bitwise():
     pk[:, idx], pv[:, idx] = ks, vs
     ref = O.sample(d, w, pk, pv, wl.cu_lens, wl.mask, wl.noise, wl.n_steps)
     np.testing.assert_array_equal(_ctx_run(wl, w, wc), ref)
+
+
+# --------------------------------------------------------------------------- VLM prefill
+def test_prefill_one_layer_matches_torch_norm_linear_and_rotation():
+    import dataclasses
+    d = dataclasses.replace(synth.TINY_VLM, layers=1)
+    w = synth.make_vlm_weights(d, 1)
+    emb = synth.prefix_embeddings(d, 1, 1)
+    ks, vs = O.prefill_request(d, w, emb)
+    norm1 = w["b_mod1"][0][: d.width]
+    y = F.rms_norm(T(emb), (d.width,), eps=d.rms_eps) * (1.0 + T(norm1))
+    k = F.linear(y, T(w["wk"][0])).numpy()
+    v = F.linear(y, T(w["wv"][0])).numpy()
+    half = d.head_dim // 2
+    z = k[:, :half] + 1j * k[:, half:]
+    freq = 1.0 / d.rope_theta ** (np.arange(0, d.head_dim, 2) / d.head_dim)
+    zr = z * np.exp(1j * np.arange(d.horizon)[:, None] * freq[None, :])
+    np.testing.assert_allclose(ks[0], np.concatenate([zr.real, zr.imag], -1), rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(vs[0], v, rtol=1e-10, atol=1e-10)
+
+
+def test_prefill_layer0_is_per_token_and_deeper_layers_see_every_token():
+    d = synth.TINY_VLM
+    w = synth.make_vlm_weights(d, 2)
+    emb = synth.prefix_embeddings(d, 2, 1)
+    ks, vs = O.prefill_request(d, w, emb)
+    emb2 = emb.copy()
+    emb2[-1] += 1.0                                   # change the last token only
+    ks2, vs2 = O.prefill_request(d, w, emb2)
+    np.testing.assert_array_equal(ks2[0][:-1], ks[0][:-1])   # layer 0: K/V of a token is its own
+    np.testing.assert_array_equal(vs2[0][:-1], vs[0][:-1])
+    assert np.abs(ks2[1][0] - ks[1][0]).max() > 1e-6          # layer 1: token 0 saw the last token
