@@ -65,6 +65,7 @@ _SIGNATURES = {
                                              ctypes.c_int32, ctypes.c_void_p]),
     "ae_bind_context": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                        ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    "ae_prefill": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "ae_sample": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "ae_sample_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "ae_set_debug_dump": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
@@ -174,6 +175,10 @@ def ae_bind_prefix_shared(ctx, n_samples: int, prefix_k, prefix_v, n_rows: int, 
 def ae_bind_context(ctx, batch: int, hidden, cu_lens: Sequence[int], prefix_mask=None) -> None:
     cu = (ctypes.c_int32 * (len(cu_lens)))(*[int(v) for v in cu_lens]) if cu_lens is not None else None
     _check(lib().ae_bind_context(ctx, batch, _ptr(hidden), cu, _ptr(prefix_mask)), ctx)
+
+
+def ae_prefill(ctx, batch: int, embeddings, out_k, out_v) -> None:
+    _check(lib().ae_prefill(ctx, batch, _ptr(embeddings), _ptr(out_k), _ptr(out_v)), ctx)
 
 
 def ae_sample(ctx, noise, n_steps: int, out_actions) -> None:

@@ -578,6 +578,28 @@ ae_status ae_bind_context(ae_ctx* c, int batch, const void* hidden, const int32_
   return AE_OK;
 }
 
+ae_status ae_prefill(ae_ctx* c, int batch, const void* embeddings, void* out_k, void* out_v) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  if (!c->fast) return set_msg(c, AE_ERR_UNSUPPORTED, "ae_prefill runs on bf16 contexts only");
+  if (batch < 1 || batch > c->max_batch)
+    return set_msg(c, AE_ERR_SHAPE, "batch %d outside 1..%d", batch, c->max_batch);
+  if (embeddings == nullptr || out_k == nullptr || out_v == nullptr)
+    return set_msg(c, AE_ERR_INVALID_ARG, "embeddings / out_k / out_v is NULL");
+  if (sticky(c) != AE_OK)
+    return set_msg(c, AE_ERR_DEVICE, "a device-side check failed earlier (code %d)", *c->status_host);
+  // the prefix tokens are the layer's tokens: an empty bound prefix, positions 0..H-1
+  int zero[AE_MAX_BATCH] = {0};
+  AE_TRY(bind_ranges(c, batch, nullptr, nullptr, zero, zero, 0, nullptr));
+  const TimeTable* t = nullptr;
+  AE_TRY(get_table(c, 1, &t));  // constant conditioning: the modulation biases
+  ae::PrefillOut po{(const ae::bf16*)embeddings, (ae::bf16*)out_k, (ae::bf16*)out_v};
+  cudaError_t e = cudaSuccess;
+  c->launches_sample = ae::launch_step_fast(c, *t, 0, nullptr, c->stream, &e, nullptr, &po);
+  if (e != cudaSuccess) return cuda_fail(c, e, "prefill launch");
+  AE_CK(c, cudaGetLastError());
+  return AE_OK;
+}
+
 ae_status ae_sample(ae_ctx* c, const float* noise, int n_steps, float* out) {
   if (c == nullptr) return AE_ERR_INVALID_ARG;
   if (c->bind.batch < 0) return set_msg(c, AE_ERR_NOT_BOUND, "ae_sample before ae_bind_prefix");

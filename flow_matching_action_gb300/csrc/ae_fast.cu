@@ -138,7 +138,7 @@ cudaError_t fast_activation_maps(ae_ctx* c, int box_rows, int box_rows_q) {
 }
 
 int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
-                     cudaError_t* err, const AttnScratch* attn_scratch) {
+                     cudaError_t* err, const AttnScratch* attn_scratch, const PrefillOut* prefill) {
   const bool pdl = c->pdl;
   const Dims& d = c->d;
   const int B = c->bind.batch, M = B * d.H, D = d.D, F = d.F, L = d.L;
@@ -196,11 +196,14 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   // on the stream (the bind kernel among them); every later kernel is chained
   // to its predecessor, so all of them start after the bind has completed and
   // may read its tables before griddepcontrol.wait.
-  ck(launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0), y,
-                        c->sumsq, s, pdl && step > 0));
+  if (prefill != nullptr)
+    ck(launch_embed_norm(prefill->emb, M, D, c->h, mod(0, 0), y, c->sumsq, s, false));
+  else
+    ck(launch_inproj_norm(x, (const bf16*)c->w_in, (const bf16*)c->b_in, M, D, d.A, c->h, mod(0, 0), y,
+                          c->sumsq, s, pdl && step > 0));
   ++n;
   for (int l = 0; l < L; ++l) {
-    dump(l);
+    if (prefill == nullptr) dump(l);
     const float* mod1 = mod(l, 0);
     const float* mod2 = mod(l, 1);
     const int ln = (l + 1) % L;  // whose weights each GEMM pulls into L2 ahead of use
@@ -213,6 +216,17 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.out_bf16 = qkv;
     ck(launch_tc_gemm(c->map_qkv, c->map_yq, pq, a, s, pdl));
     ++n;
+    if (prefill != nullptr) {
+      // this layer's K (rotated) and V: columns [Hq dh, (Hq + Hkv) dh) and the
+      // next Hkv dh of the q|k|v rows, into the prefix layout [L][M][Hkv dh]
+      const size_t kvd = d.kvdim(), row = (size_t)nqkv * sizeof(bf16);
+      ck(cudaMemcpy2DAsync(prefill->k + (size_t)l * M * kvd, kvd * sizeof(bf16), qkv + (size_t)d.Hq * d.dh, row,
+                           kvd * sizeof(bf16), M, cudaMemcpyDeviceToDevice, s));
+      ck(cudaMemcpy2DAsync(prefill->v + (size_t)l * M * kvd, kvd * sizeof(bf16),
+                           qkv + (size_t)(d.Hq + d.Hkv) * d.dh, row, kvd * sizeof(bf16), M,
+                           cudaMemcpyDeviceToDevice, s));
+      if (l + 1 == L) break;  // nothing after the last layer's K/V is an output
+    }
 
     // attention over [valid prefix || actions]
     {
@@ -279,6 +293,10 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.ss_out = c->sumsq;
     ck(launch_tc_gemm(c->map_d, c->map_mact, pd, a, s, pdl));
     ++n;
+  }
+  if (prefill != nullptr) {
+    ck(cudaGetLastError());
+    return n;
   }
   dump(L);
   ck(launch_final_bf16(c, t, step, x, s, pdl));

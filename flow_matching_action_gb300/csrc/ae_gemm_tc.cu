@@ -850,6 +850,35 @@ __global__ void __launch_bounds__(kRowThreads) k_inproj_norm(const float* __rest
   }
 }
 
+// Prefill input: h = emb of one token row, then the first QKV GEMM's operand
+// bf16(h * (1 + scale)) and the row's sums of h^2 per 128 features.
+__global__ void __launch_bounds__(kRowThreads) k_embed_norm(const bf16* __restrict__ emb, int M, int D,
+                                                           float* __restrict__ h, const float* __restrict__ scale,
+                                                           bf16* __restrict__ aout, float* __restrict__ ss_out) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ float hs[];  // the row of h [D]
+  const int t = blockIdx.x;
+  for (int n = threadIdx.x; n < D; n += kRowThreads) {
+    const float hn = __bfloat162float(emb[(size_t)t * D + n]);
+    h[(size_t)t * D + n] = hn;
+    hs[n] = hn;
+    aout[(size_t)t * D + n] = __float2bfloat16_rn(hn * (1.f + scale[n]));
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int tile = warp; tile < D / 128; tile += kRowThreads / 32) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v = hs[tile * 128 + 32 * j + lane];
+      ss += v * v;
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) ss_out[(size_t)tile * M + t] = ss;
+  }
+}
+
 // fold[s][l][off + n] = sum_k W[l][n][k] * shift[s][l][k]: the constant that
 // adaRMS's shift adds to every output feature n of a GEMM, for each flow step
 // s and layer l (shift of norm `j` of the modulation table).  One warp per
@@ -1080,6 +1109,12 @@ cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_i
                                bool pdl) {
   return launch_k(k_inproj_norm, dim3(M), dim3(kRowThreads), (size_t)(A + D) * sizeof(float), s, pdl, x,
                   w_in, b_in, M, D, A, h, scale, aout, ss_out);
+}
+
+cudaError_t launch_embed_norm(const bf16* emb, int M, int D, float* h, const float* scale, bf16* aout,
+                              float* ss_out, cudaStream_t s, bool pdl) {
+  return launch_k(k_embed_norm, dim3(M), dim3(kRowThreads), (size_t)D * sizeof(float), s, pdl, emb, M, D, h, scale,
+                  aout, ss_out);
 }
 
 cudaError_t launch_fold_shift(const bf16* W, int N, int D, const float* mod, int S, int L, int j, float* fold,

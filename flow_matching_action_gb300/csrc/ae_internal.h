@@ -247,6 +247,9 @@ GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split = 0, bool
 cudaError_t gemm_kernel_setup();
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
                            TcGemmArgs a, cudaStream_t s, bool pdl);
+// h = emb (prefill input); aout = bf16(h * (1 + scale)); ss_out [D/128][M] sums of h^2.
+cudaError_t launch_embed_norm(const bf16* emb, int M, int D, float* h, const float* scale, bf16* aout,
+                              float* ss_out, cudaStream_t s, bool pdl);
 // h = x W_in^T + b_in; aout = bf16(h * (1 + scale)); ss_out [D/128][M] sums of h^2.
 cudaError_t launch_inproj_norm(const float* x, const bf16* w_in, const bf16* b_in, int M, int D, int A,
                                float* h, const float* scale, bf16* aout, float* ss_out, cudaStream_t s,
@@ -319,8 +322,17 @@ struct AttnScratch {
   int max_units;
   CUtensorMap omap;  // make_attn_o_map of part_o
 };
+// A prefill run of the layers (ae_prefill): embeddings replace the action
+// input projection, every layer's K and V are copied out after its QKV GEMM,
+// and nothing after the last layer's QKV GEMM runs.
+struct PrefillOut {
+  const bf16* emb;  // [M][D]
+  bf16* k;          // [L][M][Hkv dh]
+  bf16* v;
+};
 int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStream_t s,
-                     cudaError_t* err, const AttnScratch* attn_scratch = nullptr);
+                     cudaError_t* err, const AttnScratch* attn_scratch = nullptr,
+                     const PrefillOut* prefill = nullptr);
 // The cached time table of n_steps, or nullptr (never allocates).
 const TimeTable* find_time_table(const ae_ctx* c, int n_steps);
 void attn_plan(AttnArgs& a, int sm_count);

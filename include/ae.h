@@ -211,6 +211,26 @@ AE_API ae_status ae_bind_context(ae_ctx* ctx, int batch, const void* hidden, con
                           const uint8_t* prefix_mask);
 
 /*
+ * VLM prefill producing the prefix KV (OxyGen: the prefill of a frame's
+ * observation and instruction produces KV[t]; MolmoBot PR Part 2: the VLM
+ * backbone runs once per query).  The context must describe the VLM: a
+ * Gemma-style decoder with the action expert's layer, whose RMSNorm weights
+ * w are given as the biases (w, 0, 1) of zero modulation Linears (w_mod1 /
+ * w_mod2 zero, b_mod1 / b_mod2 = [w | 0 | 1]): RMSNorm x rsqrt(mean(x^2) +
+ * eps) (1 + w) with plain residuals.  `horizon` of its config is the number
+ * of prefix tokens of a request.  For each of `batch` requests the prefix
+ * tokens attend to each other (bidirectionally) at positions 0..horizon-1,
+ * and every layer's K (after RoPE) and V are written out in the layout
+ * ae_bind_prefix reads.  bf16 contexts only.
+ *   embeddings  device bf16 [batch * horizon][width], request-major
+ *   out_k, out_v device bf16 [layers][batch * horizon][n_kv_heads * head_dim]
+ * Replaces the context's binding (an empty prefix for `batch` requests).
+ * Errors: AE_ERR_UNSUPPORTED (fp32 context), AE_ERR_SHAPE (batch outside
+ * 1..max_batch), AE_ERR_INVALID_ARG, AE_ERR_OOM, AE_ERR_CUDA.
+ */
+AE_API ae_status ae_prefill(ae_ctx* ctx, int batch, const void* embeddings, void* out_k, void* out_v);
+
+/*
  * Run n_steps Euler steps of delta = -1/n_steps from t = 1 for every bound
  * request (MolmoBot Part 2), the velocity of step k taken at t = 1 - k/n_steps.
  *   noise        device fp32 [batch][horizon][action_dim], the state at t = 1
