@@ -474,6 +474,72 @@ def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm):
                          "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"})}
 
 
+def prefill_line(args, dist_ctx, tf_burst, tf_sust, peak_kind):
+    """The VLM prefill that produces the prefix KV (ae_prefill): a decoder with
+    the widths and depth of Pi0.5's 2B VLM (18 layers, D 2048, MLP 16384, 8 q
+    heads, one KV head, head_dim 256) over the 712-token two-camera prefix.
+    Its 4 GB of synthetic bf16 weights are drawn on the device (seeded
+    torch generator, N(0, 0.02); norm weights N(0, 0.1) in the modulation
+    biases, zero modulation weights), not through the host generator."""
+    import dataclasses
+    import torch
+    from flow_matching_action_gb300 import ae, synth
+    d = dataclasses.replace(synth.PI05_VLM_2L, layers=18)
+    g = torch.Generator(device="cuda").manual_seed(11)
+    D, F, L = d.width, d.mlp, d.layers
+
+    def rnd(*shape, std=synth.WEIGHT_STD):
+        return (torch.randn(*shape, generator=g, device="cuda") * std).to(torch.bfloat16)
+    zero_mod = torch.zeros(3 * D, D, dtype=torch.bfloat16, device="cuda")
+    w = {"w_in": rnd(D, d.action_dim), "b_in": rnd(D), "w_t1": rnd(D, D), "b_t1": rnd(D), "w_t2": rnd(D, D),
+         "b_t2": rnd(D), "w_mod_f": rnd(2 * D, D), "b_mod_f": rnd(2 * D), "w_out": rnd(d.action_dim, D),
+         "b_out": rnd(d.action_dim)}
+    shapes = dict(synth.layer_weight_shapes(d))
+    for name in synth.LAYER_WEIGHTS:
+        w[name] = []
+    for _ in range(L):
+        for name in synth.LAYER_WEIGHTS:
+            if name in ("w_mod1", "w_mod2"):
+                w[name].append(zero_mod)
+            elif name in ("b_mod1", "b_mod2"):
+                w[name].append(torch.cat([rnd(D, std=0.1), torch.zeros(D, dtype=torch.bfloat16, device="cuda"),
+                                          torch.ones(D, dtype=torch.bfloat16, device="cuda")]))
+            else:
+                w[name].append(rnd(*shapes[name]))
+    stream = torch.cuda.Stream()
+    ex = ae.ActionExpert(d, w, 1, 0, stream=stream.cuda_stream)
+    del w
+    n = d.horizon
+    emb = torch.randn(n, D, generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.empty(L, n, d.kv_dim, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    reps = max(args.reps // 5, 5)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            ae.ae_prefill(ex.ctx, 1, emb, k, v)
+        ex.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            ae.ae_prefill(ex.ctx, 1, emb, k, v)
+            b.record(stream)
+        torch.cuda.synchronize()
+    launches = ex.info()["launches_last_sample"]
+    ex.close()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    per_layer = 2 * n * (d.q_dim + 2 * d.kv_dim) * D
+    mlp_o = 2 * n * (D * d.q_dim + 3 * F * D)
+    attn = 4 * d.n_q_heads * n * n * d.head_dim
+    flops = L * (per_layer + attn) + (L - 1) * mlp_o  # the last layer stops after its K/V
+    tflops = flops / (ms / 1e3) / 1e12
+    return {"workload": f"VLM prefill: L={L} D={D} F={F} Hq={d.n_q_heads} Hkv={d.n_kv_heads} dh={d.head_dim}, "
+                        f"one request of {n} prefix tokens -> per-layer K/V",
+            "ms_per_prefill": ms, "prefills_timed": reps, "gpu_launches": launches,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_burst, "unit": "TFLOP/s",
+                         "frac": tflops / tf_burst, "peak_kind": f"{peak_kind} burst cuBLAS bf16",
+                         "algorithmic_flops": flops}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,6 +550,7 @@ def main():
     ap.add_argument("--batched", default="pi05_b16", help="second workload reported beside ('' = none)")
     ap.add_argument("--shared", default="pi05_shared16",
                     help="many samples over one shared prefix, reported beside ('' = none)")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the VLM prefill line")
     ap.add_argument("--context", default="pi05_context",
                     help="prefix as per-layer VLM hidden states projected at bind, reported beside ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -578,6 +645,8 @@ def main():
     for key, name in (("batched", args.batched), ("shared_prefix", args.shared), ("context", args.context)):
         if name:
             line[key] = side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm)
+    if not args.no_prefill:
+        line["prefill"] = prefill_line(args, dist_ctx, tf_burst, tf_sust, peak_kind)
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, w)
     if dist_ctx.rank == 0:
