@@ -605,12 +605,21 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
         // split K: stage this partial token-major in the drained pipeline
         // buffers, then send each rank its run of tokens with one bulk copy
         float* stg = reinterpret_cast<float*>(smem);
-#pragma unroll 1
-        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-          float v[16];
-          tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+        if constexpr (EW == 4) {
+          // a tile of at most 64 tokens: every column in one TMEM load and one wait
+          float v[64];
+          tmem_ld64(tmem_d + trow, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg[(c0 + j) * 128 + f] = v[j];
+          for (int j = 0; j < 64; ++j)
+            if (j < c_hi) stg[j * 128 + f] = v[j];
+        } else {
+#pragma unroll 1
+          for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem_d + trow + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) stg[(c0 + j) * 128 + f] = v[j];
+          }
         }
         fence_proxy_async_smem();
       }
