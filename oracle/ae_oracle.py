@@ -59,6 +59,13 @@ PINS = {
                        "weights reduce to rope(), masked rows skipped, projected once == recomputed",
     "prefill_request": "tests/test_oracle_pins.py: one layer against torch rms_norm/linear and the "
                        "complex-rotation RoPE; layer-0 K/V per token, deeper K/V see every token",
+    "e4m3_value": "tests/test_oracle_pins.py: all 256 codes against torch float8_e4m3fn",
+    "e4m3_round / e4m3_encode": "tests/test_oracle_pins.py: torch float8_e4m3fn casts of in-range values, "
+                                "ties to even at every midpoint, saturation closed form, code round trip",
+    "quantize_e4m3_per_tensor": "tests/test_oracle_pins.py: amax lands on 448, error bound of half a "
+                                "mantissa step, power-of-two scale invariance, amax 0",
+    "fp8_expert_weights": "tests/test_oracle_pins.py: weights already on the e4m3 grid (times a power "
+                          "of two) give the bf16 oracle's actions bitwise",
     "sample": "tests/test_oracle_pins.py: zero velocity, constant velocity closed form, pad/mask "
               "invariance (bitwise), hoisted == recomputed (bitwise), batch independence; "
               "end-to-end values: parity unpinned (no page prints an expected action)",
@@ -208,6 +215,102 @@ def expert_layer(h: np.ndarray, mods1, mods2, w: Dict, l: int, kp: np.ndarray, v
     if trace is not None:
         trace.update(y2=y2, m=m)
     return h + g2 * (m @ _f64(w["wd"][l]).T)
+
+
+# ---------------------------------------------------------------------------
+# fp8 e4m3 weights of the block Linears
+# ---------------------------------------------------------------------------
+
+# The Linears of the attention and MLP blocks: [MolmoBot] Part 3 converts the
+# blocks' fused QKV, attention output, gate/up and down Linears and keeps the
+# norms, embeddings and input/output projections in bf16; [LoongForge]
+# section 7 likewise keeps the action/time projections at their precision.
+FP8_LINEARS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
+E4M3_MAX = 448.0
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """Value of fp8 E4M3 codes (the e4m3 of [MolmoBot] Part 3 and [LoongForge] section 7).
+
+    The pages name the format without its bit layout.  Reading: the OCP 8-bit
+    floating-point E4M3 format ("e4m3fn"): bit 7 sign, bits 6..3 exponent with
+    bias 7, bits 2..0 mantissa; exponent field 0 holds subnormals m/8 * 2^-6;
+    S.1111.111 is NaN; there are no infinities, so the largest value is
+    1.75 * 2^8 = 448.
+    """
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 0xF) & (c & 0x7 == 0x7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest E4M3 value of each (finite) v, ties to the even mantissa; a
+    magnitude above 448 after rounding saturates to 448 (the saturating cast of
+    a per-tensor scaled weight, whose largest magnitude lands on 448).  The sign
+    of a value that rounds to zero is kept."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)               # binade of a; subnormals share 2^-6's
+    q = np.exp2(e - 3.0)                     # spacing of the 3-bit mantissa there
+    r = np.minimum(np.rint(a / q) * q, E4M3_MAX)  # rint: half to even
+    return np.copysign(r, v)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Codes of e4m3_round(v) (uint8), the sign bit set for negative values and -0."""
+    r = e4m3_round(v)
+    a = np.abs(r)
+    _, ex = np.frexp(a)
+    e = ex - 1
+    normal = a >= 2.0 ** -6
+    mant_n = np.where(normal, a / np.exp2(np.where(normal, e, 0)) * 8.0 - 8.0, 0.0)
+    code_n = ((np.where(normal, e, 0) + 7) << 3) + mant_n.astype(np.int64)
+    code_s = (a / 2.0 ** -9).astype(np.int64)
+    code = np.where(normal, code_n, code_s)
+    return (code | np.where(np.signbit(r), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_e4m3_per_tensor(w):
+    """Per-tensor fp8 of one weight matrix ([MolmoBot] Part 3: per-tensor dynamic
+    e4m3, amax -> scale -> cast, with the GEMM result restored by the scale;
+    [LoongForge] section 7: TorchAO's tensorwise recipe, inputs and weights
+    cast to fp8 and the result restored using the scales).
+
+    The pages print no formula.  Reading (the tensorwise convention): amax =
+    max |w|; s = fp32(448 / amax) (s = 1 when amax = 0); codes =
+    E4M3(fp32(w * s)); the Linear applies value(code) * r with r = fp32(1 / s).
+    Every step is one fp32 operation, rounded to nearest.  Only the weights
+    are quantized here: the activations of the path stay bf16 (the expert's
+    Linears see at most a few hundred action rows, and the pages' own fp8
+    passes drop GEMMs that small).  Returns (codes uint8 like w, r float32).
+    """
+    w32 = np.asarray(w, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(w32))) if w32.size else np.float32(0.0)
+    s = np.float32(E4M3_MAX) / amax if amax > 0 else np.float32(1.0)
+    codes = e4m3_encode(w32 * np.float32(s))
+    return codes, np.float32(np.float32(1.0) / np.float32(s))
+
+
+def fp8_expert_weights(w: Dict):
+    """The weights with every block Linear (FP8_LINEARS, every layer) replaced
+    by its fp8 form value(code) * r, in float64 (exact: 4 significant bits
+    times the 24 of r); every other weight unchanged.  Returns (weights,
+    {(name, layer): (codes, r)})."""
+    out = dict(w)
+    q = {}
+    for name in FP8_LINEARS:
+        deq = []
+        for l, W in enumerate(w[name]):
+            codes, r = quantize_e4m3_per_tensor(W)
+            q[(name, l)] = (codes, r)
+            deq.append(e4m3_value(codes) * np.float64(r))
+        out[name] = deq
+    return out, q
 
 
 # ---------------------------------------------------------------------------

@@ -451,3 +451,111 @@ def test_prefill_layer0_is_per_token_and_deeper_layers_see_every_token():
     np.testing.assert_array_equal(ks2[0][:-1], ks[0][:-1])   # layer 0: K/V of a token is its own
     np.testing.assert_array_equal(vs2[0][:-1], vs[0][:-1])
     assert np.abs(ks2[1][0] - ks[1][0]).max() > 1e-6          # layer 1: token 0 saw the last token
+
+
+# --------------------------------------------------------------------------- fp8 e4m3 weights
+def test_e4m3_value_matches_torch_float8_e4m3fn_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_value(codes)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[fin], ref[fin])
+    np.testing.assert_array_equal(np.signbit(got[fin]), np.signbit(ref[fin]))  # -0 is code 0x80
+    assert np.nanmax(got) == 448.0 and got[1] == 2.0 ** -9
+
+
+def _e4m3_grid():
+    v = O.e4m3_value(np.arange(0x7F))          # the 127 non-negative finite values, ascending
+    assert np.all(np.diff(v) > 0)
+    return v
+
+
+def test_e4m3_round_matches_torch_cast_in_range():
+    rng = np.random.default_rng(0)
+    grid = _e4m3_grid()
+    mids = (grid[1:] + grid[:-1]) / 2                                # every tie
+    near = np.concatenate([mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20)])
+    rand = np.concatenate([rng.normal(0, s, 4000) for s in (1e-3, 0.05, 1.0, 30.0, 150.0)])
+    x = np.concatenate([grid, mids, near, rand, [0.0, -0.0, 1e-6, -1e-6]]).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    x = np.concatenate([x, -x])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_round(x)
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(np.signbit(got), np.signbit(ref))
+
+
+def test_e4m3_round_ties_go_to_even_mantissa_and_saturate():
+    grid = _e4m3_grid()
+    codes = np.arange(0x7F)
+    mids = (grid[1:] + grid[:-1]) / 2
+    got = O.e4m3_encode(mids)
+    even = np.where(codes[:-1] % 2 == 0, codes[:-1], codes[1:])   # the even code of each pair
+    np.testing.assert_array_equal(got, even.astype(np.uint8))
+    # 464 is the tie between 448 and 480 (= the NaN pattern): above 448 saturates
+    for v in (448.0, 449.0, 463.9, 464.0, 470.0, 1e6):
+        assert O.e4m3_round(v) == 448.0 and O.e4m3_round(-v) == -448.0
+
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.arange(256)
+    v = O.e4m3_value(codes)
+    fin = ~np.isnan(v)
+    np.testing.assert_array_equal(O.e4m3_encode(v[fin]), codes[fin].astype(np.uint8))
+
+
+def test_quantize_per_tensor_amax_lands_on_448_and_error_bound():
+    rng = np.random.default_rng(1)
+    for scale in (0.02, 3.0, 1e-4):
+        w = synth.round_to_bf16(rng.normal(0, scale, (96, 64)))
+        codes, r = O.quantize_e4m3_per_tensor(w)
+        assert codes.dtype == np.uint8 and codes.shape == w.shape and r.dtype == np.float32
+        i = np.unravel_index(np.argmax(np.abs(w)), w.shape)
+        assert abs(O.e4m3_value(codes[i])) == 448.0
+        s = 1.0 / np.float64(r)
+        deq = O.e4m3_value(codes) * np.float64(r)
+        # half a mantissa step of w * s (2^-4 relative; 2^-10 absolute among
+        # subnormals), back in w's units, plus the fp32 roundings of s, w * s and r
+        bound = np.maximum(np.abs(w) * s * 2.0 ** -4, 2.0 ** -10) / s * (1 + 1e-6) + np.abs(w) * 4e-7
+        assert np.all(np.abs(deq - w) <= bound)
+
+
+def test_quantize_per_tensor_power_of_two_invariance_and_zero():
+    rng = np.random.default_rng(2)
+    w = synth.round_to_bf16(rng.normal(0, 0.02, (64, 32)))
+    c0, r0 = O.quantize_e4m3_per_tensor(w)
+    for k in (-3, 5):
+        c1, r1 = O.quantize_e4m3_per_tensor(w * 2.0 ** k)
+        np.testing.assert_array_equal(c1, c0)
+        assert r1 == np.float32(r0 * np.float32(2.0 ** k))
+    cz, rz = O.quantize_e4m3_per_tensor(np.zeros((4, 8)))
+    assert not cz.any() and rz == 1.0
+
+
+def _on_e4m3_grid(w, p):
+    """w moved onto the e4m3 grid times the power of two p, largest magnitude 448 p."""
+    out = dict(w)
+    for name in O.FP8_LINEARS:
+        out[name] = [O.e4m3_round(W / np.abs(W).max() * 448.0) * p for W in w[name]]
+    return out
+
+
+def test_fp8_weights_on_the_grid_reproduce_the_bf16_oracle_bitwise():
+    wl = synth.tiny_variant("masked")
+    w = _on_e4m3_grid(synth.make_weights(synth.TINY, 4), 2.0 ** -14)
+    w8, q = O.fp8_expert_weights(w)
+    assert len(q) == len(O.FP8_LINEARS) * synth.TINY.layers
+    for name in O.FP8_LINEARS:
+        for l in range(synth.TINY.layers):
+            np.testing.assert_array_equal(w8[name][l], w[name][l])
+            assert q[(name, l)][1] == np.float32(2.0 ** -14)
+    ref = O.sample(synth.TINY, w, wl.prefix_k, wl.prefix_v, wl.cu_lens, wl.mask, wl.noise, 3)
+    got = O.sample(synth.TINY, w8, wl.prefix_k, wl.prefix_v, wl.cu_lens, wl.mask, wl.noise, 3)
+    np.testing.assert_array_equal(got, ref)
+    # off the grid the fp8 weights do move the actions, by quantization noise only
+    w0 = synth.make_weights(synth.TINY, 4)
+    a = O.sample(synth.TINY, w0, wl.prefix_k, wl.prefix_v, wl.cu_lens, wl.mask, wl.noise, 3)
+    b = O.sample(synth.TINY, O.fp8_expert_weights(w0)[0], wl.prefix_k, wl.prefix_v, wl.cu_lens, wl.mask,
+                 wl.noise, 3)
+    assert 0 < np.abs(a - b).max() < 0.05 * np.abs(a).max()
