@@ -32,13 +32,18 @@ METRIC = "action chunks/s and µs/flow step (B=1,B=16); % HBM / bf16 tensor roof
 N_FLOW_STEPS = 10
 
 
-def algorithmic(dims, n_valid, n_act=None):
+def algorithmic(dims, n_valid, n_act=None, fp8_weights=False):
     """Algorithmic bytes and flops of ONE flow step (weights read once, prefix
-    KV of the valid rows read once per layer; activations neglected)."""
+    KV of the valid rows read once per layer; activations neglected).  With
+    fp8 weights a block-Linear weight is one byte, plus one fp32 factor per
+    weight row."""
     d = dims
     H = d.horizon if n_act is None else n_act
     per_layer_params = (d.q_dim + 2 * d.kv_dim) * d.width + d.width * d.q_dim + 3 * d.mlp * d.width
     weight_bytes = d.layers * per_layer_params * 2
+    if fp8_weights:
+        rows = (d.q_dim + 2 * d.kv_dim) + d.width + 2 * d.mlp + d.width
+        weight_bytes = d.layers * (per_layer_params + 4 * rows)
     kv_bytes = sum(d.layers * 2 * n * d.kv_dim * 2 for n in n_valid)
     B = len(n_valid)
     gemm_flops = 2 * d.layers * per_layer_params * B * H
@@ -158,7 +163,7 @@ def _dev(x, dtype):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_reps=50):
+def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_reps=50, fp8_weights=False):
     import torch
     from flow_matching_action_gb300 import ae
 
@@ -167,7 +172,7 @@ def run_gpu_arm(wl, weights_np, steps, warmup, dist_ctx, measure_e2e=True, stat_
              for k, v in weights_np.items()}
     stream = torch.cuda.Stream()
     ex = ae.ActionExpert(wl.dims, dev_w, max(wl.batch, 1), max(max(wl.n_rows), 1),
-                         stream=stream.cuda_stream)
+                         stream=stream.cuda_stream, fp8_weights=fp8_weights)
     del dev_w
     shared = getattr(wl, "shared_rows", None)
     rows = shared if shared is not None else None
@@ -434,16 +439,17 @@ def measured_traffic(workload: str):
     return rec.get("bytes_per_flow_step", {}).get(workload)
 
 
-def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm):
+def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm, fp8_weights=False):
     """A workload reported beside the headline one: against the HBM roofline at
     batch 1 (weight streaming), else against the bf16 tensor roofline."""
     wl2 = make_workload(name)
-    b2, f2 = algorithmic(wl2.dims, wl2.n_valid)
+    b2, f2 = algorithmic(wl2.dims, wl2.n_valid, fp8_weights=fp8_weights)
     reps2 = max(args.reps, args.steps)
     if wl2.dims.ctx_dim > 0:
         from flow_matching_action_gb300 import synth
         w = {**w, **synth.make_context_weights(wl2.dims, 0)}
-    r2 = run_gpu_arm(wl2, w, reps2, args.warmup, dist_ctx, measure_e2e=False, stat_reps=reps2)
+    r2 = run_gpu_arm(wl2, w, reps2, args.warmup, dist_ctx, measure_e2e=False, stat_reps=reps2,
+                     fp8_weights=fp8_weights)
     s2 = statistics.median(r2["sample_ms"])
     t2 = dist_ctx.max(r2["total_ms"]) / reps2
     tflops = f2 * wl2.n_steps / (s2 / 1e3) / 1e12
@@ -456,6 +462,9 @@ def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm):
         extra["context_projection"] = {"bind_ms_median": bm, "flops_per_bind": pf,
                                        "achieved_tflops": pf / (bm / 1e3) / 1e12,
                                        "frac_of_burst_bf16": pf / (bm / 1e3) / 1e12 / tf_burst}
+    if fp8_weights:
+        extra["weights"] = ("block Linears (wq wk wv wo wg wu wd) as per-tensor e4m3 codes, quantized by "
+                            "ae_create (AE_WEIGHTS_FP8_E4M3); everything else bf16 / fp32")
     return {**extra, "workload": describe(wl2), "chunks_per_s": wl2.batch / (t2 / 1e3) * dist_ctx.world,
             "ms_per_step": t2, "us_per_flow_step": s2 * 1e3 / wl2.n_steps,
             "sample_ms_median": s2, "sample_ms_p90": float(np.percentile(r2["sample_ms"], 90)),
@@ -553,6 +562,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the VLM prefill line")
     ap.add_argument("--context", default="pi05_context",
                     help="prefix as per-layer VLM hidden states projected at bind, reported beside ('' = none)")
+    ap.add_argument("--fp8", default="pi05_b1",
+                    help="workload also run with e4m3 block-Linear weights ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--reps", type=int, default=50, help="minimum ae_sample calls in the per-call statistics")
@@ -645,6 +656,9 @@ def main():
     for key, name in (("batched", args.batched), ("shared_prefix", args.shared), ("context", args.context)):
         if name:
             line[key] = side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm)
+    if args.fp8:
+        line["fp8_weights"] = side_line(args.fp8, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm,
+                                        fp8_weights=True)
     if not args.no_prefill:
         line["prefill"] = prefill_line(args, dist_ctx, tf_burst, tf_sust, peak_kind)
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:

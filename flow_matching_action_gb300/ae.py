@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(_PKG, "libae.so")
 AE_OK = 0
 AE_DTYPE_BF16 = 0
 AE_DTYPE_F32 = 1
+AE_WEIGHTS_AS_DTYPE = 0
+AE_WEIGHTS_FP8_E4M3 = 1
 AE_MAX_BATCH = 64
 AE_MAX_STEPS = 128
 
@@ -35,7 +37,7 @@ class ae_config(ctypes.Structure):
                 ("action_dim", ctypes.c_int), ("horizon", ctypes.c_int),
                 ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double),
                 ("time_min_period", ctypes.c_double), ("time_max_period", ctypes.c_double),
-                ("dtype", ctypes.c_int), ("ctx_dim", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("ctx_dim", ctypes.c_int), ("weight_format", ctypes.c_int)]
 
 
 _GLOBAL = ("w_in", "b_in", "w_t1", "b_t1", "w_t2", "b_t2", "w_mod_f", "b_mod_f", "w_out", "b_out")
@@ -73,6 +75,8 @@ _SIGNATURES = {
     "ae_last_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_size_t]),
     "ae_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ae_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ae_info)]),
+    "ae_get_fp8_weight": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.POINTER(ctypes.c_float)]),
     "ae_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64]),
 }
 
@@ -117,13 +121,14 @@ def ae_status_string(status: int) -> str:
     return lib().ae_status_string(status).decode()
 
 
-def make_config(dims, dtype: Optional[str] = None) -> ae_config:
+def make_config(dims, dtype: Optional[str] = None, fp8_weights: bool = False) -> ae_config:
     """An ae_config from any object with the expert-dimension attributes."""
     dt = dtype or dims.dtype
     return ae_config(dims.layers, dims.width, dims.mlp, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
                      dims.action_dim, dims.horizon, dims.rms_eps, dims.rope_theta,
                      dims.time_min_period, dims.time_max_period,
-                     AE_DTYPE_BF16 if dt == "bf16" else AE_DTYPE_F32, getattr(dims, "ctx_dim", 0))
+                     AE_DTYPE_BF16 if dt == "bf16" else AE_DTYPE_F32, getattr(dims, "ctx_dim", 0),
+                     AE_WEIGHTS_FP8_E4M3 if fp8_weights else AE_WEIGHTS_AS_DTYPE)
 
 
 def make_weights(w: Dict) -> ae_weights:
@@ -209,6 +214,18 @@ def ae_last_error(ctx) -> str:
     return _msg(ctx)
 
 
+FP8_LINEARS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")  # the `which` of ae_get_fp8_weight
+
+
+def ae_get_fp8_weight(ctx, layer: int, which: int, codes=None) -> float:
+    """Copy one quantized block Linear's e4m3 codes into `codes` (a writable
+    uint8 numpy array of the tensor's shape, or None) and return its factor r."""
+    r = ctypes.c_float(0.0)
+    ptr = None if codes is None else codes.ctypes.data_as(ctypes.c_void_p)
+    _check(lib().ae_get_fp8_weight(ctx, layer, which, ptr, ctypes.byref(r)), ctx)
+    return r.value
+
+
 def ae_get_info(ctx) -> dict:
     info = ae_info()
     _check(lib().ae_get_info(ctx, ctypes.byref(info)), ctx)
@@ -222,9 +239,9 @@ class ActionExpert:
     """
 
     def __init__(self, dims, weights: Dict, max_batch: int, max_prefix_rows: int, stream=None,
-                 dtype: Optional[str] = None):
+                 dtype: Optional[str] = None, fp8_weights: bool = False):
         self.dims = dims
-        self.config = make_config(dims, dtype)
+        self.config = make_config(dims, dtype, fp8_weights)
         self._wstruct = make_weights(weights)
         self.ctx = ae_create(self.config, self._wstruct, max_batch, max_prefix_rows, stream)
         self._bound = None

@@ -52,6 +52,17 @@ ae_status alloc(ae_ctx* c, P** p, size_t bytes) {
   return AE_OK;
 }
 
+// Free one allocation of the context before ae_destroy (bytes: its size).
+void release(ae_ctx* c, void* p, size_t bytes) {
+  for (size_t i = 0; i < c->allocations.size(); ++i)
+    if (c->allocations[i] == p) {
+      cudaFree(p);
+      c->allocations.erase(c->allocations.begin() + (long)i);
+      c->device_bytes -= (int64_t)(bytes == 0 ? 16 : bytes);
+      return;
+    }
+}
+
 #define AE_TRY(expr)                 \
   do {                               \
     ae_status s_ = (expr);           \
@@ -75,6 +86,10 @@ ae_status check_config(const ae_config* cfg) {
     return set_msg(nullptr, AE_ERR_INVALID_ARG, "eps, rope_theta and time periods must be > 0");
   if (cfg->ctx_dim < 0 || cfg->ctx_dim % 8 != 0)
     return set_msg(nullptr, AE_ERR_SHAPE, "ctx_dim must be 0 or a positive multiple of 8");
+  if (cfg->weight_format != AE_WEIGHTS_AS_DTYPE && cfg->weight_format != AE_WEIGHTS_FP8_E4M3)
+    return set_msg(nullptr, AE_ERR_INVALID_ARG, "weight_format must be AE_WEIGHTS_AS_DTYPE or AE_WEIGHTS_FP8_E4M3");
+  if (cfg->weight_format == AE_WEIGHTS_FP8_E4M3 && cfg->dtype != AE_DTYPE_BF16)
+    return set_msg(nullptr, AE_ERR_INVALID_ARG, "fp8 weights need dtype AE_DTYPE_BF16");
   return AE_OK;
 }
 
@@ -211,6 +226,48 @@ ae_status pack_weights(ae_ctx* c, const ae_weights* w) {
   return AE_OK;
 }
 
+// fp8 weights (MolmoBot PR, Part 3; LoongForge Pi0.5 blog, section 7): the
+// packed bf16 block Linears are quantized per tensor (wq, wk, wv, wo, wg, wu,
+// wd of every layer) into e4m3 codes of the same packed layout, which replace
+// them; every packed row gets its tensor's dequantization factor.
+ae_status quantize_weights(ae_ctx* c) {
+  const Dims& d = c->d;
+  const int L = d.L, D = d.D, F = d.F, qd = d.qdim(), kvd = d.kvdim(), nq = d.qkvdim();
+  const int n_slots = L * 7;
+  float *amax = nullptr, *sv = nullptr;
+  AE_TRY(alloc(c, &amax, n_slots * sizeof(float)));
+  AE_TRY(alloc(c, &sv, n_slots * sizeof(float)));
+  AE_TRY(alloc(c, &c->fp8_tensor_scale, n_slots * sizeof(float)));
+  AE_CK(c, cudaMemsetAsync(amax, 0, n_slots * sizeof(float), c->stream));
+  struct Mat {
+    void** w;
+    int rows, K;
+    ae::RowGroups g;
+    float** row_r;
+  } mats[4] = {{&c->w_qkv, nq, D, {nq, 0, qd, qd + kvd, 0}, &c->w_scale_qkv},
+               {&c->w_o, D, qd, {D, 0, D, D, 3}, &c->w_scale_o},
+               {&c->w_gu, 2 * F, D, {2 * F, 1, 0, 0, 4}, &c->w_scale_gu},
+               {&c->w_d, D, F, {D, 0, D, D, 6}, &c->w_scale_d}};
+  for (const Mat& m : mats)
+    AE_CK(c, ae::launch_tensor_amax((const ae::bf16*)*m.w, L, m.K, m.g, amax, c->stream));
+  AE_CK(c, ae::launch_tensor_scales(amax, n_slots, sv, c->fp8_tensor_scale, c->stream));
+  for (const Mat& m : mats) {
+    const size_t n = (size_t)L * m.rows * m.K;
+    uint8_t* codes = nullptr;
+    AE_TRY(alloc(c, &codes, n));
+    AE_TRY(alloc(c, m.row_r, (size_t)L * m.rows * sizeof(float)));
+    AE_CK(c, ae::launch_quantize_e4m3((const ae::bf16*)*m.w, L, m.K, m.g, sv, c->fp8_tensor_scale, codes, *m.row_r,
+                                      c->stream));
+    AE_CK(c, cudaStreamSynchronize(c->stream));
+    release(c, *m.w, n * sizeof(ae::bf16));
+    *m.w = codes;
+  }
+  release(c, amax, n_slots * sizeof(float));
+  release(c, sv, n_slots * sizeof(float));
+  c->w_fp8 = true;
+  return AE_OK;
+}
+
 ae_status alloc_scratch(ae_ctx* c) {
   const Dims& d = c->d;
   const size_t es = elem_size(d.dtype);
@@ -274,10 +331,17 @@ ae_status get_table(ae_ctx* c, int n_steps, const TimeTable** out) {
     // adaRMS's shift folded into the QKV and gate/up GEMMs: shift W^T per step and layer
     const int nq = d.qkvdim(), ng = 2 * d.F, nf = nq + ng;
     AE_TRY(alloc(c, &t.fold, S * L * (size_t)nf * sizeof(float)));
-    AE_CK(c, ae::launch_fold_shift((const ae::bf16*)c->w_qkv, nq, d.D, t.mod, n_steps, d.L, 0, t.fold, nf, 0,
-                                   c->stream));
-    AE_CK(c, ae::launch_fold_shift((const ae::bf16*)c->w_gu, ng, d.D, t.mod, n_steps, d.L, 1, t.fold, nf, nq,
-                                   c->stream));
+    if (c->w_fp8) {
+      AE_CK(c, ae::launch_fold_shift_e4m3((const uint8_t*)c->w_qkv, c->w_scale_qkv, nq, d.D, t.mod, n_steps, d.L, 0,
+                                          t.fold, nf, 0, c->stream));
+      AE_CK(c, ae::launch_fold_shift_e4m3((const uint8_t*)c->w_gu, c->w_scale_gu, ng, d.D, t.mod, n_steps, d.L, 1,
+                                          t.fold, nf, nq, c->stream));
+    } else {
+      AE_CK(c, ae::launch_fold_shift((const ae::bf16*)c->w_qkv, nq, d.D, t.mod, n_steps, d.L, 0, t.fold, nf, 0,
+                                     c->stream));
+      AE_CK(c, ae::launch_fold_shift((const ae::bf16*)c->w_gu, ng, d.D, t.mod, n_steps, d.L, 1, t.fold, nf, nq,
+                                     c->stream));
+    }
   }
   c->tables.push_back(t);
   *out = &c->tables.back();
@@ -451,9 +515,13 @@ ae_status ae_create(const ae_config* cfg, const ae_weights* w, int max_batch,
   if (st == AE_OK && cfg->dtype == AE_DTYPE_BF16) {
     std::string why;
     if (!ae::fast_path_supported(c->d, &why)) st = set_msg(c, AE_ERR_SHAPE, "%s", why.c_str());
+    // e4m3 weights stream in 128-column stages: every reduction length a multiple of 128
+    if (st == AE_OK && cfg->weight_format == AE_WEIGHTS_FP8_E4M3 && (c->d.qdim() % 128 || c->d.F % 128))
+      st = set_msg(c, AE_ERR_SHAPE, "fp8 weights need n_q_heads * head_dim and mlp multiples of 128");
     c->fast = true;
   }
   if (st == AE_OK) st = pack_weights(c, w);
+  if (st == AE_OK && cfg->weight_format == AE_WEIGHTS_FP8_E4M3) st = quantize_weights(c);
   if (st == AE_OK) st = alloc_scratch(c);
   if (st == AE_OK && c->fast) {
     e = ae::fast_setup(c);
@@ -664,6 +732,43 @@ ae_status ae_last_error(const ae_ctx* c, char* buf, size_t n) {
     buf[k] = '\0';
   }
   return c ? sticky(c) : AE_OK;
+}
+
+ae_status ae_get_fp8_weight(ae_ctx* c, int layer, int which, uint8_t* codes, float* scale) {
+  if (c == nullptr) return AE_ERR_INVALID_ARG;
+  if (!c->w_fp8) return set_msg(c, AE_ERR_UNSUPPORTED, "the context's weights are not fp8");
+  const Dims& d = c->d;
+  if (layer < 0 || layer >= d.L || which < 0 || which > 6)
+    return set_msg(c, AE_ERR_INVALID_ARG, "layer must be in 0..%d and which in 0..6", d.L - 1);
+  const size_t D = d.D, F = d.F, qd = d.qdim(), kvd = d.kvdim(), nq = d.qkvdim(), dh = d.dh;
+  const uint8_t* qkv = (const uint8_t*)c->w_qkv + (size_t)layer * nq * D;
+  if (codes != nullptr) {
+    const cudaMemcpyKind k = cudaMemcpyDeviceToHost;
+    if (which <= 2) {
+      // packed head rows 2j, 2j + 1 are the head's dims j, j + dh/2
+      const size_t heads = which == 0 ? d.Hq : d.Hkv;
+      const size_t row0 = which == 0 ? 0 : (which == 1 ? qd : qd + kvd);
+      for (size_t h = 0; h < heads; ++h) {
+        const uint8_t* src = qkv + (row0 + h * dh) * D;
+        uint8_t* dst = codes + h * dh * D;
+        AE_CK(c, cudaMemcpy2DAsync(dst, D, src, 2 * D, D, dh / 2, k, c->stream));
+        AE_CK(c, cudaMemcpy2DAsync(dst + dh / 2 * D, D, src + D, 2 * D, D, dh / 2, k, c->stream));
+      }
+    } else if (which == 3) {
+      AE_CK(c, cudaMemcpyAsync(codes, (const uint8_t*)c->w_o + (size_t)layer * D * qd, D * qd, k, c->stream));
+    } else if (which <= 5) {
+      // packed rows 2j, 2j + 1 are gate row j and up row j
+      const uint8_t* src = (const uint8_t*)c->w_gu + (size_t)layer * 2 * F * D + (which == 5 ? D : 0);
+      AE_CK(c, cudaMemcpy2DAsync(codes, D, src, 2 * D, D, F, k, c->stream));
+    } else {
+      AE_CK(c, cudaMemcpyAsync(codes, (const uint8_t*)c->w_d + (size_t)layer * D * F, D * F, k, c->stream));
+    }
+  }
+  if (scale != nullptr)
+    AE_CK(c, cudaMemcpyAsync(scale, c->fp8_tensor_scale + layer * 7 + which, sizeof(float), cudaMemcpyDeviceToHost,
+                             c->stream));
+  AE_CK(c, cudaStreamSynchronize(c->stream));
+  return AE_OK;
 }
 
 ae_status ae_get_info(const ae_ctx* c, ae_info* info) {

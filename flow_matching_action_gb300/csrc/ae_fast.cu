@@ -54,6 +54,26 @@ cudaError_t make_map(CUtensorMap* map, const void* ptr, long rows, long K, int b
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// e4m3 codes [rows, K] (one byte each); boxes of 128 rows x 128 codes, 128-byte
+// swizzle (the GEMM's widening step un-swizzles them as it writes the bf16 tiles).
+cudaError_t make_map_e4m3(CUtensorMap* map, const void* ptr, long rows, long K) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// A stacked weight's map: bf16 boxes, or e4m3 boxes when the context quantized its block Linears.
+cudaError_t make_weight_map(const ae_ctx* c, CUtensorMap* map, const void* ptr, long rows, long K) {
+  return c->w_fp8 ? make_map_e4m3(map, ptr, rows, K) : make_map(map, ptr, rows, K, 128);
+}
+
 }  // namespace
 
 bool fast_path_supported(const Dims& d, std::string* why) {
@@ -73,10 +93,10 @@ cudaError_t fast_setup(ae_ctx* c) {
   const Dims& d = c->d;
   cudaError_t e;
   const long maxM = (long)c->max_batch * d.H;
-  if ((e = make_map(&c->map_qkv, c->w_qkv, (long)d.L * d.qkvdim(), d.D, 128)) != cudaSuccess) return e;
-  if ((e = make_map(&c->map_o, c->w_o, (long)d.L * d.D, d.qdim(), 128)) != cudaSuccess) return e;
-  if ((e = make_map(&c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D, 128)) != cudaSuccess) return e;
-  if ((e = make_map(&c->map_d, c->w_d, (long)d.L * d.D, d.F, 128)) != cudaSuccess) return e;
+  if ((e = make_weight_map(c, &c->map_qkv, c->w_qkv, (long)d.L * d.qkvdim(), d.D)) != cudaSuccess) return e;
+  if ((e = make_weight_map(c, &c->map_o, c->w_o, (long)d.L * d.D, d.qdim())) != cudaSuccess) return e;
+  if ((e = make_weight_map(c, &c->map_gu, c->w_gu, (long)d.L * 2 * d.F, d.D)) != cudaSuccess) return e;
+  if ((e = make_weight_map(c, &c->map_d, c->w_d, (long)d.L * d.D, d.F)) != cudaSuccess) return e;
   if ((e = make_map(&c->map_qkv_act, c->qkv, maxM, d.qkvdim(), 16)) != cudaSuccess) return e;
   // query tiles load in boxes of whole padded heads where possible (fewer TMA issues)
   const int hp = (d.H + 15) & ~15;
@@ -145,10 +165,11 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
   const int nqkv = d.qkvdim(), qd = d.qdim();
   const float eps = (float)d.eps;
   const int sm = c->sm_count;
-  const GemmPlan pq = plan_gemm_cl(nqkv, D, M, sm, 0, true);
-  const GemmPlan po = plan_gemm_cl(D, qd, M, sm);
-  const GemmPlan pg = plan_gemm_cl(2 * F, D, M, sm);
-  const GemmPlan pd = plan_gemm_cl(D, F, M, sm);
+  const int wf = c->w_fp8 ? 1 : 0;
+  const GemmPlan pq = plan_gemm_cl(nqkv, D, M, sm, 0, true, 0, wf);
+  const GemmPlan po = plan_gemm_cl(D, qd, M, sm, 0, false, 0, wf);
+  const GemmPlan pg = plan_gemm_cl(2 * F, D, M, sm, 0, false, 0, wf);
+  const GemmPlan pd = plan_gemm_cl(D, F, M, sm, 0, false, 0, wf);
   // the O, gate/up and down GEMMs share one token tiling (it depends on M
   // only); the QKV GEMM may use more, shorter tiles through its own operand map
   // A single token tile loads only the M valid rows (the MMA still reads the
@@ -213,6 +234,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a.e_mode = kEQkvRope;
     a.act_rows = box_q;
     a.fold = fold(l);
+    a.w_scale = c->w_scale_qkv;
     a.out_bf16 = qkv;
     ck(launch_tc_gemm(c->map_qkv, c->map_yq, pq, a, s, pdl));
     ++n;
@@ -267,6 +289,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     // O projection -> gated residual -> operand of the gate/up GEMM (adaRMS2)
     a = base_args(l * D, ln * D);
     a.e_mode = kEResid;
+    a.w_scale = c->w_scale_o;
     a.h = c->h;
     a.gate = mod1 + 2 * D;
     a.scale_next = mod2;
@@ -279,6 +302,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     a = base_args(l * 2 * F, ln * 2 * F);
     a.e_mode = kEGeglu;
     a.fold = fold(l) + nqkv;
+    a.w_scale = c->w_scale_gu;
     a.out_bf16 = m;
     ck(launch_tc_gemm(c->map_gu, c->map_y, pg, a, s, pdl));
     ++n;
@@ -286,6 +310,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
     // down projection -> gated residual -> operand of the next layer's QKV GEMM
     a = base_args(l * D, ln * D);
     a.e_mode = kEResid;
+    a.w_scale = c->w_scale_d;
     a.h = c->h;
     a.gate = mod2 + 2 * D;
     a.scale_next = l + 1 < L ? mod(l + 1, 0) : nullptr;

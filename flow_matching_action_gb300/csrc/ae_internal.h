@@ -79,6 +79,15 @@ struct ae_ctx {
   void* w_d = nullptr;    // [L][D, F]
   void* w_mod = nullptr;  // [L][2][3D, D]
   void* b_mod = nullptr;  // [L][2][3D]
+  // fp8 weights (ae_config.weight_format AE_WEIGHTS_FP8_E4M3): w_qkv, w_o,
+  // w_gu and w_d hold e4m3 codes (uint8, same packed layout) instead of bf16,
+  // and w_scale_* the dequantization factor of each packed row's tensor.
+  bool w_fp8 = false;
+  float* w_scale_qkv = nullptr;  // [L][(Hq+2Hkv)dh]
+  float* w_scale_o = nullptr;    // [L][D]
+  float* w_scale_gu = nullptr;   // [L][2F]
+  float* w_scale_d = nullptr;    // [L][D]
+  float* fp8_tensor_scale = nullptr;  // [L][7] factor of wq, wk, wv, wo, wg, wu, wd
   // Context projection (ctx_dim > 0): per layer [K rows | V rows] of [2 Hkv dh, C];
   // rows of every head as rotation pairs when ctx_tc (the tensor-core path).
   void* w_ctx = nullptr;
@@ -219,6 +228,9 @@ struct TcGemmArgs {
   int n_ss, norm_dim;   // D / 128, D; n_ss == 0: no norm (a plain projection)
   float eps;
   const float* fold;    // [N] shift W^T of this layer and flow step (nullptr: none)
+  // fp8 weights: dequantization factor of every row of the stacked weight
+  // (row w_row0 + z * z_w_rows + n); unused by the bf16-weight kernels
+  const float* w_scale;
   bf16* out_bf16;       // kEQkvRope: [M][N]; kEGeglu: [M][N/2]
   const float2* rope_cs;
   int dh, n_rot_heads;
@@ -233,6 +245,7 @@ struct TcGemmArgs {
 struct GemmPlan {
   int N, K, n_tiles, tok_tiles, tok_tile, kb_total, ksplit, tmem_cols, stages, grid;
   int xbulk;  // split K: the fp32 tile fits the drained pipeline buffers, partials go by bulk copy
+  int wf;     // 1: the weights are e4m3 codes (the kernels that widen them to bf16)
   size_t smem;
 };
 size_t tc_gemm_smem_bytes(int stages, int tok_tile);
@@ -242,9 +255,33 @@ size_t tc_gemm_smem_bytes(int stages, int tok_tile);
 // tiles (the operand's TMA box must then follow the plan's tok_tile).
 // exact_split > 0: exactly that many K splits whatever M is (the sum order over
 // K, and so the rounding of every output, then does not depend on M).
+// wf = 1: e4m3 weights (an 8 KB staging buffer more per pipeline stage).
 GemmPlan plan_gemm_cl(int N, int K, int M, int sm_count, int max_split = 0, bool retile = false,
-                      int exact_split = 0);
+                      int exact_split = 0, int wf = 0);
 cudaError_t gemm_kernel_setup();
+// The e4m3-weight instantiations of k_tc_gemm (ae_gemm_fp8.cu).
+typedef void (*GemmKernel)(const CUtensorMap, const CUtensorMap, const TcGemmArgs);
+GemmKernel gemm_kernel_fp8(int ew, int mode, int xp);
+cudaError_t gemm_kernel_setup_fp8();
+// Per-tensor e4m3 quantization of a packed, layer-stacked bf16 weight
+// [L][rows][K] into codes [L][rows][K] (ae_gemm_fp8.cu).  The rows of one
+// layer belong to its tensors as `groups` says: tensors t0, t0 + 1, t0 + 2 over
+// the row ranges [0, b1), [b1, b2), [b2, rows) (kind 0; b1 = b2 = rows for a
+// single tensor), or alternately by row parity (kind 1: even rows t0, odd
+// rows t0 + 1).  Tensor t of layer l is slot l * 7 + t of amax / scale.
+struct RowGroups {
+  int rows, kind, b1, b2, t0;
+};
+// amax[l * 7 + t] = max |w| over the tensor (amax zeroed by the caller)
+cudaError_t launch_tensor_amax(const bf16* W, int L, int K, RowGroups g, float* amax, cudaStream_t s);
+// s = 448 / amax (1 when amax == 0) and r = 1 / s for n slots, fp32 round-to-nearest
+cudaError_t launch_tensor_scales(const float* amax, int n, float* s_out, float* r_out, cudaStream_t st);
+// codes = e4m3(w * s) (round to nearest even, saturating) and row_r[row] = r of the row's tensor
+cudaError_t launch_quantize_e4m3(const bf16* W, int L, int K, RowGroups g, const float* s_slot,
+                                 const float* r_slot, uint8_t* codes, float* row_r, cudaStream_t st);
+// launch_fold_shift over e4m3 codes: fold = r_row[n] * sum_k e4m3(W8[n][k]) shift[k]
+cudaError_t launch_fold_shift_e4m3(const uint8_t* W8, const float* row_r, int N, int D, const float* mod, int S,
+                                   int L, int j, float* fold, int nf, int off, cudaStream_t s);
 cudaError_t launch_tc_gemm(const CUtensorMap& wmap, const CUtensorMap& amap, const GemmPlan& p,
                            TcGemmArgs a, cudaStream_t s, bool pdl);
 // h = emb (prefill input); aout = bf16(h * (1 + scale)); ss_out [D/128][M] sums of h^2.

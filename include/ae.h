@@ -67,6 +67,22 @@ typedef enum {
 
 typedef enum { AE_DTYPE_BF16 = 0, AE_DTYPE_F32 = 1 } ae_dtype;
 
+/*
+ * Storage of the block Linears (wq, wk, wv, wo, wg, wu, wd of every layer).
+ * AE_WEIGHTS_FP8_E4M3 (MolmoBot PR, Part 3: per-tensor dynamic fp8 on the
+ * blocks' fused QKV, attention output, gate/up and down Linears; LoongForge
+ * blog, section 7: TorchAO's tensorwise recipe, the result restored using the
+ * scales): ae_create quantizes each of these tensors on its own, amax =
+ * max |w|, s = fp32(448 / amax) (1 if amax == 0), code = E4M3(fp32(w * s))
+ * with round-to-nearest-even and saturation at +-448 (the OCP "e4m3fn"
+ * format: bias 7, subnormals, no infinities), and every GEMM output of the
+ * tensor is multiplied by r = fp32(1 / s).  The library then holds the codes
+ * (one byte per weight) instead of bf16 copies, halving the bytes every flow
+ * step streams.  Activations, norms, the time MLP, the modulation, the
+ * input/output and context projections stay bf16 / fp32.  bf16 contexts only.
+ */
+typedef enum { AE_WEIGHTS_AS_DTYPE = 0, AE_WEIGHTS_FP8_E4M3 = 1 } ae_weight_format;
+
 /* Limits checked by the host side of every call. */
 #define AE_MAX_BATCH 64  /* requests per ae_bind_prefix                  */
 #define AE_MAX_STEPS 128 /* Euler steps per ae_sample                    */
@@ -97,6 +113,7 @@ typedef struct {
   int ctx_dim;     /* C, width of the per-layer VLM hidden states that
                       ae_bind_context projects into K/V; 0 = no context
                       projection (w_ck / w_cv are then ignored) */
+  int weight_format; /* ae_weight_format of the block Linears */
 } ae_config;
 
 /*
@@ -135,6 +152,8 @@ typedef struct {
  *   out             receives the context; set to NULL on failure
  * Allocates all device memory the context will use (weights, scratch, bind
  * tables); later calls allocate only a per-n_steps time table on first use.
+ * With cfg->weight_format == AE_WEIGHTS_FP8_E4M3 the block Linears are
+ * quantized here (see ae_weight_format).
  * Errors: AE_ERR_INVALID_ARG, AE_ERR_SHAPE, AE_ERR_UNSUPPORTED, AE_ERR_OOM,
  * AE_ERR_CUDA.
  */
@@ -310,6 +329,20 @@ AE_API ae_status ae_last_error(const ae_ctx* ctx, char* buf, size_t n);
 
 /* Static name of a status code. */
 AE_API const char* ae_status_string(ae_status s);
+
+/*
+ * Copy out one quantized block Linear of a context created with
+ * AE_WEIGHTS_FP8_E4M3, in the caller's layout (row-major [out, in], rows in
+ * the order of the weight given to ae_create, whatever the library's packing).
+ *   layer   0..layers-1
+ *   which   0 wq, 1 wk, 2 wv, 3 wo, 4 wg, 5 wu, 6 wd
+ *   codes   HOST uint8 with room for the tensor's out * in codes, or NULL
+ *   scale   HOST float: the tensor's dequantization factor r, or NULL
+ * Synchronizes the context's stream.
+ * Errors: AE_ERR_INVALID_ARG (NULL ctx, layer or which out of range),
+ * AE_ERR_UNSUPPORTED (the weights are not fp8), AE_ERR_CUDA.
+ */
+AE_API ae_status ae_get_fp8_weight(ae_ctx* ctx, int layer, int which, uint8_t* codes, float* scale);
 
 /* Counters a caller can read after ae_sample, e.g. to report kernel launches. */
 typedef struct {

@@ -63,12 +63,13 @@ def device_weights(w, dtype):
 class GpuRunner:
     """One library context for a dims/weights pair; runs workloads through the C ABI."""
 
-    def __init__(self, dims, w, dtype=None, max_batch=16, max_rows=MAX_ROWS):
+    def __init__(self, dims, w, dtype=None, max_batch=16, max_rows=MAX_ROWS, fp8_weights=False):
         from flow_matching_action_gb300 import ae
         self.dtype = dtype or dims.dtype
         self.dims = dims
         self.dev_w = device_weights(w, self.dtype)
-        self.expert = ae.ActionExpert(dims, self.dev_w, max_batch, max_rows, dtype=self.dtype)
+        self.expert = ae.ActionExpert(dims, self.dev_w, max_batch, max_rows, dtype=self.dtype,
+                                      fp8_weights=fp8_weights)
 
     def upload(self, wl):
         import torch

@@ -55,7 +55,8 @@ def _weights_struct(dims, n_layers=None):
 @pytest.mark.parametrize("field,value,status", [
     ("layers", 0, -1), ("width", 30, -2), ("head_dim", 48, -2), ("head_dim", 512, -2),
     ("n_kv_heads", 3, -2), ("dtype", 7, -1), ("rms_eps", 0.0, -1), ("mlp", -4, -1),
-    ("ctx_dim", -8, -2), ("ctx_dim", 100, -2)])
+    ("ctx_dim", -8, -2), ("ctx_dim", 100, -2), ("weight_format", 2, -1),
+    ("weight_format", 1, -1)])  # TINY is fp32: fp8 weights need a bf16 context
 def test_create_rejects_bad_config(lib, field, value, status):
     cfg = ae.make_config(synth.TINY)
     setattr(cfg, field, value)
@@ -76,6 +77,7 @@ def test_create_rejects_null_weights_and_bad_batch(lib):
 
 
 def test_calls_on_null_context_are_rejected(lib):
+    assert lib.ae_get_fp8_weight(None, 0, 0, None, None) == -1
     assert lib.ae_sample(None, None, 1, None) == -1
     assert lib.ae_bind_prefix(None, 0, None, None, None, None) == -1
     assert lib.ae_bind_prefix_shared(None, 1, None, None, 10, None) == -1
