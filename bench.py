@@ -472,7 +472,10 @@ def side_line(name, w, args, dist_ctx, tf_burst, tf_sust, peak_kind, hbm, fp8_we
             "clocks": r2["clocks"],
             "roofline": ({"bound": "hbm", "achieved": b2 * wl2.n_steps / (s2 / 1e3) / 1e9, "peak": hbm,
                           "unit": "GB/s", "frac": b2 * wl2.n_steps / (s2 / 1e3) / 1e9 / hbm,
-                          "algorithmic_bytes_per_flow_step": b2} if wl2.batch == 1 else
+                          "algorithmic_bytes_per_flow_step": b2,
+                          "traffic": measured_traffic(name + ("_fp8" if fp8_weights else "")),
+                          "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)"}
+                         if wl2.batch == 1 else
                          {"bound": "tensor", "achieved": tflops, "peak": tf_sust,
                          "unit": "TFLOP/s", "frac": tflops / tf_sust,
                          "peak_burst": tf_burst, "frac_of_burst": tflops / tf_burst,
@@ -562,6 +565,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the VLM prefill line")
     ap.add_argument("--context", default="pi05_context",
                     help="prefix as per-layer VLM hidden states projected at bind, reported beside ('' = none)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
+                    help="block-Linear weights of the headline workload (fp8: AE_WEIGHTS_FP8_E4M3)")
     ap.add_argument("--fp8", default="pi05_b1",
                     help="workload also run with e4m3 block-Linear weights ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -575,7 +580,8 @@ def main():
     from flow_matching_action_gb300 import synth
     wl = make_workload(args.workload)
     w = synth.make_weights(wl.dims, 0)
-    bytes_fs, flops_fs = algorithmic(wl.dims, wl.n_valid)
+    fp8_main = args.weights == "fp8"
+    bytes_fs, flops_fs = algorithmic(wl.dims, wl.n_valid, fp8_weights=fp8_main)
 
     if args.impl == "reference":
         if dist_ctx.rank != 0:
@@ -617,7 +623,7 @@ def main():
     ae_build.build()
 
     res = run_gpu_arm(wl, w, args.steps, args.warmup, dist_ctx, measure_e2e=not args.no_e2e,
-                      stat_reps=args.reps)
+                      stat_reps=args.reps, fp8_weights=fp8_main)
     total_ms = dist_ctx.max(res["total_ms"])
     ms_per_step = total_ms / args.steps
     chunks = wl.batch * args.steps * dist_ctx.world
@@ -634,7 +640,9 @@ def main():
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) prefix KV and noise)",
         "config": {"workload": describe(wl), "batch": wl.batch, "valid_prefix_rows": wl.n_valid,
                    "n_flow_steps": wl.n_steps, "step": "ae_bind_prefix + ae_sample(10 Euler steps)",
-                   "l2": "inputs larger than L2: 623 MB of bf16 weights streamed per flow step",
+                   "l2": ("inputs larger than L2: 311 MB of e4m3 block-Linear weights streamed per flow step"
+                          if fp8_main else "inputs larger than L2: 623 MB of bf16 weights streamed per flow step"),
+                   "weights": "e4m3 block Linears (AE_WEIGHTS_FP8_E4M3)" if fp8_main else "bf16",
                    "parallelism": f"replicas x{dist_ctx.world}"},
         "us_per_flow_step": sample_ms * 1e3 / wl.n_steps,
         "sample_ms_median": sample_ms, "sample_ms_p90": float(np.percentile(res["sample_ms"], 90)),
@@ -642,7 +650,8 @@ def main():
         "bind_ms_median": bind_ms,
         "roofline": {"kernel": "ae_sample (all its launches, one flow step = 1 unit)",
                      "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm, "traffic": measured_traffic(args.workload),
+                     "frac": achieved_gbs / hbm,
+                     "traffic": measured_traffic(args.workload + ("_fp8" if fp8_main else "")),
                      "traffic_unit": "DRAM bytes read + written per flow step (ncu, warm L2)",
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_flow_step": bytes_fs},

@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
       }
       if (a.w_next_row0 >= 0)
         for (int it = 0; it < n_it; ++it)
-          tma_prefetch_l2_2d(&wmap, (kb_begin + it) * 64, a.w_next_row0 + n_tile * 128);
+          tma_prefetch_l2_2d(&wmap, kcol(it), a.w_next_row0 + n_tile * 128);
       pdl_wait();
       for (int it = 0; it < pre; ++it) {
         if (WF) mbar_arrive_expect_tx(&full[it], bytes);
