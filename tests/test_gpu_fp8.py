@@ -180,3 +180,32 @@ def test_fp8_export_rejected_on_bf16_context():
             rf.close()
     finally:
         r.close()
+
+
+def test_pi05_fp8_shared_prefix_equals_bound_copies(pi05_fp8_runner):
+    """One prefix shared by 4 samples (OxyGen cross-task KV sharing) on an fp8
+    context: bitwise the result of binding 4 copies (the same kernels)."""
+    from .test_gpu_shared_prefix import copies_of, run_shared
+    wl = synth.pi05_two_camera()
+    many = copies_of(wl, 4, noise_seed=31)
+    shared = run_shared(pi05_fp8_runner, wl, many.noise)
+    copied = pi05_fp8_runner.run(many)
+    assert np.isfinite(shared).all()
+    np.testing.assert_array_equal(shared, copied)
+
+
+def test_pi05_fp8_context_projection_matches_oracle():
+    """The projected-context prefix (MolmoBot PR, Part 2) with fp8 block
+    Linears: the context projections stay bf16, the expert's Linears are e4m3."""
+    from .test_gpu_context import run_ctx
+    dims = synth.PI05_CTX
+    wc = synth.make_context_weights(dims, 0)
+    wl = synth.pi05_context(0)
+    r = GpuRunner(dims, {**weights("pi05"), **wc}, max_batch=1, max_rows=max(wl.n_rows), fp8_weights=True)
+    try:
+        got = run_ctx(r, wl)
+    finally:
+        r.close()
+    ref = oracle_actions(wl, {**fp8_oracle_weights("pi05"), **wc}, context=(wl.context, wc["w_ck"], wc["w_cv"]))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= ACT_TOL
