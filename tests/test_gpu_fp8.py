@@ -209,3 +209,23 @@ def test_pi05_fp8_context_projection_matches_oracle():
     ref = oracle_actions(wl, {**fp8_oracle_weights("pi05"), **wc}, context=(wl.context, wc["w_ck"], wc["w_cv"]))
     assert np.isfinite(got).all()
     assert np.abs(got - ref).max() <= ACT_TOL
+
+
+@pytest.mark.parametrize("which", ["tiny", "pi05_2l"])
+def test_vlm_prefill_with_fp8_weights_matches_oracle(which):
+    """ae_prefill (OxyGen: the prefill produces KV[t]) through the e4m3 GEMMs,
+    including the long-K down projection of a 16384-wide MLP, against the
+    oracle's prefill on the same fp8 weights: every layer's K and V within
+    relative L2 1e-2."""
+    from .test_gpu_prefill import gpu_prefill, oracle_prefill, rel_l2 as rl2
+    if which == "tiny":
+        d = dataclasses.replace(synth.TINY_VLM, dtype="bf16")
+        w, emb, batch = synth.make_vlm_weights(d, 3), synth.prefix_embeddings(d, 3, 2), 2
+    else:
+        d = synth.PI05_VLM_2L
+        w, emb, batch = synth.make_vlm_weights(d, 0), synth.prefix_embeddings(d, 0, 1), 1
+    k, v = gpu_prefill(d, w, emb, batch, fp8_weights=True)
+    rk, rv = oracle_prefill(d, O.fp8_expert_weights(w)[0], emb, batch)
+    for l in range(d.layers):
+        assert rl2(k[l], rk[l]) <= 1e-2, (l, rl2(k[l], rk[l]))
+        assert rl2(v[l], rv[l]) <= 1e-2, (l, rl2(v[l], rv[l]))

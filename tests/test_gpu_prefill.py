@@ -21,11 +21,11 @@ def rel_l2(a, b):
     return float(np.sqrt(((a - b) ** 2).sum()) / np.sqrt((b ** 2).sum()))
 
 
-def gpu_prefill(dims, w, emb, batch):
+def gpu_prefill(dims, w, emb, batch, fp8_weights=False):
     import torch
     from flow_matching_action_gb300 import ae
     dev_w = device_weights(w, "bf16")
-    ex = ae.ActionExpert(dims, dev_w, batch, 0, dtype="bf16")
+    ex = ae.ActionExpert(dims, dev_w, batch, 0, dtype="bf16", fp8_weights=fp8_weights)
     try:
         e = torch.from_numpy(np.ascontiguousarray(emb)).cuda().to(torch.bfloat16)
         k = torch.empty((dims.layers, batch * dims.horizon, dims.kv_dim), dtype=torch.bfloat16, device="cuda")
