@@ -79,7 +79,9 @@ typedef enum { AE_DTYPE_BF16 = 0, AE_DTYPE_F32 = 1 } ae_dtype;
  * tensor is multiplied by r = fp32(1 / s).  The library then holds the codes
  * (one byte per weight) instead of bf16 copies, halving the bytes every flow
  * step streams.  Activations, norms, the time MLP, the modulation, the
- * input/output and context projections stay bf16 / fp32.  bf16 contexts only.
+ * input/output and context projections stay bf16 / fp32.  bf16 contexts only
+ * (AE_ERR_INVALID_ARG otherwise), with n_q_heads * head_dim and mlp multiples
+ * of 128 (AE_ERR_SHAPE otherwise).
  */
 typedef enum { AE_WEIGHTS_AS_DTYPE = 0, AE_WEIGHTS_FP8_E4M3 = 1 } ae_weight_format;
 
