@@ -30,3 +30,22 @@ def test_traffic_record_is_used_only_for_its_own_sources():
         assert got == rec["bytes_per_flow_step"]["pi05_b1"]
     else:
         assert got is None
+
+
+def test_fp8_traffic_and_algorithmic_bytes():
+    """e4m3 block Linears: one byte a weight plus a 4-byte factor per weight
+    row; the measured traffic of that path streams the codes once, at about
+    half the bf16 path's bytes."""
+    from flow_matching_action_gb300 import synth
+    d = synth.PI05
+    b16, f16 = bench.algorithmic(d, [712])
+    b8, f8 = bench.algorithmic(d, [712], fp8_weights=True)
+    per_layer = (d.q_dim + 2 * d.kv_dim) * d.width + d.width * d.q_dim + 3 * d.mlp * d.width
+    rows = (d.q_dim + 2 * d.kv_dim) + d.width + 2 * d.mlp + d.width
+    kv = d.layers * 2 * 712 * d.kv_dim * 2
+    assert b16 == d.layers * per_layer * 2 + kv == 635977728
+    assert b8 == d.layers * (per_layer + 4 * rows) + kv == 325472256
+    assert f8 == f16  # the arithmetic is the same bf16 MMA work
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        rec = json.load(f)["bytes_per_flow_step"]
+    assert 311e6 < rec["pi05_b1_fp8"] < 0.55 * rec["pi05_b1"]
