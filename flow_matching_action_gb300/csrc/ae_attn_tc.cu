@@ -18,7 +18,8 @@
 // its chunks with an online softmax, the next chunk's K/V loading while the
 // current one computes:
 //   S = Q K^T      tcgen05, M = 128 query rows, N = 64 keys, K = dh; S in TMEM
-//   P = exp(S - m) fp32 per query row (one thread per row), bf16 into smem
+//   P = exp(S - m) fp32 per query row (two threads per row, 32 keys each;
+//                  the row's maximum and sum combined through shared memory), bf16 into smem
 //   O += P V       tcgen05, M = 128, N = dh, K = 64 keys; O stays in TMEM
 // The exponent reference m is raised (and O, l rescaled in place) only when a
 // chunk's maximum exceeds it by more than 8, so P <= e^8 and most chunks skip
@@ -40,7 +41,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;  // two warps per TMEM lane quarter
 constexpr int kChunk = 64;             // keys per chunk
 constexpr float kRescaleMargin = 8.f;  // raise the exponent reference only past this
 constexpr int kSkip = -0x40000000;     // gather code: zero-fill
@@ -72,7 +73,7 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int dh) {
   L.p = L.v[1] + kv;
   L.bars = L.p + 128 * kChunk * 2;  // bar_s, bar_o, bar_q, bar_kv[2], TMEM base, abort flag
   L.idx = L.bars + 64;              // [2][kChunk] gather codes of the two K/V buffers
-  L.total = L.idx + 2 * kChunk * 4;
+  L.total = L.idx + 2 * kChunk * 4 + 2 * 2 * 128 * 4;  // + per-half row maxima and sums [2][2][128]
   return L;
 }
 
@@ -267,8 +268,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_p;
   const uint32_t tm_o = tmem, tm_s = tmem + (uint32_t)dh;
-  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-  const int row = threadIdx.x;
+  // the two warps of a TMEM lane quarter take the same 32 rows; half h takes
+  // keys 32 h.. of a chunk and the O columns of its half
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  const int row = threadIdx.x & 127;
+  const int half = threadIdx.x >> 7;
+  float* red_m = reinterpret_cast<float*>(smem + L.idx + 2 * kChunk * 4);  // [2][128]
+  float* red_l = red_m + 2 * 128;                                         // [2][128]
   float m_ref = -INFINITY, l = 0.f;
   bool failed = false;
   uint32_t kv_phase[2] = {0u, 0u};  // used by thread 0 only
@@ -321,15 +327,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_after();
     // scores in the log2 domain: s * scale * log2(e), so exp() becomes one exp2
     const float sl2 = a.scale * 1.4426950408889634f;
-    float s[kChunk];
-    tmem_ld64(tm_s + lane_off, s);
+    float s[32];
+    tmem_ld32(tm_s + lane_off + (uint32_t)(32 * half), s);
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
+    for (int j = 0; j < 32; ++j) {
       s[j] *= sl2;
-      if (j < nk) mx[j & 3] = fmaxf(mx[j & 3], s[j]);
+      if (32 * half + j < nk) mx[j & 3] = fmaxf(mx[j & 3], s[j]);
     }
-    const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    red_m[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    __syncthreads();
+    const float cmax = fmaxf(red_m[row], red_m[128 + row]);
     // raise the exponent reference; O (in TMEM) and l follow it
     float factor = 1.f;
     if (ci == 0) {
@@ -341,7 +349,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (__any_sync(0xffffffffu, factor != 1.f)) {
       l *= factor;
 #pragma unroll 1
-      for (int c0 = 0; c0 < dh; c0 += 16) {
+      for (int c0 = half * (dh / 2); c0 < (half + 1) * (dh / 2); c0 += 16) {
         float v[16];
         tmem_ld16(tm_o + lane_off + (uint32_t)c0, v);
 #pragma unroll
@@ -349,27 +357,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_st16(tm_o + lane_off + (uint32_t)c0, v);
       }
     }
-    uint32_t pk[kChunk / 2];
+    uint32_t pk[16];
     float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains, added in a fixed order
 #pragma unroll
-    for (int j = 0; j < kChunk; j += 2) {
-      const float p0 = (j < nk) ? ex2_fast(s[j] - m_ref) : 0.f;
-      const float p1 = (j + 1 < nk) ? ex2_fast(s[j + 1] - m_ref) : 0.f;
+    for (int j = 0; j < 32; j += 2) {
+      const int key = 32 * half + j;
+      const float p0 = (key < nk) ? ex2_fast(s[j] - m_ref) : 0.f;
+      const float p1 = (key + 1 < nk) ? ex2_fast(s[j + 1] - m_ref) : 0.f;
       const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
       // the row sum uses the bf16-rounded weights, the values P V multiplies
       const float2 pr = __bfloat1622float2(pb);
       ls[(j >> 1) & 3] += pr.x + pr.y;
       pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
     }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    red_l[half * 128 + row] = (ls[0] + ls[1]) + (ls[2] + ls[3]);
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc)
-      *reinterpret_cast<uint4*>(smem + L.p + sw128_offset(row, cc)) =
+    for (int cc = 0; cc < 4; ++cc)
+      *reinterpret_cast<uint4*>(smem + L.p + sw128_offset(row, 4 * half + cc)) =
           make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    l += red_l[row] + red_l[128 + row];
     // ---- O += P V: V rows are the MN-major operand (dims along MN in 64-dim
     //      blocks 8 KB apart, keys along K in 8-key atoms 1 KB apart)
     if (threadIdx.x == 0) {
@@ -410,7 +420,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // bf16 rows of O / l (half the bytes of fp32 partials): boxes of 64 columns
       const float inv_l = 1.f / l;
 #pragma unroll 1
-      for (int c0 = 0; c0 < dh; c0 += 64) {
+      for (int c0 = 64 * half; c0 < dh; c0 += 128) {
         float v[64];
         tmem_ld64(tm_o + lane_off + (uint32_t)c0, v);
         uint8_t* box = stg + (c0 >> 6) * (128 * 128);
@@ -424,7 +434,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     } else {
 #pragma unroll 1
-      for (int c0 = 0; c0 < dh; c0 += 64) {
+      for (int c0 = 64 * half; c0 < dh; c0 += 128) {
         float v[64];
         tmem_ld64(tm_o + lane_off + (uint32_t)c0, v);
 #pragma unroll
@@ -437,7 +447,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     // the stored maximum is in the log2 domain of the scaled scores
-    if (valid_row) a.part_ml[unit * 128 + row] = make_float2(m_ref, l);
+    if (valid_row && half == 0) a.part_ml[unit * 128 + row] = make_float2(m_ref, l);
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0) {
