@@ -19,8 +19,10 @@
 // current one computes:
 //   S = Q K^T      tcgen05, M = 128 query rows, N = 64 keys, K = dh; S in TMEM
 //   P = exp(S - m) fp32 per query row (two threads per row, 32 keys each;
-//                  the row's maximum and sum combined through shared memory), bf16 into smem
-//   O += P V       tcgen05, M = 128, N = dh, K = 64 keys; O stays in TMEM
+//                  the row's maximum and sum combined through shared memory),
+//                  bf16 back into TMEM over the S columns already read
+//   O += P V       tcgen05 with P as the TMEM A operand, M = 128, N = dh,
+//                  K = 64 keys; O stays in TMEM
 // The exponent reference m is raised (and O, l rescaled in place) only when a
 // chunk's maximum exceeds it by more than 8, so P <= e^8 and most chunks skip
 // the rescale.  Each CTA stores its partial (TMA store) with (m, l): bf16 rows
@@ -57,11 +59,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 struct AttnSmem {
-  uint32_t q, k[2], v[2], p, bars, idx, total;  // byte offsets from the 1024-aligned base
+  uint32_t q, k[2], v[2], bars, idx, total;  // byte offsets from the 1024-aligned base
 };
 
 // Q: [dh/64][128 rows][128 B].  K and V: [dh/64][64 keys][128 B] (8 KB blocks),
-// double buffered.  P: [128 rows][128 B].  All 128-byte swizzled.
+// double buffered.  All 128-byte swizzled.
 __host__ __device__ inline AttnSmem attn_smem_layout(int dh) {
   AttnSmem L;
   const uint32_t kv = (uint32_t)dh * kChunk * 2;
@@ -70,8 +72,7 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int dh) {
   L.k[1] = L.k[0] + kv;
   L.v[0] = L.k[1] + kv;
   L.v[1] = L.v[0] + kv;
-  L.p = L.v[1] + kv;
-  L.bars = L.p + 128 * kChunk * 2;  // bar_s, bar_o, bar_q, bar_kv[2], TMEM base, abort flag
+  L.bars = L.v[1] + kv;  // bar_s, bar_o, bar_q, bar_kv[2], TMEM base, abort flag
   L.idx = L.bars + 64;              // [2][kChunk] gather codes of the two K/V buffers
   L.total = L.idx + 2 * kChunk * 4 + 2 * 2 * 128 * 4;  // + per-half row maxima and sums [2][2][128]
   return L;
@@ -371,24 +372,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
     }
     red_l[half * 128 + row] = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    {
+      // P over the S columns already read (every thread loaded its S before
+      // the maximum exchange): column j of the row holds keys 2j, 2j + 1, the
+      // A operand of P V in tensor memory
+      float pf[16];
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc)
-      *reinterpret_cast<uint4*>(smem + L.p + sw128_offset(row, 4 * half + cc)) =
-          make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-    fence_proxy_async_smem();
+      for (int j = 0; j < 16; ++j) pf[j] = __uint_as_float(pk[j]);
+      tmem_st16(tm_s + lane_off + (uint32_t)(16 * half), pf);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     l += red_l[row] + red_l[128 + row];
-    // ---- O += P V: V rows are the MN-major operand (dims along MN in 64-dim
-    //      blocks 8 KB apart, keys along K in 8-key atoms 1 KB apart)
+    // ---- O += P V: P from TMEM (8 columns per 16 keys); V rows are the
+    //      MN-major operand (dims along MN in 64-dim blocks 8 KB apart, keys
+    //      along K in 8-key atoms 1 KB apart)
     if (threadIdx.x == 0) {
       constexpr uint32_t idesc = idesc_bf16(128, dh, true);
-      const uint64_t ad = sdesc_sw128(smem_u32(smem + L.p));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint64_t bd = sdesc_sw128_mn(smem_u32(smem + L.v[buf] + k * 2048), kChunk * 128, 1024);
-        mma_bf16(tm_o, ad + 2 * k, bd, idesc, (ci > 0 || k > 0) ? 1u : 0u);
+        mma_bf16_ts(tm_o, tm_s + (uint32_t)(8 * k), bd, idesc, (ci > 0 || k > 0) ? 1u : 0u);
       }
       mma_commit(bar_o);
     }
