@@ -422,7 +422,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const size_t unit = ((size_t)((b * a.Hkv + g) * a.q_tiles + qt)) * a.max_splits + sp;
     uint8_t* stg = smem + L.k[0];
     if constexpr (O16) {
-      // bf16 rows of O / l (half the bytes of fp32 partials): boxes of 64 columns
+      // bf16 rows of O / l (half the bytes of fp32 partials): boxes of 64
+      // columns, each stored by its half's first thread as soon as the half's
+      // four warps have staged it (the store overlaps the next box's staging)
       const float inv_l = 1.f / l;
 #pragma unroll 1
       for (int c0 = 64 * half; c0 < dh; c0 += 128) {
@@ -436,7 +438,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                          pack_bf16x2(v[8 * q + 2] * inv_l, v[8 * q + 3] * inv_l),
                          pack_bf16x2(v[8 * q + 4] * inv_l, v[8 * q + 5] * inv_l),
                          pack_bf16x2(v[8 * q + 6] * inv_l, v[8 * q + 7] * inv_l));
+        fence_proxy_async_smem();
+        if (half == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+        else asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (row == 0) tma_store_2d(&omap, box, c0, (int)(unit * 128));
       }
+      if (row == 0) bulk_commit();
     } else {
 #pragma unroll 1
       for (int c0 = 64 * half; c0 < dh; c0 += 128) {
@@ -453,15 +460,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     // the stored maximum is in the log2 domain of the scaled scores
     if (valid_row && half == 0) a.part_ml[unit * 128 + row] = make_float2(m_ref, l);
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      if constexpr (O16)
-        for (int bx = 0; bx < dh / 64; ++bx) tma_store_2d(&omap, stg + bx * (128 * 128), bx * 64, (int)(unit * 128));
-      else
+    if constexpr (O16) {
+      if (row == 0) bulk_wait_read_all();  // this half's stores have read the staging
+    } else {
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
         for (int bx = 0; bx < dh / 32; ++bx) tma_store_2d(&omap, stg + bx * (128 * 128), bx * 32, (int)(unit * 128));
-      bulk_commit();
-      bulk_wait_read_all();
+        bulk_commit();
+        bulk_wait_read_all();
+      }
     }
   }
   tc_fence_before();
