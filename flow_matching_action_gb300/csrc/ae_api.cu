@@ -435,6 +435,8 @@ ae_status bind_ranges(ae_ctx* c, int batch, const void* prefix_k, const void* pr
     const long rows = (long)c->d.L * total;
     cudaError_t e = ae::make_bf16_map(&c->bind.map_pk, prefix_k, rows, c->d.kvdim(), 64);
     if (e == cudaSuccess) e = ae::make_bf16_map(&c->bind.map_pv, prefix_v, rows, c->d.kvdim(), 64);
+    if (e == cudaSuccess) e = ae::make_kv3d_map(&c->bind.map_pk3, prefix_k, rows, c->d.kvdim(), c->d.dh);
+    if (e == cudaSuccess) e = ae::make_kv3d_map(&c->bind.map_pv3, prefix_v, rows, c->d.kvdim(), c->d.dh);
     if (e != cudaSuccess)
       return set_msg(c, AE_ERR_INVALID_ARG,
                      "prefix_k / prefix_v cannot be described for TMA (16-byte alignment needed)");

@@ -96,7 +96,7 @@ template <int DH>
 __device__ __forceinline__ bool chunk_codes(const AttnArgs& a, const CUtensorMap* kmap,
                                             const CUtensorMap* vmap, uint8_t* smem, const AttnSmem& L,
                                             uint64_t* bar_kv, int b, int g, int n_pre, int n_keys,
-                                            int c, int buf) {
+                                            int c, int buf, bool whole_rows) {
   constexpr int kdb = DH / 64;
   const int key0 = c * kChunk;
   const int nk = min(kChunk, n_keys - key0);
@@ -123,10 +123,17 @@ __device__ __forceinline__ bool chunk_codes(const AttnArgs& a, const CUtensorMap
     uint8_t* vs = smem + L.v[buf];
     mbar_arrive_expect_tx(&bar_kv[buf], 2u * kdb * kChunk * 128);
     const int row = a.layer_row0 + ix[0];
+    if (whole_rows) {
+      // K and V as one box each (the maps' 3-D views: 64 rows x DH columns land
+      // as DH / 64 swizzled [64 rows][128 B] blocks): two TMA issues, not 2 DH / 64
+      tma_load_3d_nohint(ks, kmap, &bar_kv[buf], 0, row, g * kdb);
+      tma_load_3d_nohint(vs, vmap, &bar_kv[buf], 0, row, g * kdb);
+    } else {
 #pragma unroll
-    for (int kb = 0; kb < kdb; ++kb) {
-      tma_load_2d_nohint(ks + kb * kChunk * 128, kmap, &bar_kv[buf], g * DH + kb * 64, row);
-      tma_load_2d_nohint(vs + kb * kChunk * 128, vmap, &bar_kv[buf], g * DH + kb * 64, row);
+      for (int kb = 0; kb < kdb; ++kb) {
+        tma_load_2d_nohint(ks + kb * kChunk * 128, kmap, &bar_kv[buf], g * DH + kb * 64, row);
+        tma_load_2d_nohint(vs + kb * kChunk * 128, vmap, &bar_kv[buf], g * DH + kb * 64, row);
+      }
     }
   }
   return contiguous;
@@ -177,7 +184,7 @@ __device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorM
                                               const CUtensorMap* vmap, uint8_t* smem,
                                               const AttnSmem& L, uint64_t* bar_kv, int b, int g,
                                               int n_pre, int n_keys, int c, int buf) {
-  const bool tma = chunk_codes<DH>(a, kmap, vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c, buf);
+  const bool tma = chunk_codes<DH>(a, kmap, vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c, buf, true);
   if (!tma) chunk_gather<DH>(a, smem, L, b, g, buf);
   return tma;
 }
@@ -187,7 +194,8 @@ __device__ __forceinline__ bool load_kv_chunk(const AttnArgs& a, const CUtensorM
 template <int DH, bool O16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-              const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+              const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap kmap3,
+              const __grid_constant__ CUtensorMap vmap3, const __grid_constant__ CUtensorMap omap,
               const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // keeps the shared address space
@@ -234,13 +242,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
+    prefetch_tensormap(&kmap3);
+    prefetch_tensormap(&vmap3);
   }
   if (warp == 0) {
     tmem_alloc(tmem_base_p, tcols);
     tmem_relinquish();
   }
   __syncthreads();
-  bool tma_cur = chunk_codes<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c_begin, 0);
+  // the first chunk loads while the preceding kernel finishes: boxes of 64
+  // columns; chunks inside the loop use the whole-row boxes (fewer issues on
+  // the critical path)
+  bool tma_cur = chunk_codes<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c_begin, 0, false);
   pdl_wait();
   if (!tma_cur) chunk_gather<DH>(a, smem, L, b, g, 0);
   // ---- Q tile by TMA: groups of a.q_box rows of the fold (q_box divides the
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     bool tma_next = false;
     const bool has_next = ci + 1 < n_my;
     if (has_next)
-      tma_next = load_kv_chunk<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c + 1, buf ^ 1);
+      tma_next = load_kv_chunk<DH>(a, &kmap3, &vmap3, smem, L, bar_kv, b, g, n_pre, n_keys, c + 1, buf ^ 1);
     int ok = 1;
     if (!tma_cur) {
       if (has_next && !tma_next) cp_async_wait<1>();
@@ -635,7 +648,7 @@ static unsigned combine_blocks(const AttnArgs& a) {
 }
 
 cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const CUtensorMap& omap_f32, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
+                           const CUtensorMap& kmap3, const CUtensorMap& vmap3, const CUtensorMap& omap_f32, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl) {
   attn_plan(a, sm_count);
   // bf16 rows of O / l halve the partials' bytes (store and combine)
@@ -647,9 +660,9 @@ cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, con
     constexpr bool O16 = decltype(o16_tag)::value;
     cudaError_t r;
     switch (a.dh) {
-      case 64: r = launch_k(k_attn_tc<64, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
-      case 128: r = launch_k(k_attn_tc<128, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
-      default: r = launch_k(k_attn_tc<256, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, omap, a); break;
+      case 64: r = launch_k(k_attn_tc<64, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, kmap3, vmap3, omap, a); break;
+      case 128: r = launch_k(k_attn_tc<128, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, kmap3, vmap3, omap, a); break;
+      default: r = launch_k(k_attn_tc<256, O16>, dim3(grid), dim3(kAttnThreads), smem, s, pdl, qmap, kmap, vmap, kmap3, vmap3, omap, a); break;
     }
     if (r != cudaSuccess) return r;
     return launch_k(k_attn_combine<O16>, dim3(combine_blocks(a)), dim3(32 * kCombineRows), 0, s, pdl, a, o);

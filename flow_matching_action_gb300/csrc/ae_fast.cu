@@ -109,6 +109,21 @@ cudaError_t fast_setup(ae_ctx* c) {
   return make_attn_o16_map(&c->map_attn_o16, c->attn_o, units, d.dh);
 }
 
+// bf16 [rows, kvdim] viewed as (64 columns, rows, kvdim / 64 column blocks): one box
+// of 64 rows x dh columns lands as dh / 64 blocks of [64 rows][128 B], 128-byte swizzled.
+cudaError_t make_kv3d_map(CUtensorMap* map, const void* ptr, long rows, long kvdim, int dh) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kvdim / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)kvdim * 2, 128};
+  cuuint32_t box[3] = {64, 64, (cuuint32_t)(dh / 64)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows) {
   return make_map(map, ptr, rows, cols, box_rows);
 }
@@ -280,7 +295,7 @@ int launch_step_fast(ae_ctx* c, const TimeTable& t, int step, float* x, cudaStre
       at.q_box = c->q_box_rows;
       // bf16 partials on the default path; callers' own scratch keeps fp32
       const bool o16_ok = attn_scratch == nullptr;
-      ck(launch_attn_tc(c->map_qtile, c->bind.map_pk, c->bind.map_pv,
+      ck(launch_attn_tc(c->map_qtile, c->bind.map_pk, c->bind.map_pv, c->bind.map_pk3, c->bind.map_pv3,
                         attn_scratch ? attn_scratch->omap : c->map_attn_o, o16_ok ? &c->map_attn_o16 : nullptr, at, o,
                         sm, s, pdl));
       n += 2;

@@ -51,6 +51,7 @@ struct BindState {
   int64_t total_rows = 0;               // rows per layer of pk / pv
   int max_phys_rows = 0;                // longest request of the binding
   CUtensorMap map_pk, map_pv;           // bf16 path: TMA views of pk / pv, boxes 64 rows x 64
+  CUtensorMap map_pk3, map_pv3;         // the same as boxes of 64 rows x head_dim (all column blocks)
   std::vector<int> lens;                // physical rows of every request
 };
 
@@ -327,10 +328,12 @@ cudaError_t attn_kernel_setup();
 // omap16: bf16 view of the same partials (make_attn_o16_map), or nullptr (fp32
 // partials through omap).
 cudaError_t launch_attn_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const CUtensorMap& kmap3, const CUtensorMap& vmap3,
                            const CUtensorMap& omap, const CUtensorMap* omap16, AttnArgs a, bf16* o, int sm_count,
                            cudaStream_t s, bool pdl);
 cudaError_t make_bf16_map(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows);
 // fp32 [d2][d1][d0] view with boxes {32, box1, 1}, 128-byte swizzle (split-K partials)
+cudaError_t make_kv3d_map(CUtensorMap* map, const void* ptr, long rows, long kvdim, int dh);
 cudaError_t make_f32_3d_map(CUtensorMap* map, const void* ptr, long d0, long d1, long d2, int box1);
 cudaError_t make_attn_o_map(CUtensorMap* map, float* part_o, size_t units, int dh);
 // bf16 [units * 128, dh] view of part_o, boxes of 128 rows x 64 columns, 128-byte swizzle

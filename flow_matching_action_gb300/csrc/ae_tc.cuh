@@ -168,6 +168,15 @@ __device__ __forceinline__ void tma_load_2d_nohint(void* dst, const CUtensorMap*
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_nohint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                                   int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // Prefetch one box of a tiled tensor into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(c0),
