@@ -254,6 +254,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // columns; chunks inside the loop use the whole-row boxes (fewer issues on
   // the critical path)
   bool tma_cur = chunk_codes<DH>(a, &kmap, &vmap, smem, L, bar_kv, b, g, n_pre, n_keys, c_begin, 0, false);
+  // bit i: buffer i has a TMA copy in flight (thread 0's view; drained on
+  // the way out after a failure)
+  uint32_t kv_pending = tma_cur ? 1u : 0u;
   pdl_wait();
   if (!tma_cur) chunk_gather<DH>(a, smem, L, b, g, 0);
   // ---- Q tile by TMA: groups of a.q_box rows of the fold (q_box divides the
@@ -291,28 +294,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   float* red_l = red_m + 2 * 128;                                         // [2][128]
   float m_ref = -INFINITY, l = 0.f;
   bool failed = false;
-  uint32_t kv_phase[2] = {0u, 0u};  // used by thread 0 only
+  int fail_at = 0;                  // 1: S = Q K^T in flight, 2: P V in flight
+  uint32_t fail_par = 0u;           // parity of that MMA's commit
+  uint32_t kv_phase = 0u;           // bit i: parity of buffer i's next load (thread 0)
+  bool q_pending = true;
 
   for (int ci = 0; ci < n_my; ++ci) {
     const int c = c_begin + ci;
     const int buf = ci & 1;
     const int nk = min(kChunk, n_keys - c * kChunk);
-    // start the next chunk into the other buffer (its last reader, the
-    // previous chunk's P V, completed before this iteration began)
-    bool tma_next = false;
     const bool has_next = ci + 1 < n_my;
-    if (has_next)
-      tma_next = load_kv_chunk<DH>(a, &kmap3, &vmap3, smem, L, bar_kv, b, g, n_pre, n_keys, c + 1, buf ^ 1);
     int ok = 1;
     if (!tma_cur) {
-      if (has_next && !tma_next) cp_async_wait<1>();
-      else cp_async_wait<0>();
+      cp_async_wait<0>();  // the next chunk's copies start only after S is issued
       fence_proxy_async_smem();
     } else if (threadIdx.x == 0) {
-      ok = mbar_wait(&bar_kv[buf], kv_phase[buf], abort_flag, a.status) ? 1 : 0;
-      kv_phase[buf] ^= 1u;
+      ok = mbar_wait(&bar_kv[buf], (kv_phase >> buf) & 1u, abort_flag, a.status) ? 1 : 0;
+      if (ok) {
+        kv_phase ^= 1u << buf;
+        kv_pending &= ~(1u << buf);
+      }
     }
-    if (ci == 0 && threadIdx.x == 0 && ok) ok = mbar_wait(bar_q, 0, abort_flag, a.status) ? 1 : 0;
+    if (ci == 0 && threadIdx.x == 0 && ok) {
+      ok = mbar_wait(bar_q, 0, abort_flag, a.status) ? 1 : 0;
+      if (ok) q_pending = false;
+    }
     tc_fence_before();
     if (__syncthreads_or(!ok)) {
       failed = true;
@@ -332,10 +338,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       mma_commit(bar_s);
     }
+    // the next chunk starts loading into the other buffer while S runs: its
+    // last readers, the previous chunk's S and P V, have completed (their
+    // waits came before this point), and neither the gather codes' global
+    // reads nor the copies' issue sit between P V and this chunk's S
+    bool tma_next = false;
+    if (has_next) {
+      tma_next = load_kv_chunk<DH>(a, &kmap3, &vmap3, smem, L, bar_kv, b, g, n_pre, n_keys, c + 1, buf ^ 1);
+      if (tma_next) kv_pending |= 1u << (buf ^ 1);
+    }
     ok = 1;
     if (lane == 0) ok = mbar_wait(bar_s, (uint32_t)ci & 1u, abort_flag, a.status) ? 1 : 0;
     if (__syncthreads_or(!ok)) {
       failed = true;
+      fail_at = 1;
+      fail_par = (uint32_t)ci & 1u;
       break;
     }
     tc_fence_after();
@@ -414,6 +431,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) ok = mbar_wait(bar_o, (uint32_t)ci & 1u, abort_flag, a.status) ? 1 : 0;
     if (__syncthreads_or(!ok)) {
       failed = true;
+      fail_at = 2;
+      fail_par = (uint32_t)ci & 1u;
       break;
     }
     tc_fence_after();
@@ -421,10 +440,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   cp_async_wait<0>();
   if (failed && threadIdx.x == 0) {
-    // no TMA copy may still be writing shared memory when the CTA exits
-    mbar_wait(bar_q, 0, abort_flag, a.status);
-    mbar_wait(&bar_kv[0], kv_phase[0], abort_flag, a.status);
-    mbar_wait(&bar_kv[1], kv_phase[1], abort_flag, a.status);
+    // no TMA copy may still be writing shared memory, nor an MMA tensor
+    // memory, when the CTA exits: bounded waits that hold after an abort
+    if (q_pending) mbar_drain(bar_q, 0, a.status);
+    for (int i = 0; i < 2; ++i)
+      if ((kv_pending >> i) & 1u) mbar_drain(&bar_kv[i], (kv_phase >> i) & 1u, a.status);
+    if (fail_at == 1) mbar_drain(bar_s, fail_par, a.status);
+    if (fail_at == 2) mbar_drain(bar_o, fail_par, a.status);
   }
   __syncthreads();  // every chunk buffer is free: reuse K/V space to stage O
   if (!failed) {

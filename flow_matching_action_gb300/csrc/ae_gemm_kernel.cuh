@@ -571,10 +571,11 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
           tma_load_2d_nohint(smB + ((size_t)s * SW + j) * btile, &amap, &full[s], kc + 64 * j,
                              a.act_row0 + z * a.z_act_rows + t0);
       }
-      // drain: no copy may still be in flight when the CTA exits
+      // drain: no copy may still be in flight when the CTA exits (stages
+      // already consumed pass at once; the wait holds even after an abort)
       for (int j = it - S > 0 ? it - S : 0; j < it; ++j) {
-        mbar_wait(&full[j % S], (uint32_t)(j / S) & 1u, abort_flag, a.status);
-        if (WF) mbar_wait(&wfull[j % S], (uint32_t)(j / S) & 1u, abort_flag, a.status);
+        mbar_drain(&full[j % S], (uint32_t)(j / S) & 1u, a.status);
+        if (WF) mbar_drain(&wfull[j % S], (uint32_t)(j / S) & 1u, a.status);
       }
     }
   } else if (warp == 1) {
@@ -896,7 +897,7 @@ __global__ void __launch_bounds__(kThreadsFor(EW), 1)
   __syncthreads();
   if (warp == 1) {
     // the last commit tracks every MMA this CTA issued: wait for it before freeing TMEM
-    if (*abort_flag && lane == 0) mbar_wait(tmem_full, 0, abort_flag, a.status);
+    if (*abort_flag && lane == 0) mbar_drain(tmem_full, 0, a.status);
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_d, tmem_cols);

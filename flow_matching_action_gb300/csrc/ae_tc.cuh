@@ -117,6 +117,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait for a copy or MMA this CTA issued, used on the way out after a
+// failure: unlike mbar_wait it does not give up when the abort flag is raised
+// (the copy must have landed before the CTA's shared memory or tensor memory
+// is released), only when the budget runs out.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, int* status) {
+  volatile int keep_waiting = 0;
+  return mbar_wait(bar, parity, &keep_waiting, status);
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Wait until the preceding kernel of the stream has completed and its memory
 // is visible (a no-op when the kernel was launched without the attribute).
