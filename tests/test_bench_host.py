@@ -1,7 +1,10 @@
 """Host-side pieces of bench.py that need no GPU: the digest that ties the
-committed DRAM-traffic counters to the CUDA sources they were taken on."""
+committed DRAM-traffic counters to the CUDA sources they were taken on, and
+the algorithmic bytes and FLOPs the roofline fractions divide."""
 import json
 import os
+
+import numpy as np
 
 import bench
 
@@ -49,3 +52,35 @@ def test_fp8_traffic_and_algorithmic_bytes():
     with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
         rec = json.load(f)["bytes_per_flow_step"]
     assert 311e6 < rec["pi05_b1_fp8"] < 0.55 * rec["pi05_b1"]
+
+
+def test_flop_model_equals_torch_flop_counter():
+    """The FLOPs the tensor roofline divides by (the block Linears of every
+    token plus Q K^T and P V over each request's valid prefix rows and its own
+    action rows) equal what torch's FLOP counter counts when the same
+    contractions of one flow step run as plain torch ops, for a ragged batch
+    with an empty prefix in it."""
+    import torch
+    import torch.nn.functional as F
+    from torch.utils.flop_counter import FlopCounterMode
+
+    from flow_matching_action_gb300 import synth
+    d = synth.TINY
+    w = synth.make_weights(d, 0)
+    T = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    H, hq, hkv, dh = d.horizon, d.n_q_heads, d.n_kv_heads, d.head_dim
+    n_valid = [40, 7, 0]
+    with FlopCounterMode(display=False) as fc:
+        for n in n_valid:
+            h = torch.ones(H, d.width, dtype=torch.float64)
+            prefix = torch.ones(n, d.kv_dim, dtype=torch.float64)
+            for l in range(d.layers):
+                q = F.linear(h, T(w["wq"][l])).reshape(H, hq, dh).transpose(0, 1)
+                k = torch.cat([prefix, F.linear(h, T(w["wk"][l]))]).reshape(n + H, hkv, dh).transpose(0, 1)
+                v = torch.cat([prefix, F.linear(h, T(w["wv"][l]))]).reshape(n + H, hkv, dh).transpose(0, 1)
+                p = torch.softmax(torch.matmul(q, k.transpose(-1, -2)), dim=-1)
+                o = torch.matmul(p, v).transpose(0, 1).reshape(H, hq * dh)
+                h = h + F.linear(o, T(w["wo"][l]))
+                m = F.gelu(F.linear(h, T(w["wg"][l])), approximate="tanh") * F.linear(h, T(w["wu"][l]))
+                h = h + F.linear(m, T(w["wd"][l]))
+    assert bench.algorithmic(d, n_valid)[1] == fc.get_total_flops()
