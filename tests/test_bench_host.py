@@ -84,3 +84,21 @@ def test_flop_model_equals_torch_flop_counter():
                 m = F.gelu(F.linear(h, T(w["wg"][l])), approximate="tanh") * F.linear(h, T(w["wu"][l]))
                 h = h + F.linear(m, T(w["wd"][l]))
     assert bench.algorithmic(d, n_valid)[1] == fc.get_total_flops()
+
+
+def test_byte_model_counts_the_block_linears_and_valid_prefix_rows():
+    """The HBM roofline's bytes are the block Linears the weight generator
+    makes (7 per layer, 2 bytes an element; 1 byte plus a 4-byte factor per
+    output row with e4m3 codes) and the K and V rows each request reads at
+    every layer: its valid prefix rows, not the masked or padded ones."""
+    from flow_matching_action_gb300 import synth
+    d = synth.TINY
+    w = synth.make_weights(d, 0)
+    block = [np.asarray(a) for name in ("wq", "wk", "wv", "wo", "wg", "wu", "wd") for a in w[name]]
+    assert len(block) == 7 * d.layers
+    wl = synth.tiny_variant("masked")  # a masked slot inside the prefix
+    n_valid = [int(m.sum()) for m in np.split(wl.mask, np.asarray(wl.cu_lens[1:-1]))]
+    assert sum(n_valid) < int(wl.cu_lens[-1])
+    kv = sum(d.layers * 2 * n * d.kv_dim * 2 for n in n_valid)
+    assert bench.algorithmic(d, n_valid)[0] == sum(a.size for a in block) * 2 + kv
+    assert bench.algorithmic(d, n_valid, fp8_weights=True)[0] == sum(a.size + 4 * a.shape[0] for a in block) + kv
